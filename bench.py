@@ -1,0 +1,506 @@
+#!/usr/bin/env python
+"""Benchmark: split-KV decode attention on one GB300, one JSON line on stdout.
+
+Workload (one layer of a 3B Llama-style model): B=1, Hq=24, Hkv=8, D=128, bf16 KV cache
+of Smax=32768 rows, attended length 32768, automatic split. One *call* is the hot path
+for one decode token: append the new key/value row (td_kv_append) and attend
+(td_decode_attn). One *step* is a batch of R such calls, each on its own query and new
+row, rotating over C copies of the cache so that every call's 134 MB of KV reads come from
+HBM (C * 134 MB > 4x L2), captured once as a CUDA graph and replayed.
+
+  value      KV-read GB/s = KV bytes attended / device time, inputs resident in HBM
+  e2e        the same through the Python API with host buffers: every call copies its q
+             and new rows from pinned host memory and reads its output back
+  roofline   the attention kernel timed alone (graph of R attention launches), against the
+             measured HBM copy bandwidth
+  cpu_baseline  the CPU oracle (fp64, all host cores) on a bounded sample of the workload
+  sweep      the other workloads' points (us/call, GB/s), attention kernel only
+
+``--impl reference`` times the CPU oracle as the reference arm instead.
+Under torchrun every rank runs the same workload on its own GPU (replicas; no collective
+on the data path) and rank 0 prints value = all ranks' bytes / slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from decode_attention_split_gb300.workloads import WORKLOADS, kv_read_bytes, make_case, to_numpy  # noqa: E402
+
+METRIC = "decode-attn achieved KV-read GB/s (% of HBM peak) and µs/call, B=1 at 4k–32k ctx"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="td", choices=["td", "reference"])
+    ap.add_argument("--calls-per-step", type=int, default=1000)
+    ap.add_argument("--workload", default="llama3b")
+    ap.add_argument("--seq-len", type=int, default=32768)
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--profile-launches", type=int, default=0,
+                    help="profiling mode: W warm-up calls then this many plain launches, no graphs, no JSON extras")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------------------ environment
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return json.load(f), "measured"
+    except (OSError, ValueError):
+        return {"hbm_gbs": FALLBACK_HBM_GBS}, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    src = os.path.join(ROOT, "decode_attention_split_gb300", "csrc")
+    for name in sorted(os.listdir(src)):
+        with open(os.path.join(src, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    with open(os.path.join(ROOT, "include", "td.h"), "rb") as f:
+        h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, workload_key: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on the current kernel source."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    ent = rec.get(kernel, {}).get(workload_key)
+    if not ent or ent.get("source_hash") != kernel_source_hash():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 100 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device: torch.device):
+        self.proc = None
+        self.lines = []
+        sel = []
+        try:
+            uuid = str(torch.cuda.get_device_properties(device).uuid)
+            sel = ["-i", uuid if uuid.startswith("GPU-") else "GPU-" + uuid]
+        except Exception:  # noqa: BLE001
+            sel = []
+        self.cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100", *sel]
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(self.cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+        return False
+
+    def summary(self):
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        sm, mx, pw, reasons = [], [], [], set()
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+                pw.append(float(parts[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        # samples under load: the busiest half by power
+        order = sorted(range(len(sm)), key=lambda i: pw[i], reverse=True)
+        loaded = [sm[i] for i in order[:max(1, len(order) // 2)]]
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm), "power_w_max": max(pw)}
+
+
+# ---------------------------------------------------------------------------- reference arm
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    import oracle
+    orc = oracle.load()
+    w = WORKLOADS[args.workload]
+    case = make_case(w, seq_len=args.seq_len)
+    qn, kn, vn, sn = (to_numpy(x) for x in (case.q, case.k_cache, case.v_cache, case.seq_lens))
+    bytes_call = kv_read_bytes(w, args.seq_len)
+    for _ in range(args.warmup):
+        orc.attention(qn, kn, vn, sn, case.scale)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        orc.attention(qn, kn, vn, sn, case.scale)
+    dt = time.perf_counter() - t0
+    gbs = bytes_call * args.steps / dt / 1e9
+    cfg = workload_config(w, args.seq_len, None, None)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": cfg,
+        "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": orc.num_threads, "kind": "oracle",
+                         "sample": f"{args.steps} full oracle calls (24 heads x {args.seq_len} keys), fp64"},
+        "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------------------- our arm
+
+def workload_config(w, L, R, C):
+    cfg = {
+        "workload": f"{w.name} decode attention: B={w.B} Hq={w.Hq} Hkv={w.Hkv} D={w.D} Smax={w.Smax} "
+                    f"seq_len={L} {w.dtype}, split auto",
+        "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D, "Smax": w.Smax, "seq_len": L, "split": "auto",
+        "kv_bytes_per_call": kv_read_bytes(w, L),
+        "step": "R calls, each kv_append of 1 token + decode attention, one CUDA graph replay",
+    }
+    if R is not None:
+        cfg["calls_per_step"] = R
+    if C is not None:
+        cfg["l2"] = (f"inputs larger than L2: each call reads {kv_read_bytes(w, L) / 1e6:.1f} MB of KV and "
+                     f"calls rotate over {C} cache copies")
+    return cfg
+
+
+def rotating_copies(src: torch.Tensor, n: int) -> torch.Tensor:
+    out = torch.empty((n,) + tuple(src.shape), dtype=src.dtype, device=src.device)
+    out.copy_(src.unsqueeze(0).expand_as(out))
+    return out
+
+
+def time_graph(graph, stream, reps, warm=2):
+    """Replays (which launch on the current stream) and events, all on `stream`; returns ms."""
+    with torch.cuda.stream(stream):
+        for _ in range(warm):
+            graph.replay()
+        stream.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            graph.replay()
+        e1.record(stream)
+    e1.synchronize()
+    return e0.elapsed_time(e1)
+
+
+def sweep_point(td, name, L, dev, l2_bytes, peak, budget_calls=200):
+    """Attention kernel alone on one workload point: graph of R launches over rotating caches."""
+    w = WORKLOADS[name]
+    case = make_case(w, seq_len=L if not w.ragged else None)
+    bytes_call = kv_read_bytes(w, case.seq_lens.tolist())
+    C = max(2, math.ceil(4 * l2_bytes / bytes_call))
+    per_copy = case.k_cache.numel() * case.k_cache.element_size() * 2
+    C = min(C, max(2, int(48e9 // per_copy)))
+    kc = rotating_copies(case.k_cache.to(dev), C)
+    vc = rotating_copies(case.v_cache.to(dev), C)
+    q = case.q.to(dev)
+    sl = case.seq_lens.to(dev)
+    R = max(C, budget_calls)
+    out = torch.empty_like(q)
+    ws = td.make_workspace(w.B, w.Hq, w.Hkv, w.Smax, w.D, w.T, 0, device=dev)
+    s = torch.cuda.Stream(dev)
+
+    def calls():
+        for i in range(R):
+            c = i % C
+            if w.T == 1:
+                td.td_decode_attn(q[:, :, 0], kc[c], vc[c], sl, case.scale, 0, out=out[:, :, 0], workspace=ws,
+                                  stream=s)
+            else:
+                td.td_verify_attn(q, kc[c], vc[c], sl, case.scale, 0, out=out, workspace=ws, stream=s)
+
+    with torch.cuda.stream(s):
+        calls()
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        calls()
+    ms = min(time_graph(g, s, 3) for _ in range(3))
+    us = ms * 1e3 / (3 * R)
+    gbs = bytes_call / (us * 1e-6) / 1e9
+    del kc, vc
+    torch.cuda.empty_cache()
+    return {"workload": name, "seq_len": L if not w.ragged else "ragged", "us_per_call": round(us, 3),
+            "kv_gbs": round(gbs, 1), "frac_of_measured_hbm": round(gbs / peak, 4), "kv_bytes": bytes_call,
+            "cache_copies": C}
+
+
+def run_td(args, world, rank, local):
+    from decode_attention_split_gb300 import build
+    build.build()
+    import decode_attention_split_gb300 as td
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    w = WORKLOADS[args.workload]
+    L = args.seq_len
+    case = make_case(w, seq_len=L)
+    bytes_call = kv_read_bytes(w, L)
+    props = torch.cuda.get_device_properties(dev)
+    l2 = props.L2_cache_size
+    C = max(2, math.ceil(4 * l2 / bytes_call))
+    R = max(args.calls_per_step, C)
+    peaks, peak_kind = measured_peaks()
+    peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
+
+    kc = rotating_copies(case.k_cache.to(dev), C)
+    vc = rotating_copies(case.v_cache.to(dev), C)
+    gen = torch.Generator().manual_seed(1)
+    qh = torch.randn(R, w.B, w.Hq, w.D, generator=gen).to(torch.bfloat16)
+    knh = torch.randn(R, w.B, w.Hkv, 1, w.D, generator=gen).to(torch.bfloat16)
+    vnh = torch.randn(R, w.B, w.Hkv, 1, w.D, generator=gen).to(torch.bfloat16)
+    q, kn, vn = qh.to(dev), knh.to(dev), vnh.to(dev)
+    out = torch.empty_like(q)
+    sl_pre = torch.full((w.B,), L - 1, dtype=torch.int32, device=dev)  # new row goes to position L-1
+    sl_post = torch.full((w.B,), L, dtype=torch.int32, device=dev)
+    ws = td.make_workspace(w.B, w.Hq, w.Hkv, w.Smax, w.D, 1, 0, device=dev)
+    s = torch.cuda.Stream(dev)
+
+    def calls(append=True):
+        for i in range(R):
+            c = i % C
+            if append:
+                td.td_kv_append(kn[i], vn[i], kc[c], vc[c], sl_pre, advance=False, stream=s)
+            td.td_decode_attn(q[i], kc[c], vc[c], sl_post, case.scale, 0, out=out[i], workspace=ws, stream=s)
+
+    if args.profile_launches:
+        with torch.cuda.stream(s):
+            for _ in range(args.warmup):
+                td.td_decode_attn(q[0], kc[0], vc[0], sl_post, case.scale, 0, out=out[0], workspace=ws, stream=s)
+            for i in range(args.profile_launches):
+                c = i % C
+                td.td_kv_append(kn[i], vn[i], kc[c], vc[c], sl_pre, advance=False, stream=s)
+                td.td_decode_attn(q[i], kc[c], vc[c], sl_post, case.scale, 0, out=out[i], workspace=ws, stream=s)
+        s.synchronize()
+        print(json.dumps({"profile_launches": args.profile_launches, "ok": True}))
+        return
+
+    with torch.cuda.stream(s):
+        calls()
+    s.synchronize()
+    g_step = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_step, stream=s):
+        calls(append=True)
+    g_attn = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_attn, stream=s):
+        calls(append=False)
+
+    with torch.cuda.stream(s):  # graph replays launch on the current stream
+        for _ in range(args.warmup):
+            g_step.replay()
+    s.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(dev) as clk:
+        with torch.cuda.stream(s):
+            e0.record(s)
+            for _ in range(args.steps):
+                g_step.replay()
+            e1.record(s)
+        e1.synchronize()
+        torch.cuda.synchronize()
+        ms_attn = time_graph(g_attn, s, args.steps, warm=2)
+    ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([ms, ms_attn], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms, ms_attn = float(t[0]), float(t[1])
+        torch.distributed.barrier()
+
+    # correctness of what was timed: call 0 of the last replay against the oracle
+    checked = None
+    if rank == 0:
+        import numpy as np
+        import oracle
+        ek = to_numpy(case.k_cache).copy()
+        ev = to_numpy(case.v_cache).copy()
+        last = ((R - 1) // C) * C  # the last call that appended into copy 0 before out[0] was computed
+        ek[:, :, L - 1] = to_numpy(knh[last])[:, :, 0]
+        ev[:, :, L - 1] = to_numpy(vnh[last])[:, :, 0]
+        ref, _, _ = oracle.load().attention(to_numpy(qh[0]), ek, ev, np.array([L], np.int32), case.scale)
+        got = out[0].double().cpu().numpy()
+        checked = bool(np.all(np.abs(got - ref) <= 2e-2 + 1e-2 * np.abs(ref)))
+
+    total_calls = args.steps * R
+    value = world * total_calls * bytes_call / (ms * 1e-3) / 1e9
+    us_attn = ms_attn * 1e3 / total_calls
+    achieved = bytes_call / (us_attn * 1e-6) / 1e9
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(td, args, w, case, kc, vc, C, R, sl_pre, sl_post, ws, dev, bytes_call, world)
+
+    if rank != 0:
+        return
+    cpu = None if (args.no_cpu or world > 1) else cpu_baseline(case, w, L, args.cpu_seconds)
+    sweep = None
+    if not args.no_sweep:
+        del kc, vc
+        torch.cuda.empty_cache()
+        sweep = []
+        for name in ("smollm2_360m", "llama3b"):
+            for Ls in WORKLOADS[name].seq_lens:
+                sweep.append(sweep_point(td, name, Ls, dev, l2, peak))
+        sweep.append(sweep_point(td, "ragged8", None, dev, l2, peak))
+        sweep.append(sweep_point(td, "verify6", 16390, dev, l2, peak))
+    traffic = recorded_traffic("split_attn_kernel", f"{w.name}:{L}")
+    line = {
+        "metric": METRIC,
+        "value": round(value, 1),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms / args.steps, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) q/k/v, 1% keys x8; no model weights)",
+        "config": dict(workload_config(w, L, R, C), parallelism=f"replicas x{world}" if world > 1 else "1 GPU"),
+        "us_per_call": round(ms * 1e3 / total_calls, 3),
+        "frac_of_measured_hbm": round(value / world / peak, 4),
+        "checked_against_oracle": checked,
+        "clocks": clk.summary(),
+        "gpu_launches": 2 * total_calls,
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "kernel": "split_attn_kernel<bf16,128,4> (fused split + merge), timed alone",
+                     "us_per_launch": round(us_attn, 3), "peak_kind": f"hbm_gbs of {peak_kind}",
+                     "algorithmic_bytes_per_launch": bytes_call},
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+        "sweep": sweep,
+        "kernel_source": kernel_source_hash(),
+        "device": props.name,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_e2e(td, args, w, case, kc, vc, C, R, sl_pre, sl_post, ws, dev, bytes_call, world):
+    """Through the public Python API with host buffers: per call H2D of q and the new rows, D2H of out."""
+    steps = max(1, min(args.steps, 10))
+    gen = torch.Generator().manual_seed(2)
+    qh = torch.randn(R, w.B, w.Hq, w.D, generator=gen).to(torch.bfloat16).pin_memory()
+    knh = torch.randn(R, w.B, w.Hkv, 1, w.D, generator=gen).to(torch.bfloat16).pin_memory()
+    vnh = torch.randn(R, w.B, w.Hkv, 1, w.D, generator=gen).to(torch.bfloat16).pin_memory()
+    outh = torch.empty(R, w.B, w.Hq, w.D, dtype=torch.bfloat16).pin_memory()
+    qd = torch.empty(w.B, w.Hq, w.D, dtype=torch.bfloat16, device=dev)
+    knd = torch.empty(w.B, w.Hkv, 1, w.D, dtype=torch.bfloat16, device=dev)
+    vnd = torch.empty_like(knd)
+    outd = torch.empty_like(qd)
+    s = torch.cuda.Stream(dev)
+
+    def one_step():
+        with torch.cuda.stream(s):
+            for i in range(R):
+                c = i % C
+                qd.copy_(qh[i], non_blocking=True)
+                knd.copy_(knh[i], non_blocking=True)
+                vnd.copy_(vnh[i], non_blocking=True)
+                td.td_kv_append(knd, vnd, kc[c], vc[c], sl_pre, advance=False, stream=s)
+                td.td_decode_attn(qd, kc[c], vc[c], sl_post, case.scale, 0, out=outd, workspace=ws, stream=s)
+                outh[i].copy_(outd, non_blocking=True)
+
+    one_step()
+    s.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    for _ in range(steps):
+        one_step()
+    e1.record(s)
+    e1.synchronize()
+    ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t[0])
+    per_call_in = (qh[0].numel() + knh[0].numel() + vnh[0].numel()) * 2
+    return {"value": round(world * steps * R * bytes_call / (ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+            "h2d_bytes_per_step": R * per_call_in, "d2h_bytes_per_step": R * outh[0].numel() * 2,
+            "steps": steps, "us_per_call": round(ms * 1e3 / (steps * R), 3),
+            "path": "python binding td_kv_append + td_decode_attn, pinned host q/new rows in, out back"}
+
+
+def cpu_baseline(case, w, L, seconds):
+    import oracle
+    orc = oracle.load()
+    qn, kn, vn, sn = (to_numpy(x) for x in (case.q, case.k_cache, case.v_cache, case.seq_lens))
+    n, t0 = 0, time.perf_counter()
+    while n < 3 or time.perf_counter() - t0 < seconds:
+        orc.attention(qn, kn, vn, sn, case.scale)
+        n += 1
+    dt = (time.perf_counter() - t0) / n
+    return {"value": round(kv_read_bytes(w, L) / dt / 1e9, 3), "unit": "GB/s", "cores": orc.num_threads,
+            "kind": "oracle", "sample": f"{n} full calls (B=1, 24 heads x {L} keys, fp64), {dt * 1e3:.1f} ms each"}
+
+
+def main():
+    args = parse()
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        return
+    run_td(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,205 @@
+"""Python binding of the td C ABI (include/td.h), with the same function names.
+
+Argument marshalling only: shapes and pointers are read off torch tensors, outputs and the
+workspace are allocated with torch when the caller does not pass them, and every step of
+the computation runs in the CUDA library. Nothing falls back to another implementation:
+without the built library, or with tensors off the GPU, the calls raise.
+
+For CUDA-graph capture pass ``out`` (and ``lse``), ``workspace`` and ``stream`` explicitly
+and warm the call up once outside the capture.
+"""
+from __future__ import annotations
+
+import math
+import threading
+
+import torch
+
+from ._lib import check, lib
+
+TD_F32, TD_BF16 = 0, 1
+# bits a call ORs into dev_status (see td.h)
+DEV_SEQLEN_CLAMPED = 1
+DEV_APPEND_OVERFLOW = 2
+DEV_VERIFY_SHORT = 4
+DEV_NEGATIVE_SEQLEN = 8
+DEV_WAIT_TIMEOUT = 16
+DEV_WORKSPACE_DIRTY = 32
+
+_ws_lock = threading.Lock()
+_ws_cache: dict[tuple[int, int], torch.Tensor] = {}
+
+
+def _code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return TD_F32
+    if t.dtype == torch.bfloat16:
+        return TD_BF16
+    raise TypeError(f"td supports float32 and bfloat16 tensors, got {t.dtype}")
+
+
+def _cuda(*ts: torch.Tensor | None) -> torch.device:
+    dev = None
+    for t in ts:
+        if t is None:
+            continue
+        if not t.is_cuda:
+            raise ValueError("td kernels take CUDA tensors")
+        if not t.is_contiguous():
+            raise ValueError("td kernels take contiguous tensors")
+        if dev is None:
+            dev = t.device
+        elif t.device != dev:
+            raise ValueError("all tensors must be on one CUDA device")
+    return dev
+
+
+def _ptr(t: torch.Tensor | None):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream, device) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def td_decode_workspace_bytes(B: int, Hq: int, Hkv: int, Smax: int, D: int, q_len: int = 1, split: int = 0) -> int:
+    """Workspace bytes td_decode_attn / td_verify_attn need on the current device (0 = invalid)."""
+    return int(lib().td_decode_workspace_bytes(B, Hq, Hkv, Smax, D, q_len, split))
+
+
+def make_workspace(B, Hq, Hkv, Smax, D, q_len=1, split=0, device=None) -> torch.Tensor:
+    """A zero-filled workspace for a stream of calls with exactly these shape arguments."""
+    device = torch.device(device or "cuda")
+    with torch.cuda.device(device):
+        n = td_decode_workspace_bytes(B, Hq, Hkv, Smax, D, q_len, split)
+    if n == 0:
+        raise ValueError("invalid shapes for td_decode_workspace_bytes")
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+_WS_CACHE_MAX = 32
+
+
+def _cached_workspace(nbytes: int, device: torch.device, stream_ptr: int, shape_key: tuple) -> torch.Tensor:
+    """A zero-filled workspace per (device, stream, call shape).
+
+    The library leaves the counter area of a workspace zero only for its own layout, and the
+    layout follows the call's shape arguments, so a workspace is never shared across shapes."""
+    key = (device.index, stream_ptr) + shape_key
+    with _ws_lock:
+        ws = _ws_cache.pop(key, None)
+        if ws is None or ws.numel() < nbytes:
+            ws = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=device)
+        _ws_cache[key] = ws  # most recently used last
+        while len(_ws_cache) > _WS_CACHE_MAX:
+            _ws_cache.pop(next(iter(_ws_cache)))
+        return ws
+
+
+def td_kv_append(k_new, v_new, k_cache, v_cache, seq_lens, advance: bool = True, dev_status=None,
+                 stream=None) -> None:
+    """Write k_new/v_new [B,Hkv,T,D] into the caches [B,Hkv,Smax,D] at rows seq_lens[b].."""
+    dev = _cuda(k_new, v_new, k_cache, v_cache, seq_lens, dev_status)
+    B, Hkv, T, D = k_new.shape
+    Smax = k_cache.shape[2]
+    if v_new.shape != k_new.shape or k_cache.shape != (B, Hkv, Smax, D) or v_cache.shape != k_cache.shape:
+        raise ValueError("shape mismatch between new rows and caches")
+    if not (k_new.dtype == v_new.dtype == k_cache.dtype == v_cache.dtype):
+        raise TypeError("new rows and caches must share a dtype")
+    if seq_lens.dtype != torch.int32 or seq_lens.shape != (B,):
+        raise TypeError("seq_lens must be int32 [B]")
+    with torch.cuda.device(dev):
+        st = lib().td_kv_append(_code(k_cache), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
+                                _ptr(seq_lens), B, Hkv, T, Smax, D, int(bool(advance)), _ptr(dev_status),
+                                _stream(stream, dev))
+    check("td_kv_append", st)
+
+
+def _attn(name, q4, k_cache, v_cache, seq_lens, scale, split, out, lse, workspace, dev_status, stream):
+    dev = _cuda(q4, k_cache, v_cache, seq_lens, out, lse, workspace, dev_status)
+    B, Hq, T, D = q4.shape
+    _, Hkv, Smax, Dk = k_cache.shape
+    if k_cache.shape[0] != B or Dk != D or v_cache.shape != k_cache.shape:
+        raise ValueError("q and cache shapes disagree")
+    if not (q4.dtype == k_cache.dtype == v_cache.dtype):
+        raise TypeError("q and caches must share a dtype")
+    if seq_lens.dtype != torch.int32 or seq_lens.shape != (B,):
+        raise TypeError("seq_lens must be int32 [B]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    with torch.cuda.device(dev):
+        sp = _stream(stream, dev)
+        if workspace is None:
+            need = td_decode_workspace_bytes(B, Hq, Hkv, Smax, D, T, split)
+            workspace = _cached_workspace(need, dev, sp, (B, Hq, Hkv, Smax, D, T, split))
+        if workspace.dtype != torch.uint8:
+            raise TypeError("workspace must be a uint8 tensor")
+        fn = getattr(lib(), name)
+        if name == "td_decode_attn":
+            st = fn(_code(q4), _ptr(q4), _ptr(k_cache), _ptr(v_cache), _ptr(seq_lens), B, Hq, Hkv, Smax, D,
+                    float(scale), int(split), _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(),
+                    _ptr(dev_status), sp)
+        else:
+            st = fn(_code(q4), _ptr(q4), _ptr(k_cache), _ptr(v_cache), _ptr(seq_lens), B, Hq, Hkv, T, Smax, D,
+                    float(scale), int(split), _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(),
+                    _ptr(dev_status), sp)
+    check(name, st)
+
+
+def td_decode_attn(q, k_cache, v_cache, seq_lens, scale: float | None = None, split: int = 0, out=None, lse=None,
+                   workspace=None, dev_status=None, stream=None, return_lse: bool = False):
+    """Single-token decode attention. q [B,Hq,D] -> out [B,Hq,D] (and lse [B,Hq] fp32)."""
+    if q.dim() != 3:
+        raise ValueError("q must be [B, Hq, D]")
+    B, Hq, D = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty(B, Hq, dtype=torch.float32, device=q.device)
+    if lse is not None and (lse.dtype != torch.float32 or lse.shape != (B, Hq)):
+        raise TypeError("lse must be float32 [B, Hq]")
+    if out.shape != q.shape or out.dtype != q.dtype:
+        raise TypeError("out must match q")
+    _attn("td_decode_attn", q.view(B, Hq, 1, D), k_cache, v_cache, seq_lens, scale, split, out, lse, workspace,
+          dev_status, stream)
+    return (out, lse) if (return_lse or lse is not None) else out
+
+
+def td_verify_attn(q, k_cache, v_cache, seq_lens, scale: float | None = None, split: int = 0, out=None, lse=None,
+                   workspace=None, dev_status=None, stream=None, return_lse: bool = False):
+    """Verify-chunk attention. q [B,Hq,T,D] (seq_lens count the T new tokens) -> out [B,Hq,T,D]."""
+    if q.dim() != 4:
+        raise ValueError("q must be [B, Hq, T, D]")
+    B, Hq, T, D = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty(B, Hq, T, dtype=torch.float32, device=q.device)
+    if lse is not None and (lse.dtype != torch.float32 or lse.shape != (B, Hq, T)):
+        raise TypeError("lse must be float32 [B, Hq, T]")
+    if out.shape != q.shape or out.dtype != q.dtype:
+        raise TypeError("out must match q")
+    _attn("td_verify_attn", q, k_cache, v_cache, seq_lens, scale, split, out, lse, workspace, dev_status, stream)
+    return (out, lse) if (return_lse or lse is not None) else out
+
+
+def td_lse_merge(m, l, acc, seq_lens, split: int, out_dtype=torch.float32, out=None, lse=None, stream=None,
+                 return_lse: bool = False):
+    """Merge per-split partials m,l [B,rows,NS], acc [B,rows,NS,D] -> out [B,rows,D] (+ lse [B,rows])."""
+    dev = _cuda(m, l, acc, seq_lens, out, lse)
+    B, rows, NS, D = acc.shape
+    if m.shape != (B, rows, NS) or l.shape != (B, rows, NS):
+        raise ValueError("m and l must be [B, rows, NS]")
+    if not (m.dtype == l.dtype == acc.dtype == torch.float32):
+        raise TypeError("partials must be float32")
+    if out is None:
+        out = torch.empty(B, rows, D, dtype=out_dtype, device=acc.device)
+    if lse is None and return_lse:
+        lse = torch.empty(B, rows, dtype=torch.float32, device=acc.device)
+    with torch.cuda.device(dev):
+        st = lib().td_lse_merge(_ptr(m), _ptr(l), _ptr(acc), _ptr(seq_lens), B, rows, NS, D, int(split), _code(out),
+                                _ptr(out), _ptr(lse), _stream(stream, dev))
+    check("td_lse_merge", st)
+    return (out, lse) if (return_lse or lse is not None) else out

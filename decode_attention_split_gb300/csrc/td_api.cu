@@ -1,0 +1,143 @@
+// The C ABI declared in td.h: host-side argument checks, then one launch per call.
+#include <math.h>
+
+#include "td_internal.h"
+#include "td_split_attn.cuh"
+
+namespace {
+
+thread_local int g_last_cuda_error = 0;
+
+td_status cuda_fail(cudaError_t e) {
+  g_last_cuda_error = (int)e;
+  return TD_ERR_CUDA;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+size_t elem_size(td_dtype d) { return d == TD_F32 ? 4 : 2; }
+
+td_status attn(td_dtype dtype, const void *q, const void *k_cache, const void *v_cache, const int32_t *seq_lens,
+               int B, int Hq, int Hkv, int T, int Smax, int D, float scale, int split, void *out, float *lse,
+               void *workspace, size_t workspace_bytes, uint32_t *dev_status, void *stream) {
+  if (q == nullptr || k_cache == nullptr || v_cache == nullptr || seq_lens == nullptr || out == nullptr)
+    return TD_ERR_INVALID_ARG;
+  if (!isfinite(scale)) return TD_ERR_INVALID_ARG;
+  td::SplitPlan plan;
+  const td_status st = td::plan_split(dtype, B, Hq, Hkv, T, Smax, D, split, &plan);
+  if (st == TD_ERR_CUDA) return cuda_fail(cudaGetLastError());
+  if (st != TD_OK) return st;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) || !aligned4(seq_lens) ||
+      (lse != nullptr && !aligned4(lse)) || (dev_status != nullptr && !aligned4(dev_status)))
+    return TD_ERR_UNSUPPORTED;
+  if (workspace == nullptr || workspace_bytes < plan.bytes || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return TD_ERR_WORKSPACE;
+  unsigned char *ws = static_cast<unsigned char *>(workspace);
+  td::SplitParams p;
+  p.q = q;
+  p.k = k_cache;
+  p.v = v_cache;
+  p.seq_lens = seq_lens;
+  p.out = out;
+  p.lse = lse;
+  p.ws_m = reinterpret_cast<float *>(ws + plan.off_m);
+  p.ws_l = reinterpret_cast<float *>(ws + plan.off_l);
+  p.ws_acc = reinterpret_cast<float *>(ws + plan.off_acc);
+  p.counters = reinterpret_cast<int *>(ws);
+  p.status = dev_status;
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.G = Hq / Hkv;
+  p.T = T;
+  p.Smax = Smax;
+  p.R = plan.R;
+  p.RB = plan.RB;
+  p.split = split;
+  p.ns_ws = plan.ns_ws;
+  p.p_target = plan.p_target;
+  p.qscale = scale * td::kLog2e;
+  const cudaError_t e = td::launch_split(dtype, D, plan, p, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? TD_OK : cuda_fail(e);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *td_status_string(td_status s) {
+  switch (s) {
+    case TD_OK: return "ok";
+    case TD_ERR_INVALID_ARG: return "invalid argument";
+    case TD_ERR_UNSUPPORTED: return "unsupported shape, dtype or alignment";
+    case TD_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case TD_ERR_CUDA: return "CUDA error";
+  }
+  return "unknown status";
+}
+
+const char *td_version(void) { return "td 0.1 (sm_103a)"; }
+
+int td_last_cuda_error(void) { return g_last_cuda_error; }
+
+size_t td_decode_workspace_bytes(int B, int Hq, int Hkv, int Smax, int D, int q_len, int split) {
+  // the kernel variant (and so the grid and the partial slots) may differ by element type:
+  // size for the larger of the two so one workspace serves both
+  size_t bytes = 0;
+  for (td_dtype dt : {TD_F32, TD_BF16}) {
+    td::SplitPlan plan;
+    if (td::plan_split(dt, B, Hq, Hkv, q_len, Smax, D, split, &plan) != TD_OK) return 0;
+    if (plan.bytes > bytes) bytes = plan.bytes;
+  }
+  return bytes;
+}
+
+td_status td_kv_append(td_dtype dtype, const void *k_new, const void *v_new, void *k_cache, void *v_cache,
+                       int32_t *seq_lens, int B, int Hkv, int T, int Smax, int D, int advance, uint32_t *dev_status,
+                       void *stream) {
+  if (dtype != TD_F32 && dtype != TD_BF16) return TD_ERR_UNSUPPORTED;
+  if (k_new == nullptr || v_new == nullptr || k_cache == nullptr || v_cache == nullptr || seq_lens == nullptr)
+    return TD_ERR_INVALID_ARG;
+  if (B < 1 || Hkv < 1 || T < 1 || Smax < 1 || D < 1) return TD_ERR_INVALID_ARG;
+  if (B > 65535 || ((size_t)D * elem_size(dtype)) % 16 != 0) return TD_ERR_UNSUPPORTED;
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned4(seq_lens) ||
+      (dev_status != nullptr && !aligned4(dev_status)))
+    return TD_ERR_UNSUPPORTED;
+  const cudaError_t e = td::launch_append(elem_size(dtype), k_new, v_new, k_cache, v_cache, seq_lens, B, Hkv, T,
+                                          Smax, D, advance, dev_status, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? TD_OK : cuda_fail(e);
+}
+
+td_status td_decode_attn(td_dtype dtype, const void *q, const void *k_cache, const void *v_cache,
+                         const int32_t *seq_lens, int B, int Hq, int Hkv, int Smax, int D, float scale, int split,
+                         void *out, float *lse, void *workspace, size_t workspace_bytes, uint32_t *dev_status,
+                         void *stream) {
+  return attn(dtype, q, k_cache, v_cache, seq_lens, B, Hq, Hkv, 1, Smax, D, scale, split, out, lse, workspace,
+              workspace_bytes, dev_status, stream);
+}
+
+td_status td_verify_attn(td_dtype dtype, const void *q, const void *k_cache, const void *v_cache,
+                         const int32_t *seq_lens, int B, int Hq, int Hkv, int T, int Smax, int D, float scale,
+                         int split, void *out, float *lse, void *workspace, size_t workspace_bytes,
+                         uint32_t *dev_status, void *stream) {
+  return attn(dtype, q, k_cache, v_cache, seq_lens, B, Hq, Hkv, T, Smax, D, scale, split, out, lse, workspace,
+              workspace_bytes, dev_status, stream);
+}
+
+td_status td_lse_merge(const float *m, const float *l, const float *acc, const int32_t *seq_lens, int B, int rows,
+                       int NS, int D, int split, td_dtype out_dtype, void *out, float *lse, void *stream) {
+  if (m == nullptr || l == nullptr || acc == nullptr || seq_lens == nullptr || out == nullptr)
+    return TD_ERR_INVALID_ARG;
+  if (B < 1 || rows < 1 || NS < 1 || D < 1 || split < 1) return TD_ERR_INVALID_ARG;
+  if (out_dtype != TD_F32 && out_dtype != TD_BF16) return TD_ERR_UNSUPPORTED;
+  if (D % 4 != 0 || D > 1024 || B > 65535) return TD_ERR_UNSUPPORTED;
+  if (!aligned4(m) || !aligned4(l) || !aligned4(acc) || !aligned4(seq_lens) ||
+      !aligned4(out) || (lse != nullptr && !aligned4(lse)))
+    return TD_ERR_UNSUPPORTED;
+  const cudaError_t e = td::launch_merge(m, l, acc, seq_lens, B, rows, NS, D, split, out_dtype, out, lse,
+                                         static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? TD_OK : cuda_fail(e);
+}
+
+}  // extern "C"

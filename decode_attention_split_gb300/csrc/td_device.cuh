@@ -1,0 +1,138 @@
+// Device-side helpers shared by the td kernels: asynchronous bulk copies (TMA engine)
+// into shared memory with mbarrier completion, bounded waits, and fp32 widening of
+// stored elements.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "td.h"
+
+namespace td {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+// A wait on an asynchronous copy gives up after this many SM cycles (about one second)
+// and reports TD_DEV_WAIT_TIMEOUT instead of hanging the GPU.
+constexpr long long kWaitLimitCycles = 2000000000LL;
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+// Makes mbarrier initialisation visible to the asynchronous (TMA) proxy.
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+// Orders this thread's earlier generic-proxy shared-memory accesses before later
+// asynchronous-proxy accesses (a bulk copy overwriting a buffer just read).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Waits for phase `parity` of an mbarrier to complete; false after kWaitLimitCycles.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (clock64() - t0 > kWaitLimitCycles) return false;
+  }
+  return true;
+}
+
+// L2 policy for data read exactly once (the KV stream): evict it first.
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+// One bulk copy global -> shared through the TMA engine; completion is counted on `bar`
+// in bytes. dst, src and bytes must be multiples of 16.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar,
+                                         uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+          dst),
+      "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+      : "memory");
+}
+
+// ---- widening of stored elements to fp32 ----------------------------------------------
+
+// A bf16 value is the upper half of a binary32 value.
+__device__ __forceinline__ void widen_bf16x2(uint32_t w, float &lo, float &hi) {
+  lo = __uint_as_float(w << 16);
+  hi = __uint_as_float(w & 0xffff0000u);
+}
+
+// Loads N consecutive elements of type E from shared or global memory at p (aligned to
+// N * sizeof(E) bytes, which is 4, 8 or 16) and widens them to fp32.
+template <typename E, int N>
+__device__ __forceinline__ void load_widen(const void *p, float (&f)[N]) {
+  if constexpr (sizeof(E) == 4) {
+    static_assert(N == 2 || N == 4, "fp32 vector of 2 or 4");
+    if constexpr (N == 4) {
+      const float4 x = *reinterpret_cast<const float4 *>(p);
+      f[0] = x.x, f[1] = x.y, f[2] = x.z, f[3] = x.w;
+    } else {
+      const float2 x = *reinterpret_cast<const float2 *>(p);
+      f[0] = x.x, f[1] = x.y;
+    }
+  } else {
+    static_assert(N == 2 || N == 4 || N == 8, "bf16 vector of 2, 4 or 8");
+    if constexpr (N == 8) {
+      const uint4 x = *reinterpret_cast<const uint4 *>(p);
+      widen_bf16x2(x.x, f[0], f[1]);
+      widen_bf16x2(x.y, f[2], f[3]);
+      widen_bf16x2(x.z, f[4], f[5]);
+      widen_bf16x2(x.w, f[6], f[7]);
+    } else if constexpr (N == 4) {
+      const uint2 x = *reinterpret_cast<const uint2 *>(p);
+      widen_bf16x2(x.x, f[0], f[1]);
+      widen_bf16x2(x.y, f[2], f[3]);
+    } else {
+      const uint32_t x = *reinterpret_cast<const uint32_t *>(p);
+      widen_bf16x2(x, f[0], f[1]);
+    }
+  }
+}
+
+template <typename E>
+__device__ __forceinline__ void store_elem(E *p, float x);
+template <>
+__device__ __forceinline__ void store_elem<float>(float *p, float x) {
+  *p = x;
+}
+template <>
+__device__ __forceinline__ void store_elem<__nv_bfloat16>(__nv_bfloat16 *p, float x) {
+  *p = __float2bfloat16_rn(x);
+}
+
+__device__ __forceinline__ void report(uint32_t *status, uint32_t bits) {
+  if (status != nullptr && bits != 0u) atomicOr(status, bits);
+}
+
+}  // namespace td

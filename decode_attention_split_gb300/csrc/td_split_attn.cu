@@ -1,0 +1,152 @@
+// Instantiations, launch planning and per-device attribute cache for the split-attention kernel.
+#include <mutex>
+
+#include "td_internal.h"
+#include "td_split_attn.cuh"
+
+namespace td {
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int kKernelSlots = 2 * 2 * 4;  // dtype x head dim x row padding
+
+struct KernelRef {
+  const void *fn;
+  int smem;
+  void (*launch)(const SplitParams &, int grid, int smem, cudaStream_t);
+};
+
+template <typename E, int D, int RP>
+void launch_one(const SplitParams &p, int grid, int smem, cudaStream_t stream) {
+  split_attn_kernel<E, D, RP><<<grid, kThreads, smem, stream>>>(p);
+}
+
+template <typename E, int D, int RP>
+KernelRef ref_of() {
+  if constexpr (SplitCfg<E, D, RP>::kFits) {
+    return KernelRef{reinterpret_cast<const void *>(&split_attn_kernel<E, D, RP>), SplitCfg<E, D, RP>::SMEM_BYTES,
+                     &launch_one<E, D, RP>};
+  } else {
+    return KernelRef{nullptr, 0, nullptr};
+  }
+}
+
+int rp_index(int RP) { return RP == 1 ? 0 : RP == 2 ? 1 : RP == 4 ? 2 : 3; }
+
+// Returns the kernel for (dtype, D, RP); fn == nullptr when not built.
+template <typename E>
+KernelRef pick_d(int D, int RP) {
+  if (D == 64) {
+    switch (RP) {
+      case 1: return ref_of<E, 64, 1>();
+      case 2: return ref_of<E, 64, 2>();
+      case 4: return ref_of<E, 64, 4>();
+      case 8: return ref_of<E, 64, 8>();
+    }
+  } else if (D == 128) {
+    switch (RP) {
+      case 1: return ref_of<E, 128, 1>();
+      case 2: return ref_of<E, 128, 2>();
+      case 4: return ref_of<E, 128, 4>();
+    }
+  }
+  return KernelRef{nullptr, 0, nullptr};
+}
+
+KernelRef pick(td_dtype dtype, int D, int RP) {
+  return dtype == TD_F32 ? pick_d<float>(D, RP) : pick_d<__nv_bfloat16>(D, RP);
+}
+
+int slot_of(td_dtype dtype, int D, int RP) { return ((dtype == TD_F32 ? 0 : 1) * 2 + (D == 64 ? 0 : 1)) * 4 + rp_index(RP); }
+
+std::mutex g_mu;
+int g_sms[kMaxDevices];
+int g_blocks[kMaxDevices][kKernelSlots];  // resident CTAs per SM (0 = not yet queried)
+
+// Sets the shared-memory opt-in once per device and returns the resident CTAs per SM.
+int blocks_per_sm(int device, td_dtype dtype, int D, int RP, const KernelRef &k) {
+  const int slot = slot_of(dtype, D, RP);
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (device >= 0 && device < kMaxDevices && g_blocks[device][slot] > 0) return g_blocks[device][slot];
+  if (cudaFuncSetAttribute(k.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, k.smem) != cudaSuccess) return 0;
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k.fn, kThreads, k.smem) != cudaSuccess) return 0;
+  if (device >= 0 && device < kMaxDevices) g_blocks[device][slot] = n;
+  return n;
+}
+
+size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+
+}  // namespace
+
+int device_sm_count(int device) {
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (device >= 0 && device < kMaxDevices && g_sms[device] > 0) return g_sms[device];
+  }
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) return 0;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (device >= 0 && device < kMaxDevices) g_sms[device] = n;
+  return n;
+}
+
+td_status plan_split(td_dtype dtype, int B, int Hq, int Hkv, int T, int Smax, int D, int split, SplitPlan *plan) {
+  if (dtype != TD_F32 && dtype != TD_BF16) return TD_ERR_UNSUPPORTED;
+  if (D != 64 && D != 128) return TD_ERR_UNSUPPORTED;
+  if (B < 1 || Hq < 1 || Hkv < 1 || T < 1 || Smax < 1 || split < 0 || Hq % Hkv != 0) return TD_ERR_INVALID_ARG;
+  if (B > TD_MAX_BATCH || Smax > (1 << 30) || T > Smax) return TD_ERR_UNSUPPORTED;
+  const long long GT = (long long)(Hq / Hkv) * T;
+  const int rmax = D == 128 ? 4 : 8;
+  const int R = (int)(GT < rmax ? GT : rmax);
+  int RP = 1;
+  while (RP < R) RP <<= 1;
+  // a 512-byte fp32 row makes a one-row CTA's 32-key stages too large: pad to two rows
+  if (dtype == TD_F32 && D == 128 && RP < 2) RP = 2;
+  const long long RB = (GT + R - 1) / R;
+  const long long U = (long long)Hkv * RB;
+  const KernelRef k = pick(dtype, D, RP);
+  if (k.fn == nullptr) return TD_ERR_UNSUPPORTED;
+  int device = 0;
+  if (cudaGetDevice(&device) != cudaSuccess) return TD_ERR_CUDA;
+  const int sms = device_sm_count(device);
+  const int per_sm = blocks_per_sm(device, dtype, D, RP, k);
+  if (sms <= 0 || per_sm <= 0) return TD_ERR_CUDA;
+  const long long p_target = (long long)sms * per_sm;
+  long long ns;
+  if (split > 0) {
+    ns = ((long long)Smax + split - 1) / split;
+  } else {
+    const long long by_size = ((long long)Smax + 15) / 16;
+    const long long by_grid = (p_target + U - 1) / U;
+    ns = by_size < by_grid ? by_size : by_grid;
+    if (ns < 1) ns = 1;
+  }
+  const long long items_max = (long long)B * U * ns;
+  if (items_max >= (1LL << 31)) return TD_ERR_UNSUPPORTED;
+  plan->RP = RP;
+  plan->R = R;
+  plan->RB = (int)RB;
+  plan->ns_ws = (int)ns;
+  plan->p_target = (int)p_target;
+  plan->grid = (int)(items_max < p_target ? items_max : p_target);
+  if (plan->grid < 1) plan->grid = 1;
+  plan->smem = k.smem;
+  const size_t rows = (size_t)B * Hq * T;
+  const size_t counters = align256((size_t)B * U * sizeof(int));
+  plan->off_m = counters;
+  plan->off_l = plan->off_m + align256(rows * ns * sizeof(float));
+  plan->off_acc = plan->off_l + align256(rows * ns * sizeof(float));
+  plan->bytes = plan->off_acc + align256(rows * ns * D * sizeof(float));
+  return TD_OK;
+}
+
+cudaError_t launch_split(td_dtype dtype, int D, const SplitPlan &plan, const SplitParams &p, cudaStream_t stream) {
+  const KernelRef k = pick(dtype, D, plan.RP);
+  if (k.fn == nullptr) return cudaErrorInvalidValue;
+  k.launch(p, plan.grid, plan.smem, stream);
+  return cudaGetLastError();
+}
+
+}  // namespace td

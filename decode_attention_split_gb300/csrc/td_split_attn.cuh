@@ -1,0 +1,495 @@
+// Split-KV attention for decode and speculative-verify chunks.
+//
+// Method ("tinydecode", section "how the decode step is put together"; "llm-decode-cuda",
+// split-KV attention section): the keys of each sequence are cut into chunks; one CTA
+// computes, for one (sequence b, kv head, chunk) and every query row that reads that kv
+// head (the whole grouped-query group, times the T tokens of a verify chunk), the partial
+// softmax (m, l, acc) of the chunk; the partials are merged with log-sum-exp. Query head hq
+// reads kv head hq / G (index math, no copies).
+//
+// GB300 design:
+//  * Work items (b, kv head, row block, chunk) are enumerated on the device from seq_lens,
+//    so the grid depends only on the arguments (CUDA-graph capturable) and chunks past a
+//    sequence's length are never scheduled. With split = 0 the chunk size is chosen on the
+//    device so the items fill the grid (persistent-style, grid-stride over items).
+//  * Inside a CTA each warp streams its own slice of the chunk through a private ring of
+//    shared-memory stages, filled by bulk asynchronous copies (the TMA engine; one K and one
+//    V copy per stage, each a contiguous run of cache rows) and completed on an mbarrier.
+//  * Scores: 8 lanes per key, each lane owning D/8 dimensions as 16-byte vectors; the
+//    partial dot products of 8 (key, row) pairs are reduced across the 8 lanes with a
+//    transposing butterfly, leaving one full score per lane. Online softmax in base 2.
+//  * p @ V: each lane owns D/32 dimensions of every row's accumulator; the probabilities are
+//    broadcast through a per-warp shared stash.
+//  * Warps combine their partials in shared memory; a chunk that is the only one of its
+//    sequence writes the output directly, otherwise the partial goes to the workspace and
+//    the CTA that completes the last chunk of a (b, kv head, row block) merges (atomic
+//    ticket, no spin-wait).
+#pragma once
+
+#include "td_device.cuh"
+#include "td_merge.cuh"
+
+namespace td {
+
+constexpr int kWarps = 4;
+constexpr int kThreads = kWarps * 32;
+constexpr int kStages = 3;
+
+struct SplitParams {
+  const void *q;        // [B, Hq, T, D]
+  const void *k;        // [B, Hkv, Smax, D]
+  const void *v;
+  const int32_t *seq_lens;
+  void *out;            // [B, Hq, T, D]
+  float *lse;           // [B, Hq, T] or null
+  float *ws_m;          // [B, Hq*T, ns_ws]
+  float *ws_l;
+  float *ws_acc;        // [B, Hq*T, ns_ws, D]
+  int *counters;        // [B, Hkv, RB]
+  uint32_t *status;
+  int B, Hq, Hkv, G, T, Smax;
+  int R;                // query rows per CTA (<= RP)
+  int RB;               // row blocks per kv head: ceil(G*T / R)
+  int split;            // fixed chunk size, or 0 = chosen on the device
+  int ns_ws;            // partial slots per row in the workspace
+  int p_target;         // CTAs the automatic chunk size aims to fill
+  float qscale;         // scale * log2(e)
+};
+
+template <typename E, int D, int RP>
+struct SplitCfg {
+  static constexpr int EB = sizeof(E);
+  static constexpr int ROW_BYTES = D * EB;
+  static constexpr int VE = 16 / EB;             // elements per 16-byte vector
+  static constexpr int NV = ROW_BYTES / 16;      // 16-byte vectors per cache row
+  static constexpr int QV = NV / 8;              // vectors per lane for scores (8 lanes per key)
+  static constexpr int DQ = QV * VE;             // = D / 8 dims per lane for scores
+  static constexpr int DV = D / 32;              // dims per lane for p @ V
+  static constexpr int KB = 32 / RP;             // keys per batch (one score per lane)
+  static constexpr int SLOTS = 8 / RP;           // keys per 8-lane group per batch
+  static constexpr int TKW = KB > 16 ? KB : 16;  // keys per warp stage
+  static constexpr int TILE_BYTES = TKW * ROW_BYTES;
+  static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
+  static constexpr int RING_BYTES = kStages * STAGE_BYTES;  // per warp
+  static constexpr int STASH_FLOATS = KB * RP + 8;
+  static constexpr int COMBINE_FLOATS = kWarps * RP * (D + 2);
+  static constexpr int MERGE_FLOATS = RP * kMergeBlock + 2 * RP;
+  static constexpr int SMEM_BYTES = kWarps * RING_BYTES + kWarps * STASH_FLOATS * 4 + kWarps * kStages * 8;
+  static_assert(NV % 8 == 0, "cache row must hold a multiple of 8 16-byte vectors");
+  static_assert(D % 32 == 0, "head dim multiple of 32");
+  static_assert(RP == 1 || RP == 2 || RP == 4 || RP == 8, "row padding is a power of two <= 8");
+  static_assert((COMBINE_FLOATS + MERGE_FLOATS) * 4 <= kWarps * RING_BYTES, "combine area fits in the rings");
+  static_assert(TKW % KB == 0, "stage holds whole batches");
+  // fits next to the ~8.3 KB of static shared memory within the 227 KB a CTA may use
+  static constexpr bool kFits = SMEM_BYTES + 8448 <= 227 * 1024;
+};
+
+__device__ __forceinline__ int clamp_len(int32_t L, int Smax) { return L < 0 ? 0 : (L > Smax ? Smax : L); }
+
+// Exclusive prefix over the per-sequence item counts, computed by the whole CTA.
+// s_len[b] receives the clamped length; returns the chunk size through *s_chunk and the
+// item total in s_prefix[B].
+static __device__ void plan_items(const SplitParams &p, int *s_len, int *s_prefix, int *s_chunk, long long *s_red) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int U = p.Hkv * p.RB;
+  constexpr int kSeg = (TD_MAX_BATCH + kThreads - 1) / kThreads;
+  const int b0 = tid * kSeg;
+  long long tot = 0;
+  uint32_t bits = 0;
+#pragma unroll
+  for (int i = 0; i < kSeg; ++i) {
+    const int b = b0 + i;
+    if (b < p.B) {
+      const int32_t raw = p.seq_lens[b];
+      const int L = clamp_len(raw, p.Smax);
+      if (raw < 0) bits |= TD_DEV_NEGATIVE_SEQLEN;
+      if (raw > p.Smax) bits |= TD_DEV_SEQLEN_CLAMPED;
+      if (p.T > 1 && L < p.T) bits |= TD_DEV_VERIFY_SHORT;
+      s_len[b] = L;
+      tot += L;
+    }
+  }
+  if (blockIdx.x == 0) report(p.status, bits);
+  // total keys over the batch
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+  if (lane == 0) s_red[warp] = tot;
+  __syncthreads();
+  if (tid == 0) {
+    long long all = 0;
+    for (int w = 0; w < kWarps; ++w) all += s_red[w];
+    int S;
+    if (p.split > 0) {
+      S = p.split;
+    } else {
+      long long want = (all * U + p.p_target - 1) / p.p_target;  // keys per item to fill the grid
+      want = (want + 15) / 16 * 16;
+      if (want < 16) want = 16;
+      const long long floor_ws = ((long long)p.Smax + p.ns_ws - 1) / p.ns_ws;  // keeps chunks <= ns_ws
+      if (want < floor_ws) want = floor_ws;
+      S = (int)(want > p.Smax ? p.Smax : want);
+      if (S < 1) S = 1;
+    }
+    *s_chunk = S;
+  }
+  __syncthreads();
+  const int S = *s_chunk;
+  // per-thread segment sums of items, then a CTA-wide exclusive scan
+  int seg = 0;
+#pragma unroll
+  for (int i = 0; i < kSeg; ++i) {
+    const int b = b0 + i;
+    if (b < p.B) seg += ((s_len[b] + S - 1) / S) * U;
+  }
+  int incl = seg;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  __syncthreads();  // s_red reuse
+  if (lane == 31) s_red[warp] = incl;
+  __syncthreads();
+  int before = incl - seg;
+  for (int w = 0; w < warp; ++w) before += (int)s_red[w];
+#pragma unroll
+  for (int i = 0; i < kSeg; ++i) {
+    const int b = b0 + i;
+    if (b < p.B) {
+      s_prefix[b] = before;
+      before += ((s_len[b] + S - 1) / S) * U;
+    }
+  }
+  if (tid == kThreads - 1) {
+    int all = 0;
+    for (int w = 0; w < kWarps; ++w) all += (int)s_red[w];
+    s_prefix[p.B] = all;
+  }
+  __syncthreads();
+}
+
+template <typename E, int D, int RP>
+__global__ void __launch_bounds__(kThreads) split_attn_kernel(const SplitParams p) {
+  using C = SplitCfg<E, D, RP>;
+  extern __shared__ __align__(128) unsigned char smem[];
+  __shared__ int s_len[TD_MAX_BATCH];
+  __shared__ int s_prefix[TD_MAX_BATCH + 1];
+  __shared__ long long s_red[kWarps];
+  __shared__ int s_chunk, s_last, s_abort;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g8 = lane >> 3, sub = lane & 7;
+  unsigned char *ring = smem + warp * C::RING_BYTES;
+  float *stash = reinterpret_cast<float *>(smem + kWarps * C::RING_BYTES) + warp * C::STASH_FLOATS;
+  uint64_t *bars =
+      reinterpret_cast<uint64_t *>(smem + kWarps * C::RING_BYTES + kWarps * C::STASH_FLOATS * 4) + warp * kStages;
+  float *combine = reinterpret_cast<float *>(smem);           // after all rings are idle
+  float *merge_scratch = combine + C::COMBINE_FLOATS;
+
+  if (lane == 0) {
+#pragma unroll
+    for (int s = 0; s < kStages; ++s) mbar_init(smem_u32(&bars[s]), 1);
+    fence_mbar_init();
+  }
+  if (tid == 0) s_abort = 0;
+  plan_items(p, s_len, s_prefix, &s_chunk, s_red);  // ends with __syncthreads
+
+  const int S = s_chunk;
+  const int W = s_prefix[p.B];
+  const int U = p.Hkv * p.RB;
+  const int rows = p.Hq * p.T;
+  const int GT = p.G * p.T;
+  const uint64_t policy = l2_evict_first_policy();
+  uint32_t seq = 0;  // stages consumed by this warp so far (mbarrier phase bookkeeping)
+
+  // sequences with no key get no item: their rows are 0 with lse = -inf
+  for (int b = blockIdx.x; b < p.B; b += gridDim.x) {
+    if (s_len[b] != 0) continue;
+    for (int idx = tid; idx < rows * D; idx += kThreads)
+      store_elem<E>(static_cast<E *>(p.out) + (long long)b * rows * D + idx, 0.f);
+    if (p.lse != nullptr)
+      for (int r = tid; r < rows; r += kThreads) p.lse[(long long)b * rows + r] = -INFINITY;
+  }
+
+  for (int item = blockIdx.x; item < W; item += gridDim.x) {
+    // ---- locate the item: sequence b by binary search over the prefix, then kv head, row block, chunk
+    int lo = 0, hi = p.B - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (s_prefix[mid] <= item) lo = mid; else hi = mid - 1;
+    }
+    const int b = lo;
+    const int L = s_len[b];
+    const int NC = (L + S - 1) / S;
+    const int local = item - s_prefix[b];
+    const int c = local % NC;
+    const int rest = local / NC;
+    const int rb = rest % p.RB;
+    const int kvh = rest / p.RB;
+    const int c0 = c * S;
+    const int c1 = min(c0 + S, L);
+
+    // ---- this warp's slice of the chunk, in whole stages
+    const int n = c1 - c0;
+    const int per = ((n + kWarps - 1) / kWarps + C::TKW - 1) / C::TKW * C::TKW;
+    const int w0 = c0 + warp * per;
+    const int w1 = min(w0 + per, c1);
+    const int ntiles = w0 < w1 ? (w1 - w0 + C::TKW - 1) / C::TKW : 0;
+    const size_t head_off = ((size_t)b * p.Hkv + kvh) * (size_t)p.Smax * C::ROW_BYTES;
+    const unsigned char *kg = static_cast<const unsigned char *>(p.k) + head_off;
+    const unsigned char *vg = static_cast<const unsigned char *>(p.v) + head_off;
+
+    auto issue = [&](int i) {
+      const int st = (seq + i) % kStages;
+      const int j0 = w0 + i * C::TKW;
+      const uint32_t bytes = (uint32_t)min(C::TKW, w1 - j0) * C::ROW_BYTES;
+      const uint32_t bar = smem_u32(&bars[st]);
+      unsigned char *dst = ring + st * C::STAGE_BYTES;
+      fence_proxy_async_smem();
+      mbar_arrive_expect_tx(bar, 2 * bytes);
+      bulk_g2s(smem_u32(dst), kg + (size_t)j0 * C::ROW_BYTES, bytes, bar, policy);
+      bulk_g2s(smem_u32(dst + C::TILE_BYTES), vg + (size_t)j0 * C::ROW_BYTES, bytes, bar, policy);
+    };
+    if (lane == 0) {
+      for (int i = 0; i < min(kStages, ntiles); ++i) issue(i);
+    }
+
+    // ---- query rows of this CTA: row r is group row rb*R + r = (head in group, token t)
+    int nvis[RP];
+    float qr[RP][C::DQ];
+#pragma unroll
+    for (int r = 0; r < RP; ++r) {
+      const int gr = rb * p.R + r;
+      const bool valid = r < p.R && gr < GT;
+      const int hq = kvh * p.G + gr / p.T;
+      const int t = gr % p.T;
+      nvis[r] = valid ? max(L - p.T + t + 1, 0) : 0;
+      const unsigned char *qrow =
+          static_cast<const unsigned char *>(p.q) + (((size_t)b * p.Hq + hq) * p.T + t) * C::ROW_BYTES;
+#pragma unroll
+      for (int qv = 0; qv < C::QV; ++qv) {
+        float f[C::VE];
+        if (valid) {
+          load_widen<E, C::VE>(qrow + (sub + 8 * qv) * 16, f);
+        } else {
+#pragma unroll
+          for (int e = 0; e < C::VE; ++e) f[e] = 0.f;
+        }
+#pragma unroll
+        for (int e = 0; e < C::VE; ++e) qr[r][qv * C::VE + e] = f[e] * p.qscale;
+      }
+    }
+
+    // ---- stream the slice: online softmax in base 2
+    const int my_row = sub % RP;  // row of the single score this lane holds after the reduction
+    int my_nvis = 0;               // (selected without a runtime index so nvis stays in registers)
+#pragma unroll
+    for (int r = 0; r < RP; ++r)
+      if (r == my_row) my_nvis = nvis[r];
+    float m_run = -INFINITY, l_run = 0.f;
+    float acc[RP][C::DV];
+#pragma unroll
+    for (int r = 0; r < RP; ++r)
+#pragma unroll
+      for (int d = 0; d < C::DV; ++d) acc[r][d] = 0.f;
+
+    int consumed = 0;
+    bool ok = true;
+    for (int i = 0; i < ntiles; ++i) {
+      const int st = (seq + i) % kStages;
+      const uint32_t parity = ((seq + i) / kStages) & 1u;
+      if (!mbar_wait_bounded(smem_u32(&bars[st]), parity)) {
+        ok = false;
+        break;
+      }
+      const unsigned char *Ks = ring + st * C::STAGE_BYTES;
+      const unsigned char *Vs = Ks + C::TILE_BYTES;
+      const int j0 = w0 + i * C::TKW;
+      const int nk = min(C::TKW, w1 - j0);
+      for (int kb0 = 0; kb0 < nk; kb0 += C::KB) {
+        // partial scores: slot s holds key kb0 + 4s + g8, for every row
+        float part[8];
+#pragma unroll
+        for (int x = 0; x < 8; ++x) part[x] = 0.f;
+#pragma unroll
+        for (int s = 0; s < C::SLOTS; ++s) {
+          const unsigned char *krow = Ks + (kb0 + 4 * s + g8) * C::ROW_BYTES;
+#pragma unroll
+          for (int qv = 0; qv < C::QV; ++qv) {
+            float kf[C::VE];
+            load_widen<E, C::VE>(krow + (sub + 8 * qv) * 16, kf);
+#pragma unroll
+            for (int r = 0; r < RP; ++r)
+#pragma unroll
+              for (int e = 0; e < C::VE; ++e) part[s * RP + r] = fmaf(qr[r][qv * C::VE + e], kf[e], part[s * RP + r]);
+          }
+        }
+        // transposing butterfly over the 8 lanes of a key group: lane `sub` ends with pair `sub`
+#pragma unroll
+        for (int o = 4, nh = 4; o > 0; o >>= 1, nh >>= 1) {
+          const bool up = (sub & o) != 0;
+#pragma unroll
+          for (int x = 0; x < nh; ++x) {
+            const float send = up ? part[x] : part[x + nh];
+            const float keep = up ? part[x + nh] : part[x];
+            part[x] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+          }
+        }
+        const int kk = kb0 + (sub / RP) * 4 + g8;  // key (within the stage) of this lane's score
+        const int j = j0 + kk;
+        const bool valid = kk < nk && j < my_nvis;
+        const float sc = valid ? part[0] : -INFINITY;
+        float bm = sc;
+#pragma unroll
+        for (int o = RP; o < 32; o <<= 1) bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, o));
+        const float m_new = fmaxf(m_run, bm);
+        const float base = m_new == -INFINITY ? 0.f : m_new;
+        const float pr = exp2f(sc - base);
+        const float alpha = exp2f(m_run - base);
+        l_run = l_run * alpha + pr;
+        m_run = m_new;
+        stash[((sub / RP) * 4 + g8) * RP + my_row] = pr;
+        if (lane < RP) stash[C::KB * RP + lane] = alpha;
+        __syncwarp();
+        // p @ V: rescale, then accumulate this batch's keys
+        float al[RP];
+#pragma unroll
+        for (int r = 0; r < RP; ++r) al[r] = stash[C::KB * RP + r];
+        bool rescale = false;
+#pragma unroll
+        for (int r = 0; r < RP; ++r) rescale |= al[r] != 1.f;
+        if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll
+          for (int r = 0; r < RP; ++r)
+#pragma unroll
+            for (int d = 0; d < C::DV; ++d) acc[r][d] *= al[r];
+        }
+        const int nkb = min(C::KB, nk - kb0);
+#pragma unroll
+        for (int x = 0; x < C::KB; ++x) {
+          if (x < nkb) {
+            float vf[C::DV];
+            load_widen<E, C::DV>(Vs + (kb0 + x) * C::ROW_BYTES + lane * C::DV * C::EB, vf);
+#pragma unroll
+            for (int r = 0; r < RP; ++r) {
+              const float pw = stash[x * RP + r];
+#pragma unroll
+              for (int d = 0; d < C::DV; ++d) acc[r][d] = fmaf(pw, vf[d], acc[r][d]);
+            }
+          }
+        }
+        __syncwarp();
+      }
+      consumed = i + 1;
+      if (lane == 0 && i + kStages < ntiles) issue(i + kStages);
+    }
+    if (!ok) {
+      // a copy never completed: wait (bounded) for this warp's other copies, then drop the slice
+      const int issued = min(ntiles, consumed + kStages);
+      for (int i = consumed + 1; i < issued; ++i)
+        mbar_wait_bounded(smem_u32(&bars[(seq + i) % kStages]), ((seq + i) / kStages) & 1u);
+      if (lane == 0) {
+        report(p.status, TD_DEV_WAIT_TIMEOUT);
+        s_abort = 1;
+      }
+      m_run = -INFINITY;
+      l_run = 0.f;
+#pragma unroll
+      for (int r = 0; r < RP; ++r)
+#pragma unroll
+        for (int d = 0; d < C::DV; ++d) acc[r][d] = 0.f;
+    }
+    seq += ntiles;
+
+    // ---- combine the warps' partials (shared memory, rings idle)
+    float l_tot = l_run;
+#pragma unroll
+    for (int o = RP; o < 32; o <<= 1) l_tot += __shfl_xor_sync(0xffffffffu, l_tot, o);
+    __syncthreads();
+    float *cm = combine;                      // [kWarps][RP]
+    float *cl = combine + kWarps * RP;        // [kWarps][RP]
+    float *ca = combine + 2 * kWarps * RP;    // [kWarps][RP][D]
+    if (lane < RP) {
+      cm[warp * RP + lane] = m_run;
+      cl[warp * RP + lane] = l_tot;
+    }
+#pragma unroll
+    for (int r = 0; r < RP; ++r)
+#pragma unroll
+      for (int d = 0; d < C::DV; ++d) ca[(warp * RP + r) * D + lane * C::DV + d] = acc[r][d];
+    __syncthreads();
+
+    const bool single = NC == 1;
+    for (int idx = tid; idx < RP * D; idx += kThreads) {
+      const int r = idx / D, d = idx % D;
+      const int gr = rb * p.R + r;
+      if (r >= p.R || gr >= GT) continue;
+      const int hq = kvh * p.G + gr / p.T;
+      const int t = gr % p.T;
+      const long long row = (long long)b * rows + (long long)hq * p.T + t;
+      float M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) M = fmaxf(M, cm[w * RP + r]);
+      float Ls = 0.f, A = 0.f;
+      if (M != -INFINITY) {
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) {
+          const float mw = cm[w * RP + r];
+          if (mw != -INFINITY) {
+            const float f = exp2f(mw - M);
+            Ls = fmaf(cl[w * RP + r], f, Ls);
+            A = fmaf(ca[(w * RP + r) * D + d], f, A);
+          }
+        }
+      }
+      if (single) {
+        store_elem<E>(static_cast<E *>(p.out) + row * D + d, Ls > 0.f ? A / Ls : 0.f);
+        if (d == 0 && p.lse != nullptr) p.lse[row] = Ls > 0.f ? (M + log2f(Ls)) * kLn2 : -INFINITY;
+      } else {
+        const long long slot = row * p.ns_ws + c;
+        p.ws_acc[slot * D + d] = A;
+        if (d == 0) {
+          p.ws_m[slot] = Ls > 0.f ? M * kLn2 : -INFINITY;
+          p.ws_l[slot] = Ls;
+        }
+      }
+    }
+
+    if (!single) {
+      // completion ticket for (b, kv head, row block); the CTA finishing the last chunk merges
+      __threadfence();
+      __syncthreads();
+      int *cnt = p.counters + ((long long)b * p.Hkv + kvh) * p.RB + rb;
+      if (tid == 0) {
+        const int before = atomicAdd(cnt, 1);
+        if (before < 0 || before >= NC) report(p.status, TD_DEV_WORKSPACE_DIRTY);
+        s_last = before == NC - 1;
+      }
+      __syncthreads();
+      if (s_last) {
+        __threadfence();
+        long long rowbase[RP], out_row[RP];
+#pragma unroll
+        for (int r = 0; r < RP; ++r) {
+          const int gr = rb * p.R + r;
+          if (r < p.R && gr < GT) {
+            const int hq = kvh * p.G + gr / p.T;
+            const int t = gr % p.T;
+            out_row[r] = (long long)b * rows + (long long)hq * p.T + t;
+            rowbase[r] = out_row[r] * p.ns_ws;
+          } else {
+            out_row[r] = 0;
+            rowbase[r] = -1;
+          }
+        }
+        merge_rows<RP, E>(p.ws_m, p.ws_l, p.ws_acc, rowbase, out_row, NC, D, static_cast<E *>(p.out), p.lse,
+                          merge_scratch, merge_scratch + RP * kMergeBlock);
+        if (tid == 0) *cnt = 0;  // leave the counter area zero for the next call
+      }
+    }
+    __syncthreads();  // combine area and rings are reused by the next item
+    if (s_abort) break;
+  }
+}
+
+}  // namespace td

@@ -1,0 +1,144 @@
+/*
+ * td.h - split-KV decode attention over a static KV cache, for NVIDIA GB300 (sm_103a).
+ *
+ * A C ABI over hand-written CUDA kernels. Every pointer argument is a device pointer
+ * unless stated otherwise; every buffer is allocated and owned by the caller; the library
+ * allocates nothing, keeps no state beyond a per-device cache of attribute queries, and
+ * may be called from several host threads at once.
+ *
+ * Operations (sources are web pages, cited by title and section):
+ *   td_kv_append   write new key/value rows at position seq_lens[b] of a preallocated
+ *                  cache ("tinydecode", "how the decode step is put together": the cache
+ *                  write is an index_put_ at seq_lens, which live on the device).
+ *   td_decode_attn single-token attention of every query head over its sequence's cache
+ *                  rows j < seq_lens[b], split into key chunks whose partial softmax
+ *                  (m, l, acc) is merged by log-sum-exp ("tinydecode", same section;
+ *                  "llm-decode-cuda", split-KV attention section: one block per kv head
+ *                  and chunk serves the whole query-head group).
+ *   td_verify_attn the same for a chunk of T new query tokens that are causal among
+ *                  themselves ("tinydecode", "speculative decoding": the verify pass over
+ *                  k+1 tokens with the head group folded so the cache is read once).
+ *   td_lse_merge   the log-sum-exp merge of per-split partials on its own.
+ *
+ * Layouts (row-major, contiguous, element type given by td_dtype):
+ *   q, out         [B, Hq, D] for decode; [B, Hq, T, D] for verify
+ *   k/v cache      [B, Hkv, Smax, D]
+ *   seq_lens       int32 [B], on the device
+ *   lse            fp32 [B, Hq] (decode) or [B, Hq, T] (verify); nullable
+ *   partials       fp32 m, l [B, rows, NS]; acc [B, rows, NS, D]  (rows = Hq*T, row = hq*T + t)
+ * Query head hq reads kv head hq / (Hq / Hkv) (contiguous groups, Hq % Hkv == 0).
+ * Accumulation and the softmax statistics are fp32. out is written in the cache's dtype,
+ * rounded to nearest even.
+ *
+ * Errors. Arguments are checked on the host before anything is launched: a bad shape,
+ * a null or misaligned pointer (q, caches, new rows, out and workspace need 16-byte
+ * alignment), an unsupported head dimension or a too-small workspace returns an error
+ * code and launches nothing. TD_ERR_CUDA reports a launch failure (cudaGetLastError).
+ * Problems in device-resident data never stop a kernel: they are clamped or skipped as
+ * described per call and OR a TD_DEV_* bit into *dev_status (a caller-owned device
+ * uint32; pass NULL to ignore them). No call synchronises with the host, allocates, or
+ * reads seq_lens on the host, so every call can be captured in a CUDA graph.
+ *
+ * stream: a cudaStream_t passed as void* (NULL = the legacy default stream).
+ */
+#ifndef TD_H
+#define TD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum td_status {
+  TD_OK = 0,
+  TD_ERR_INVALID_ARG = 1, /* null pointer, bad shape, bad scale */
+  TD_ERR_UNSUPPORTED = 2, /* valid but not built: head dim, dtype, alignment, batch size */
+  TD_ERR_WORKSPACE = 3,   /* workspace missing or smaller than td_decode_workspace_bytes() */
+  TD_ERR_CUDA = 4         /* a CUDA call failed (see td_last_cuda_error) */
+} td_status;
+
+typedef enum td_dtype { TD_F32 = 0, TD_BF16 = 1 } td_dtype;
+
+/* Bits OR-ed into *dev_status by the kernels. */
+#define TD_DEV_SEQLEN_CLAMPED 1u   /* seq_lens[b] > Smax in attention: Smax rows attended */
+#define TD_DEV_APPEND_OVERFLOW 2u  /* append with seq_lens[b] < 0 or seq_lens[b] + T > Smax: b skipped */
+#define TD_DEV_VERIFY_SHORT 4u     /* verify with seq_lens[b] < T: rows that see no key give 0 */
+#define TD_DEV_NEGATIVE_SEQLEN 8u  /* seq_lens[b] < 0 in attention: treated as 0 */
+#define TD_DEV_WAIT_TIMEOUT 16u    /* a bounded wait for an asynchronous copy gave up: output invalid */
+#define TD_DEV_WORKSPACE_DIRTY 32u /* a completion counter was not zero: workspace not zeroed for this
+                                      layout; output invalid (zero the workspace and call again) */
+
+/* Largest batch a call accepts. */
+#define TD_MAX_BATCH 1024
+
+const char *td_status_string(td_status s);
+const char *td_version(void);
+/* Last CUDA error code seen by a call that returned TD_ERR_CUDA on this host thread. */
+int td_last_cuda_error(void);
+
+/*
+ * Workspace for td_decode_attn / td_verify_attn, in bytes, for the current CUDA device.
+ * q_len = T (1 for decode); split as passed to the attention call (0 = automatic).
+ * The workspace holds a counter area followed by per-split partials; their layout follows
+ * the shape arguments. It must be zero-filled (e.g. cudaMemset) before its first use; every
+ * call that runs to completion leaves its counter area zero again, so the workspace can be
+ * reused by later calls with the same (B, Hq, Hkv, Smax, D, q_len, split) on one stream.
+ * Before using it for other shapes, zero it again (or use another). Calls running
+ * concurrently need separate workspaces. Returns 0 for invalid arguments.
+ */
+size_t td_decode_workspace_bytes(int B, int Hq, int Hkv, int Smax, int D, int q_len, int split);
+
+/*
+ * Cache append: for each b with 0 <= L = seq_lens[b] and L + T <= Smax, copies
+ * k_new[b, h, t, :] to k_cache[b, h, L + t, :] (and v likewise) bit for bit for all h < Hkv,
+ * t < T. With advance != 0, seq_lens[b] += T afterwards (same launch, after every read of
+ * seq_lens[b]). A sequence that does not fit is left untouched and sets
+ * TD_DEV_APPEND_OVERFLOW. k_new, v_new: [B, Hkv, T, D]; caches [B, Hkv, Smax, D].
+ */
+td_status td_kv_append(td_dtype dtype, const void *k_new, const void *v_new, void *k_cache, void *v_cache,
+                       int32_t *seq_lens, int B, int Hkv, int T, int Smax, int D, int advance,
+                       uint32_t *dev_status, void *stream);
+
+/*
+ * Decode attention: out[b, hq, :] = softmax_j(scale * q[b, hq, :] . k[b, kvh, j, :]) v[b, kvh, j, :]
+ * over j < L_b = seq_lens[b] (clamped to [0, Smax], see TD_DEV_* bits); L_b = 0 gives
+ * out = 0 and lse = -inf. lse[b, hq] = ln sum_j exp(scale * q . k_j) (nullable).
+ * split: keys per chunk; 0 lets the library size chunks from the device lengths and the
+ * GPU's SM count. The grid depends only on the arguments (never on the lengths), and
+ * chunks past a sequence's length do no work. D must be 64 or 128.
+ */
+td_status td_decode_attn(td_dtype dtype, const void *q, const void *k_cache, const void *v_cache,
+                         const int32_t *seq_lens, int B, int Hq, int Hkv, int Smax, int D, float scale, int split,
+                         void *out, float *lse, void *workspace, size_t workspace_bytes, uint32_t *dev_status,
+                         void *stream);
+
+/*
+ * Verify-chunk attention: query row (hq, t), t < T, attends keys j < L_b - T + t + 1, where
+ * L_b = seq_lens[b] already counts the T new tokens (append them first). q/out [B, Hq, T, D],
+ * lse [B, Hq, T]. A row that sees no key (L_b < T) gives out = 0, lse = -inf and sets
+ * TD_DEV_VERIFY_SHORT. Otherwise as td_decode_attn.
+ */
+td_status td_verify_attn(td_dtype dtype, const void *q, const void *k_cache, const void *v_cache,
+                         const int32_t *seq_lens, int B, int Hq, int Hkv, int T, int Smax, int D, float scale,
+                         int split, void *out, float *lse, void *workspace, size_t workspace_bytes,
+                         uint32_t *dev_status, void *stream);
+
+/*
+ * Log-sum-exp merge of per-split partials computed with split size `split` (>= 1).
+ * For each (b, row) the active splits are s < min(NS, ceil(max(seq_lens[b], 0) / split));
+ * those with l > 0 are merged:
+ *   M = max_s m_s,  Lsum = sum_s l_s exp(m_s - M),  out = sum_s acc_s exp(m_s - M) / Lsum,
+ *   lse = M + ln Lsum.
+ * A row with no such split gets out = 0, lse = -inf. m, l: [B, rows, NS]; acc [B, rows, NS, D]
+ * (acc unnormalised); out [B, rows, D] in out_dtype; lse fp32 [B, rows] (nullable).
+ * D must be a multiple of 4 and at most 1024.
+ */
+td_status td_lse_merge(const float *m, const float *l, const float *acc, const int32_t *seq_lens, int B, int rows,
+                       int NS, int D, int split, td_dtype out_dtype, void *out, float *lse, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* TD_H */

@@ -1,0 +1,135 @@
+"""The C-ABI library without a GPU: it builds, loads, exports what include/td.h declares,
+and rejects bad arguments on the host before touching CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from decode_attention_split_gb300 import build as td_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "td.h")
+
+TD_OK, TD_ERR_INVALID_ARG, TD_ERR_UNSUPPORTED, TD_ERR_WORKSPACE, TD_ERR_CUDA = range(5)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    path = td_build.build()
+    from decode_attention_split_gb300 import _lib
+    assert os.path.samefile(path, _lib.LIB_PATH)
+    return _lib.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(td_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_calls():
+    names = declared_functions()
+    for n in ("td_kv_append", "td_decode_attn", "td_verify_attn", "td_lse_merge", "td_decode_workspace_bytes"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    from decode_attention_split_gb300 import _lib
+    names = declared_functions()
+    assert sorted(_lib.SYMBOLS) == names
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_no_cuda_runtime_symbols_leak(lib):
+    # the static CUDA runtime stays private to the library
+    raw = ctypes.CDLL(lib._name)
+    with pytest.raises(AttributeError):
+        raw.cudaMalloc  # noqa: B018
+
+
+def test_status_strings(lib):
+    assert lib.td_status_string(TD_OK) == b"ok"
+    assert b"workspace" in lib.td_status_string(TD_ERR_WORKSPACE)
+    assert lib.td_version().startswith(b"td ")
+
+
+FAKE = 0x10000  # a 16-byte aligned address the host never dereferences
+
+
+def _decode(lib, **kw):
+    a = dict(dtype=1, q=FAKE, k=FAKE, v=FAKE, sl=FAKE, B=1, Hq=4, Hkv=2, Smax=64, D=128, scale=0.1, split=0,
+             out=FAKE, lse=None, ws=FAKE, wsb=1 << 20, st=None, stream=None)
+    a.update(kw)
+    return lib.td_decode_attn(a["dtype"], a["q"], a["k"], a["v"], a["sl"], a["B"], a["Hq"], a["Hkv"], a["Smax"],
+                              a["D"], a["scale"], a["split"], a["out"], a["lse"], a["ws"], a["wsb"], a["st"],
+                              a["stream"])
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(q=None), TD_ERR_INVALID_ARG),
+    (dict(out=None), TD_ERR_INVALID_ARG),
+    (dict(sl=None), TD_ERR_INVALID_ARG),
+    (dict(Hq=5, Hkv=2), TD_ERR_INVALID_ARG),
+    (dict(B=0), TD_ERR_INVALID_ARG),
+    (dict(split=-1), TD_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), TD_ERR_INVALID_ARG),
+    (dict(D=96), TD_ERR_UNSUPPORTED),
+    (dict(dtype=7), TD_ERR_UNSUPPORTED),
+    (dict(B=1025), TD_ERR_UNSUPPORTED),
+])
+def test_decode_rejects_bad_arguments_on_host(lib, kw, expect):
+    assert _decode(lib, **kw) == expect
+
+
+def test_verify_rejects_chunk_longer_than_cache(lib):
+    st = lib.td_verify_attn(1, FAKE, FAKE, FAKE, FAKE, 1, 4, 2, 65, 64, 128, 0.1, 0, FAKE, None, FAKE, 1 << 20, None,
+                            None)
+    assert st == TD_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(k_new=None), TD_ERR_INVALID_ARG),
+    (dict(T=0), TD_ERR_INVALID_ARG),
+    (dict(D=4), TD_ERR_UNSUPPORTED),             # a bf16 row of 8 bytes is not a whole 16-byte vector
+    (dict(k_cache=FAKE + 8), TD_ERR_UNSUPPORTED),  # misaligned
+    (dict(dtype=3), TD_ERR_UNSUPPORTED),
+])
+def test_append_rejects_bad_arguments_on_host(lib, kw, expect):
+    a = dict(dtype=1, k_new=FAKE, v_new=FAKE, k_cache=FAKE, v_cache=FAKE, sl=FAKE, B=2, Hkv=2, T=1, Smax=16, D=64)
+    a.update(kw)
+    st = lib.td_kv_append(a["dtype"], a["k_new"], a["v_new"], a["k_cache"], a["v_cache"], a["sl"], a["B"],
+                          a["Hkv"], a["T"], a["Smax"], a["D"], 1, None, None)
+    assert st == expect
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(m=None), TD_ERR_INVALID_ARG),
+    (dict(split=0), TD_ERR_INVALID_ARG),
+    (dict(D=6), TD_ERR_UNSUPPORTED),
+    (dict(D=2048), TD_ERR_UNSUPPORTED),
+    (dict(out_dtype=5), TD_ERR_UNSUPPORTED),
+])
+def test_merge_rejects_bad_arguments_on_host(lib, kw, expect):
+    a = dict(m=FAKE, l=FAKE, acc=FAKE, sl=FAKE, B=1, rows=4, NS=3, D=64, split=16, out_dtype=0, out=FAKE)
+    a.update(kw)
+    st = lib.td_lse_merge(a["m"], a["l"], a["acc"], a["sl"], a["B"], a["rows"], a["NS"], a["D"], a["split"],
+                          a["out_dtype"], a["out"], None, None)
+    assert st == expect
+
+
+def test_hot_kernels_have_no_spills(lib):
+    """Register gate (ptxas): the instantiations the workloads run keep every value in registers."""
+    log = open(td_build.PTXAS_LOG).read()
+    entries = re.findall(r"Compiling entry function '(\w+)'.*?\n(?:.*?\n)*?\s+(\d+) bytes stack frame, (\d+) bytes "
+                         r"spill stores, (\d+) bytes spill loads", log)
+    hot = {"split_attn_kernelI13__nv_bfloat16Li128ELi4E", "split_attn_kernelI13__nv_bfloat16Li64ELi4E",
+           "split_attn_kernelIfLi64ELi2E"}
+    seen = set()
+    for name, _stack, st, ld in entries:
+        for h in hot:
+            if h in name:
+                seen.add(h)
+                assert int(st) == 0 and int(ld) == 0, (name, st, ld)
+    assert seen == hot
