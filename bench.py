@@ -423,7 +423,7 @@ def run_td(args, world, rank, local):
         "gpu_launches": 2 * total_calls,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "kernel": "split_attn_kernel<bf16,128,4> (fused split + merge), timed alone",
+                     "kernel": "split_attn_mma_kernel<128,1> (fused split + merge, mma.sync bf16), timed alone",
                      "us_per_launch": round(us_attn, 3), "peak_kind": f"hbm_gbs of {peak_kind}",
                      "algorithmic_bytes_per_launch": bytes_call},
         "e2e": e2e,

@@ -41,9 +41,7 @@ td_status attn(td_dtype dtype, const void *q, const void *k_cache, const void *v
   p.seq_lens = seq_lens;
   p.out = out;
   p.lse = lse;
-  p.ws_m = reinterpret_cast<float *>(ws + plan.off_m);
-  p.ws_l = reinterpret_cast<float *>(ws + plan.off_l);
-  p.ws_acc = reinterpret_cast<float *>(ws + plan.off_acc);
+  p.ws_part = reinterpret_cast<float *>(ws + plan.off_part);
   p.counters = reinterpret_cast<int *>(ws);
   p.status = dev_status;
   p.B = B;
@@ -57,6 +55,7 @@ td_status attn(td_dtype dtype, const void *q, const void *k_cache, const void *v
   p.split = split;
   p.ns_ws = plan.ns_ws;
   p.p_target = plan.p_target;
+  p.min_chunk = plan.min_chunk;
   p.qscale = scale * td::kLog2e;
   const cudaError_t e = td::launch_split(dtype, D, plan, p, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? TD_OK : cuda_fail(e);

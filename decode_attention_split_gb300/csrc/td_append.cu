@@ -18,6 +18,8 @@ __global__ void __launch_bounds__(kAppendThreads) kv_append_kernel(const uint4 *
                                                                    int advance, uint32_t *status) {
   __shared__ int s_start;
   const int b = blockIdx.x;
+  griddep_wait();  // the cache and lengths may come from the previous kernel in the stream
+  griddep_launch_dependents();
   if (threadIdx.x == 0) {
     const long long L = seq_lens[b];
     const bool fits = L >= 0 && L + T <= Smax;
@@ -46,10 +48,9 @@ cudaError_t launch_append(size_t elem_bytes, const void *k_new, const void *v_ne
                           int32_t *seq_lens, int B, int Hkv, int T, int Smax, int D, int advance,
                           uint32_t *dev_status, cudaStream_t stream) {
   const int vec_per_row = (int)((size_t)D * elem_bytes / 16);
-  kv_append_kernel<<<B, kAppendThreads, 0, stream>>>(
-      static_cast<const uint4 *>(k_new), static_cast<const uint4 *>(v_new), static_cast<uint4 *>(k_cache),
-      static_cast<uint4 *>(v_cache), seq_lens, Hkv, T, Smax, vec_per_row, advance, dev_status);
-  return cudaGetLastError();
+  return launch_pdl(kv_append_kernel, dim3(B), dim3(kAppendThreads), 0, stream, static_cast<const uint4 *>(k_new),
+                    static_cast<const uint4 *>(v_new), static_cast<uint4 *>(k_cache), static_cast<uint4 *>(v_cache),
+                    seq_lens, Hkv, T, Smax, vec_per_row, advance, dev_status);
 }
 
 }  // namespace td

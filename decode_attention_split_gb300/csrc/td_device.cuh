@@ -62,6 +62,20 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity)
   return true;
 }
 
+// Orders this thread's earlier generic-proxy global accesses (and those it has observed, e.g.
+// partials other CTAs published before an atomic ticket) before its later asynchronous-proxy
+// (bulk copy) accesses.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// Programmatic dependent launch: wait until the grids this one depends on have completed and
+// their writes are visible; allow the next grid in the stream to be scheduled early.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // L2 policy for data read exactly once (the KV stream): evict it first.
 __device__ __forceinline__ uint64_t l2_evict_first_policy() {
   uint64_t pol;
@@ -78,6 +92,13 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
           dst),
       "l"(src), "r"(bytes), "r"(bar), "l"(policy)
       : "memory");
+}
+
+// Bulk copy global -> shared without a cache hint (16-byte multiples, as bulk_g2s).
+__device__ __forceinline__ void bulk_g2s_plain(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
 }
 
 // ---- widening of stored elements to fp32 ----------------------------------------------

@@ -13,14 +13,16 @@ struct SplitParams;
 
 // Launch geometry and workspace layout of one split-attention call.
 struct SplitPlan {
-  int RP;        // padded query rows per CTA (1, 2, 4 or 8)
+  bool mma;      // tensor-core kernel (bf16) or CUDA-core kernel
+  int RP;        // CUDA-core: padded query rows per CTA (1, 2, 4 or 8); tensor-core: m tiles (1 or 2)
   int R;         // real query rows per CTA
   int RB;        // row blocks per kv head
   int ns_ws;     // partial slots per query row
   int p_target;  // CTAs that fill the GPU once
   int grid;      // CTAs launched
   int smem;      // dynamic shared memory per CTA
-  size_t off_m, off_l, off_acc, bytes;  // workspace layout
+  int min_chunk; // smallest automatic chunk (keys)
+  size_t off_part, bytes;  // workspace layout: counters, then partial blocks
 };
 
 // Fills *plan for the current device; TD_OK, or an error for unsupported shapes.
@@ -37,5 +39,24 @@ cudaError_t launch_append(size_t elem_bytes, const void *k_new, const void *v_ne
 
 // SM count of the current device (cached per device).
 int device_sm_count(int device);
+
+// Launches `kernel` with programmatic dependent launch allowed: its CTAs may be scheduled
+// while the previous kernel in the stream drains; every td kernel starts with a
+// griddepcontrol.wait, so it still sees all of that kernel's writes.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
 
 }  // namespace td

@@ -15,18 +15,22 @@ __global__ void __launch_bounds__(kMergeThreads) lse_merge_kernel(const float *m
                                                                    int split, OutE *out, float *lse) {
   __shared__ float factors[R * kMergeBlock];
   __shared__ float stats[2 * R];
+  __shared__ long long rowbase[R], out_row[R];
   const int b = blockIdx.y;
+  griddep_wait();  // partials may come from the previous kernel in the stream
+  griddep_launch_dependents();
   const long long L = seq_lens[b] < 0 ? 0 : seq_lens[b];
   long long nc = (L + split - 1) / split;
   if (nc > NS) nc = NS;
-  long long rowbase[R], out_row[R];
-#pragma unroll
-  for (int r = 0; r < R; ++r) {
+  if (threadIdx.x < R) {
+    const int r = threadIdx.x;
     const int row = blockIdx.x * R + r;
     out_row[r] = (long long)b * rows + row;
     rowbase[r] = row < rows ? out_row[r] * NS : -1;
   }
-  merge_rows<R, OutE>(m, l, acc, rowbase, out_row, (int)nc, D, out, lse, factors, stats);
+  __syncthreads();
+  // at most 8 (row, dim) pairs per thread: R * D <= 8 * kMergeThreads (D <= 256 for R = 4, 1024 for R = 1)
+  merge_rows<R, kMergeThreads, 8, OutE>(m, l, acc, rowbase, out_row, (int)nc, D, out, lse, factors, stats);
 }
 
 template <int R>
@@ -34,11 +38,11 @@ void launch_r(const float *m, const float *l, const float *acc, const int32_t *s
               int D, int split, td_dtype out_dtype, void *out, float *lse, cudaStream_t stream) {
   const dim3 grid((rows + R - 1) / R, B);
   if (out_dtype == TD_F32)
-    lse_merge_kernel<R, float><<<grid, kMergeThreads, 0, stream>>>(m, l, acc, seq_lens, rows, NS, D, split,
-                                                                   static_cast<float *>(out), lse);
+    launch_pdl(lse_merge_kernel<R, float>, grid, dim3(kMergeThreads), 0, stream, m, l, acc, seq_lens, rows, NS, D,
+               split, static_cast<float *>(out), lse);
   else
-    lse_merge_kernel<R, __nv_bfloat16><<<grid, kMergeThreads, 0, stream>>>(
-        m, l, acc, seq_lens, rows, NS, D, split, static_cast<__nv_bfloat16 *>(out), lse);
+    launch_pdl(lse_merge_kernel<R, __nv_bfloat16>, grid, dim3(kMergeThreads), 0, stream, m, l, acc, seq_lens, rows,
+               NS, D, split, static_cast<__nv_bfloat16 *>(out), lse);
 }
 
 }  // namespace

@@ -3,13 +3,14 @@
 
 #include "td_internal.h"
 #include "td_split_attn.cuh"
+#include "td_split_mma.cuh"
 
 namespace td {
 
 namespace {
 
 constexpr int kMaxDevices = 64;
-constexpr int kKernelSlots = 2 * 2 * 4;  // dtype x head dim x row padding
+constexpr int kKernelSlots = 2 * 2 * 4 + 2 * 2;  // CUDA-core: dtype x D x row padding; mma: D x m tiles
 
 struct KernelRef {
   const void *fn;
@@ -19,7 +20,7 @@ struct KernelRef {
 
 template <typename E, int D, int RP>
 void launch_one(const SplitParams &p, int grid, int smem, cudaStream_t stream) {
-  split_attn_kernel<E, D, RP><<<grid, kThreads, smem, stream>>>(p);
+  launch_pdl(split_attn_kernel<E, D, RP>, dim3(grid), dim3(kThreads), smem, stream, p);
 }
 
 template <typename E, int D, int RP>
@@ -54,19 +55,42 @@ KernelRef pick_d(int D, int RP) {
   return KernelRef{nullptr, 0, nullptr};
 }
 
-KernelRef pick(td_dtype dtype, int D, int RP) {
-  return dtype == TD_F32 ? pick_d<float>(D, RP) : pick_d<__nv_bfloat16>(D, RP);
+template <int D, int MT>
+void launch_mma(const SplitParams &p, int grid, int smem, cudaStream_t stream) {
+  launch_pdl(split_attn_mma_kernel<D, MT>, dim3(grid), dim3(kThreads), smem, stream, p);
 }
 
-int slot_of(td_dtype dtype, int D, int RP) { return ((dtype == TD_F32 ? 0 : 1) * 2 + (D == 64 ? 0 : 1)) * 4 + rp_index(RP); }
+template <int D, int MT>
+KernelRef mma_ref_of() {
+  static_assert(MmaCfg<D, MT>::kFits, "mma kernel shared memory");
+  return KernelRef{reinterpret_cast<const void *>(&split_attn_mma_kernel<D, MT>), MmaCfg<D, MT>::SMEM_BYTES,
+                   &launch_mma<D, MT>};
+}
+
+KernelRef pick_mma(int D, int MT) {
+  if (MT != 1) return KernelRef{nullptr, 0, nullptr};
+  if (D == 64) return mma_ref_of<64, 1>();
+  if (D == 128) return mma_ref_of<128, 1>();
+  return KernelRef{nullptr, 0, nullptr};
+}
+
+// variant: row padding RP of the CUDA-core kernel, or m tiles MT of the tensor-core kernel
+KernelRef pick(td_dtype dtype, int D, bool mma, int variant) {
+  if (mma) return pick_mma(D, variant);
+  return dtype == TD_F32 ? pick_d<float>(D, variant) : pick_d<__nv_bfloat16>(D, variant);
+}
+
+int slot_of(td_dtype dtype, int D, bool mma, int variant) {
+  if (mma) return 16 + (D == 64 ? 0 : 2) + (variant == 1 ? 0 : 1);
+  return ((dtype == TD_F32 ? 0 : 1) * 2 + (D == 64 ? 0 : 1)) * 4 + rp_index(variant);
+}
 
 std::mutex g_mu;
 int g_sms[kMaxDevices];
 int g_blocks[kMaxDevices][kKernelSlots];  // resident CTAs per SM (0 = not yet queried)
 
 // Sets the shared-memory opt-in once per device and returns the resident CTAs per SM.
-int blocks_per_sm(int device, td_dtype dtype, int D, int RP, const KernelRef &k) {
-  const int slot = slot_of(dtype, D, RP);
+int blocks_per_sm(int device, int slot, const KernelRef &k) {
   std::lock_guard<std::mutex> lock(g_mu);
   if (device >= 0 && device < kMaxDevices && g_blocks[device][slot] > 0) return g_blocks[device][slot];
   if (cudaFuncSetAttribute(k.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, k.smem) != cudaSuccess) return 0;
@@ -98,20 +122,32 @@ td_status plan_split(td_dtype dtype, int B, int Hq, int Hkv, int T, int Smax, in
   if (B < 1 || Hq < 1 || Hkv < 1 || T < 1 || Smax < 1 || split < 0 || Hq % Hkv != 0) return TD_ERR_INVALID_ARG;
   if (B > TD_MAX_BATCH || Smax > (1 << 30) || T > Smax) return TD_ERR_UNSUPPORTED;
   const long long GT = (long long)(Hq / Hkv) * T;
-  const int rmax = D == 128 ? 4 : 8;
-  const int R = (int)(GT < rmax ? GT : rmax);
-  int RP = 1;
-  while (RP < R) RP <<= 1;
-  // a 512-byte fp32 row makes a one-row CTA's 32-key stages too large: pad to two rows
-  if (dtype == TD_F32 && D == 128 && RP < 2) RP = 2;
+  // bf16 caches: tensor-core kernel, one 16-row m tile per CTA, the group's rows split evenly
+  // over ceil(rows / 16) row blocks (a 24-row verify chunk: two blocks of 12, whose second
+  // read of each K/V tile is mostly served by L2, and two half-size merges in parallel);
+  // fp32 caches: CUDA-core kernel, up to 4 (D = 128) or 8 (D = 64) rows per CTA
+  const bool mma = dtype == TD_BF16;
+  int R, variant;
+  if (mma) {
+    variant = 1;
+    const long long blocks = (GT + 15) / 16;
+    R = (int)((GT + blocks - 1) / blocks);
+  } else {
+    const int rmax = D == 128 ? 4 : 8;
+    R = (int)(GT < rmax ? GT : rmax);
+    variant = 1;
+    while (variant < R) variant <<= 1;
+    // a 512-byte fp32 row makes a one-row CTA's 32-key stages too large: pad to two rows
+    if (dtype == TD_F32 && D == 128 && variant < 2) variant = 2;
+  }
   const long long RB = (GT + R - 1) / R;
   const long long U = (long long)Hkv * RB;
-  const KernelRef k = pick(dtype, D, RP);
+  const KernelRef k = pick(dtype, D, mma, variant);
   if (k.fn == nullptr) return TD_ERR_UNSUPPORTED;
   int device = 0;
   if (cudaGetDevice(&device) != cudaSuccess) return TD_ERR_CUDA;
   const int sms = device_sm_count(device);
-  const int per_sm = blocks_per_sm(device, dtype, D, RP, k);
+  const int per_sm = blocks_per_sm(device, slot_of(dtype, D, mma, variant), k);
   if (sms <= 0 || per_sm <= 0) return TD_ERR_CUDA;
   const long long p_target = (long long)sms * per_sm;
   long long ns;
@@ -125,7 +161,8 @@ td_status plan_split(td_dtype dtype, int B, int Hq, int Hkv, int T, int Smax, in
   }
   const long long items_max = (long long)B * U * ns;
   if (items_max >= (1LL << 31)) return TD_ERR_UNSUPPORTED;
-  plan->RP = RP;
+  plan->mma = mma;
+  plan->RP = variant;
   plan->R = R;
   plan->RB = (int)RB;
   plan->ns_ws = (int)ns;
@@ -133,20 +170,19 @@ td_status plan_split(td_dtype dtype, int B, int Hq, int Hkv, int T, int Smax, in
   plan->grid = (int)(items_max < p_target ? items_max : p_target);
   if (plan->grid < 1) plan->grid = 1;
   plan->smem = k.smem;
-  const size_t rows = (size_t)B * Hq * T;
+  // a chunk must stream enough keys to amortise its fixed costs (tensor-core kernel: two stages)
+  plan->min_chunk = mma ? 128 : 32;
   const size_t counters = align256((size_t)B * U * sizeof(int));
-  plan->off_m = counters;
-  plan->off_l = plan->off_m + align256(rows * ns * sizeof(float));
-  plan->off_acc = plan->off_l + align256(rows * ns * sizeof(float));
-  plan->bytes = plan->off_acc + align256(rows * ns * D * sizeof(float));
+  plan->off_part = counters;
+  plan->bytes = plan->off_part + align256((size_t)B * U * ns * part_block_floats(R, D) * sizeof(float));
   return TD_OK;
 }
 
 cudaError_t launch_split(td_dtype dtype, int D, const SplitPlan &plan, const SplitParams &p, cudaStream_t stream) {
-  const KernelRef k = pick(dtype, D, plan.RP);
+  const KernelRef k = pick(dtype, D, plan.mma, plan.RP);
   if (k.fn == nullptr) return cudaErrorInvalidValue;
   k.launch(p, plan.grid, plan.smem, stream);
-  return cudaGetLastError();
+  return cudaPeekAtLastError() != cudaSuccess ? cudaGetLastError() : cudaSuccess;
 }
 
 }  // namespace td

@@ -42,9 +42,7 @@ struct SplitParams {
   const int32_t *seq_lens;
   void *out;            // [B, Hq, T, D]
   float *lse;           // [B, Hq, T] or null
-  float *ws_m;          // [B, Hq*T, ns_ws]
-  float *ws_l;
-  float *ws_acc;        // [B, Hq*T, ns_ws, D]
+  float *ws_part;       // [B, Hkv, RB][ns_ws] partial blocks (see part_block_floats)
   int *counters;        // [B, Hkv, RB]
   uint32_t *status;
   int B, Hq, Hkv, G, T, Smax;
@@ -53,8 +51,23 @@ struct SplitParams {
   int split;            // fixed chunk size, or 0 = chosen on the device
   int ns_ws;            // partial slots per row in the workspace
   int p_target;         // CTAs the automatic chunk size aims to fill
+  int min_chunk;        // smallest automatic chunk (keys)
   float qscale;         // scale * log2(e)
 };
+
+// A chunk's partial result for its row block: acc[R][D] (unnormalised p @ V sums), then
+// m[R] (natural-log units) and l[R]; padded to whole 16-byte units so blocks can be
+// bulk-copied and every acc row is 16-byte aligned.
+__host__ __device__ constexpr int part_block_floats(int R, int D) { return (R * (D + 2) + 3) / 4 * 4; }
+
+// Ticket on a completion counter: release (the CTA's partial writes, ordered before this by
+// a barrier, become visible first) and acquire (other CTAs' released writes are visible
+// after it). Returns the previous count.
+__device__ __forceinline__ int ticket_acq_rel(int *cnt) {
+  int prev;
+  asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], 1;" : "=r"(prev) : "l"(cnt) : "memory");
+  return prev;
+}
 
 template <typename E, int D, int RP>
 struct SplitCfg {
@@ -73,12 +86,12 @@ struct SplitCfg {
   static constexpr int RING_BYTES = kStages * STAGE_BYTES;  // per warp
   static constexpr int STASH_FLOATS = KB * RP + 8;
   static constexpr int COMBINE_FLOATS = kWarps * RP * (D + 2);
-  static constexpr int MERGE_FLOATS = RP * kMergeBlock + 2 * RP;
+  static constexpr int MERGE_FLOATS = 0;
   static constexpr int SMEM_BYTES = kWarps * RING_BYTES + kWarps * STASH_FLOATS * 4 + kWarps * kStages * 8;
   static_assert(NV % 8 == 0, "cache row must hold a multiple of 8 16-byte vectors");
   static_assert(D % 32 == 0, "head dim multiple of 32");
   static_assert(RP == 1 || RP == 2 || RP == 4 || RP == 8, "row padding is a power of two <= 8");
-  static_assert((COMBINE_FLOATS + MERGE_FLOATS) * 4 <= kWarps * RING_BYTES, "combine area fits in the rings");
+  static_assert(COMBINE_FLOATS * 4 <= kWarps * RING_BYTES, "combine area fits in the rings");
   static_assert(TKW % KB == 0, "stage holds whole batches");
   // fits next to the ~8.3 KB of static shared memory within the 227 KB a CTA may use
   static constexpr bool kFits = SMEM_BYTES + 8448 <= 227 * 1024;
@@ -88,13 +101,14 @@ __device__ __forceinline__ int clamp_len(int32_t L, int Smax) { return L < 0 ? 0
 
 // Exclusive prefix over the per-sequence item counts, computed by the whole CTA.
 // s_len[b] receives the clamped length; returns the chunk size through *s_chunk and the
-// item total in s_prefix[B].
+// item total in s_prefix[B]. s_red holds 2 * kWarps values.
 static __device__ void plan_items(const SplitParams &p, int *s_len, int *s_prefix, int *s_chunk, long long *s_red) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int U = p.Hkv * p.RB;
   constexpr int kSeg = (TD_MAX_BATCH + kThreads - 1) / kThreads;
   const int b0 = tid * kSeg;
   long long tot = 0;
+  int lmax = 0;
   uint32_t bits = 0;
 #pragma unroll
   for (int i = 0; i < kSeg; ++i) {
@@ -107,26 +121,40 @@ static __device__ void plan_items(const SplitParams &p, int *s_len, int *s_prefi
       if (p.T > 1 && L < p.T) bits |= TD_DEV_VERIFY_SHORT;
       s_len[b] = L;
       tot += L;
+      lmax = max(lmax, L);
     }
   }
   if (blockIdx.x == 0) report(p.status, bits);
   // total keys over the batch
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
-  if (lane == 0) s_red[warp] = tot;
+  for (int o = 16; o > 0; o >>= 1) {
+    tot += __shfl_xor_sync(0xffffffffu, tot, o);
+    lmax = max(lmax, __shfl_xor_sync(0xffffffffu, lmax, o));
+  }
+  if (lane == 0) {
+    s_red[warp] = tot;
+    s_red[kWarps + warp] = lmax;
+  }
   __syncthreads();
   if (tid == 0) {
     long long all = 0;
-    for (int w = 0; w < kWarps; ++w) all += s_red[w];
+    int longest = 0;
+    for (int w = 0; w < kWarps; ++w) {
+      all += s_red[w];
+      longest = max(longest, (int)s_red[kWarps + w]);
+    }
     int S;
     if (p.split > 0) {
       S = p.split;
     } else {
-      long long want = (all * U + p.p_target - 1) / p.p_target;  // keys per item to fill the grid
+      // keys per item so the items fill the grid once; then every sequence has at most
+      // ceil(p_target / U) chunks, which is what the workspace holds (the guard below only
+      // restates that bound)
+      long long want = (all * U + p.p_target - 1) / p.p_target;
       want = (want + 15) / 16 * 16;
-      if (want < 16) want = 16;
-      const long long floor_ws = ((long long)p.Smax + p.ns_ws - 1) / p.ns_ws;  // keeps chunks <= ns_ws
-      if (want < floor_ws) want = floor_ws;
+      if (want < p.min_chunk) want = p.min_chunk;
+      const long long fits = ((long long)longest + p.ns_ws - 1) / p.ns_ws;
+      if (want < fits) want = fits;
       S = (int)(want > p.Smax ? p.Smax : want);
       if (S < 1) S = 1;
     }
@@ -168,14 +196,209 @@ static __device__ void plan_items(const SplitParams &p, int *s_len, int *s_prefi
   __syncthreads();
 }
 
+// Shared memory (floats) the fused merge needs besides the staged partial blocks.
+template <int D, int ROWS>
+__host__ __device__ constexpr int merge_fixed_floats() {
+  return ROWS * D + 4 * ROWS + ROWS * 64;
+}
+
+// Output row (flattened [B, Hq*T]) of local row r of row block rb of kv head kvh.
+__device__ __forceinline__ long long out_row_of(const SplitParams &p, int b, int kvh, int rb, int r) {
+  const int gr = rb * p.R + r;
+  return (long long)b * p.Hq * p.T + (long long)(kvh * p.G + gr / p.T) * p.T + gr % p.T;
+}
+
+// Log-sum-exp merge of the NC chunk partials of (b, kv head, row block), run by the CTA that
+// took the last completion ticket; rows r < nv exist. The group's partial blocks are
+// contiguous in the workspace, so they cross from L2 in bulk asynchronous copies, as many
+// chunks at a time as the free shared memory holds, and are merged online: per row the
+// running maximum M, normaliser Lsum and weighted sum are rescaled when a block raises M.
+// `smem_f` spans `smem_floats` floats no one else uses now; `bar` is this CTA's merge
+// mbarrier and `phase` its current parity (uniform across the CTA).
+template <typename E, int D, int ROWS>
+__device__ void merge_group(const SplitParams &p, float *smem_f, int smem_floats, uint64_t *bar, uint32_t &phase,
+                            int b, int kvh, int rb, int NC, int nv) {
+  constexpr int kFB = 64;  // most chunks staged at a time
+  constexpr int D4 = D / 4;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int R = p.R;
+  const int BF = part_block_floats(R, D);
+  const long long g = ((long long)b * p.Hkv + kvh) * p.RB + rb;
+  const float *src = p.ws_part + g * p.ns_ws * (long long)BF;
+  float *acc = smem_f;          // [ROWS][D] running weighted sums
+  float *st = acc + ROWS * D;   // M[ROWS], Lsum[ROWS], rescale[ROWS], (pad)
+  float *fac = st + 4 * ROWS;   // [ROWS][kFB] factors exp(m_c - M) of the staged chunks
+  float *stage = fac + ROWS * kFB;
+  int FB = (smem_floats - merge_fixed_floats<D, ROWS>()) / BF;
+  if (FB > kFB) FB = kFB;
+#pragma unroll 1
+  for (int i = tid; i < nv * D; i += kThreads) acc[i] = 0.f;
+  if (tid < nv) {
+    st[tid] = -INFINITY;
+    st[ROWS + tid] = 0.f;
+  }
+#pragma unroll 1
+  for (int c0 = 0; c0 < NC; c0 += FB) {
+    const int nb = min(FB, NC - c0);
+    if (tid == 0) {
+      fence_proxy_async_global();
+      mbar_arrive_expect_tx(smem_u32(bar), (uint32_t)(nb * BF * 4));
+      bulk_g2s_plain(smem_u32(stage), src + (long long)c0 * BF, (uint32_t)(nb * BF * 4), smem_u32(bar));
+    }
+    if (!mbar_wait_bounded(smem_u32(bar), phase)) {
+      report(p.status, TD_DEV_WAIT_TIMEOUT);
+      mbar_wait_bounded(smem_u32(bar), phase);  // one more bounded wait for the copy in flight
+    }
+    phase ^= 1u;
+    __syncthreads();  // staged blocks and the previous round's statistics are visible
+    // per-row statistics of this block: a warp per row, lanes over chunks
+#pragma unroll 1
+    for (int r = warp; r < nv; r += kWarps) {
+      float mv[2], lv[2];
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const int c = lane + 32 * k;
+        lv[k] = c < nb ? stage[c * BF + R * D + R + r] : 0.f;
+        mv[k] = lv[k] > 0.f ? stage[c * BF + R * D + r] : -INFINITY;
+      }
+      float bm = fmaxf(mv[0], mv[1]);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, o));
+      const float Mo = st[r];
+      const float Mn = fmaxf(Mo, bm);
+      const float base = Mn == -INFINITY ? 0.f : Mn;
+      float ls = 0.f;
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const float f = lv[k] > 0.f ? expf(mv[k] - base) : 0.f;
+        if (lane + 32 * k < nb) fac[r * kFB + lane + 32 * k] = f;
+        ls = fmaf(lv[k], f, ls);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) ls += __shfl_xor_sync(0xffffffffu, ls, o);
+      if (lane == 0) {
+        const float alpha = expf(Mo - base);
+        st[r] = Mn;
+        st[ROWS + r] = st[ROWS + r] * alpha + ls;
+        st[2 * ROWS + r] = alpha;
+      }
+    }
+    __syncthreads();
+    // weighted sums, four dims per thread
+#pragma unroll 1
+    for (int idx = tid; idx < nv * D4; idx += kThreads) {
+      const int r = idx / D4, d = (idx % D4) * 4;
+      const float *a = stage + r * D + d;
+      const float *f = fac + r * kFB;
+      const float sc = st[2 * ROWS + r];
+      float4 x = *reinterpret_cast<const float4 *>(acc + r * D + d);
+      x.x *= sc, x.y *= sc, x.z *= sc, x.w *= sc;
+#pragma unroll 4
+      for (int c = 0; c < nb; ++c) {
+        const float4 v = *reinterpret_cast<const float4 *>(a + c * BF);
+        const float w = f[c];
+        x.x = fmaf(v.x, w, x.x), x.y = fmaf(v.y, w, x.y), x.z = fmaf(v.z, w, x.z), x.w = fmaf(v.w, w, x.w);
+      }
+      *reinterpret_cast<float4 *>(acc + r * D + d) = x;
+    }
+    __syncthreads();  // the next block overwrites the staging area
+  }
+#pragma unroll 1
+  for (int idx = tid; idx < nv * D; idx += kThreads) {
+    const int r = idx / D, d = idx % D;
+    const long long orow = out_row_of(p, b, kvh, rb, r);
+    const float Ls = st[ROWS + r];
+    store_elem<E>(static_cast<E *>(p.out) + orow * D + d, Ls > 0.f ? acc[idx] / Ls : 0.f);
+    if (d == 0 && p.lse != nullptr) p.lse[orow] = Ls > 0.f ? st[r] + logf(Ls) : -INFINITY;
+  }
+}
+
+// Completes one work item (sequence b, kv head, row block rb, chunk c of NC).
+// The item's partial sources (warps or key slices) have written, in base-2 units,
+//   cm[NSRC][ROWS] (row max), cl[NSRC][ROWS] (row sum), ca[NSRC][ROWS][D] (unnormalised p @ V)
+// at the start of the CTA's shared memory (`smem_f`, `smem_floats` floats free after this
+// call's combine), and a __syncthreads has made them visible. The sources are combined; a
+// chunk that is its sequence's only one writes out/lse, any other writes its partial block
+// to the workspace and takes a completion ticket, and the CTA holding the last ticket of
+// (b, kv head, row block) merges all chunks and zeroes the counter again. Ends with a
+// __syncthreads (the shared areas may be reused afterwards).
+template <typename E, int D, int ROWS, int NSRC>
+__device__ void finish_item(const SplitParams &p, float *smem_f, int smem_floats, uint64_t *merge_bar,
+                            uint32_t &merge_phase, int b, int kvh, int rb, int c, int NC, int *s_last) {
+  constexpr int D4 = D / 4;
+  const int tid = threadIdx.x;
+  const int GT = p.G * p.T;
+  const int R = p.R;
+  const float *cm = smem_f;
+  const float *cl = smem_f + NSRC * ROWS;
+  const float *ca = smem_f + 2 * NSRC * ROWS;
+  const bool single = NC == 1;
+  const int nv = min(R, GT - rb * R);  // rows of this block that exist
+  const long long g = ((long long)b * p.Hkv + kvh) * p.RB + rb;
+  float *blk = p.ws_part + (g * p.ns_ws + c) * (long long)part_block_floats(R, D);
+#pragma unroll 1
+  for (int idx = tid; idx < nv * D4; idx += kThreads) {
+    const int r = idx / D4, d = (idx % D4) * 4;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < NSRC; ++w) M = fmaxf(M, cm[w * ROWS + r]);
+    float Ls = 0.f;
+    float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < NSRC; ++w) {
+        const float mw = cm[w * ROWS + r];
+        if (mw != -INFINITY) {
+          const float f = exp2f(mw - M);
+          Ls = fmaf(cl[w * ROWS + r], f, Ls);
+          const float4 v = *reinterpret_cast<const float4 *>(ca + (w * ROWS + r) * D + d);
+          A.x = fmaf(v.x, f, A.x), A.y = fmaf(v.y, f, A.y), A.z = fmaf(v.z, f, A.z), A.w = fmaf(v.w, f, A.w);
+        }
+      }
+    }
+    if (single) {
+      const long long row = out_row_of(p, b, kvh, rb, r);
+      const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+      E *o = static_cast<E *>(p.out) + row * D + d;
+      store_elem<E>(o + 0, A.x * inv);
+      store_elem<E>(o + 1, A.y * inv);
+      store_elem<E>(o + 2, A.z * inv);
+      store_elem<E>(o + 3, A.w * inv);
+      if (d == 0 && p.lse != nullptr) p.lse[row] = Ls > 0.f ? (M + log2f(Ls)) * kLn2 : -INFINITY;
+    } else {
+      *reinterpret_cast<float4 *>(blk + r * D + d) = A;
+      if (d == 0) {
+        blk[R * D + r] = Ls > 0.f ? M * kLn2 : -INFINITY;
+        blk[R * D + R + r] = Ls;
+      }
+    }
+  }
+  if (!single) {
+    __syncthreads();  // every thread's block writes happen before thread 0's release
+    int *cnt = p.counters + g;
+    if (tid == 0) {
+      const int before = ticket_acq_rel(cnt);
+      if (before < 0 || before >= NC) report(p.status, TD_DEV_WORKSPACE_DIRTY);
+      *s_last = before == NC - 1;
+    }
+    __syncthreads();
+    if (*s_last) {
+      merge_group<E, D, ROWS>(p, smem_f, smem_floats, merge_bar, merge_phase, b, kvh, rb, NC, nv);
+      if (tid == 0) *cnt = 0;  // leave the counter area zero for the next call
+    }
+  }
+  __syncthreads();
+}
+
 template <typename E, int D, int RP>
-__global__ void __launch_bounds__(kThreads) split_attn_kernel(const SplitParams p) {
+__global__ void __launch_bounds__(kThreads, 2) split_attn_kernel(const SplitParams p) {
   using C = SplitCfg<E, D, RP>;
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ int s_len[TD_MAX_BATCH];
   __shared__ int s_prefix[TD_MAX_BATCH + 1];
-  __shared__ long long s_red[kWarps];
+  __shared__ long long s_red[2 * kWarps];
   __shared__ int s_chunk, s_last, s_abort;
+  __shared__ __align__(8) uint64_t s_merge_bar;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g8 = lane >> 3, sub = lane & 7;
@@ -184,14 +407,20 @@ __global__ void __launch_bounds__(kThreads) split_attn_kernel(const SplitParams 
   uint64_t *bars =
       reinterpret_cast<uint64_t *>(smem + kWarps * C::RING_BYTES + kWarps * C::STASH_FLOATS * 4) + warp * kStages;
   float *combine = reinterpret_cast<float *>(smem);           // after all rings are idle
-  float *merge_scratch = combine + C::COMBINE_FLOATS;
 
   if (lane == 0) {
 #pragma unroll
     for (int s = 0; s < kStages; ++s) mbar_init(smem_u32(&bars[s]), 1);
     fence_mbar_init();
   }
-  if (tid == 0) s_abort = 0;
+  if (tid == 0) {
+    s_abort = 0;
+    mbar_init(smem_u32(&s_merge_bar), 1);
+    fence_mbar_init();
+  }
+  uint32_t merge_phase = 0;
+  griddep_wait();  // inputs may come from the previous kernel in the stream
+  griddep_launch_dependents();
   plan_items(p, s_len, s_prefix, &s_chunk, s_red);  // ends with __syncthreads
 
   const int S = s_chunk;
@@ -418,76 +647,8 @@ __global__ void __launch_bounds__(kThreads) split_attn_kernel(const SplitParams 
 #pragma unroll
       for (int d = 0; d < C::DV; ++d) ca[(warp * RP + r) * D + lane * C::DV + d] = acc[r][d];
     __syncthreads();
-
-    const bool single = NC == 1;
-    for (int idx = tid; idx < RP * D; idx += kThreads) {
-      const int r = idx / D, d = idx % D;
-      const int gr = rb * p.R + r;
-      if (r >= p.R || gr >= GT) continue;
-      const int hq = kvh * p.G + gr / p.T;
-      const int t = gr % p.T;
-      const long long row = (long long)b * rows + (long long)hq * p.T + t;
-      float M = -INFINITY;
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w) M = fmaxf(M, cm[w * RP + r]);
-      float Ls = 0.f, A = 0.f;
-      if (M != -INFINITY) {
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) {
-          const float mw = cm[w * RP + r];
-          if (mw != -INFINITY) {
-            const float f = exp2f(mw - M);
-            Ls = fmaf(cl[w * RP + r], f, Ls);
-            A = fmaf(ca[(w * RP + r) * D + d], f, A);
-          }
-        }
-      }
-      if (single) {
-        store_elem<E>(static_cast<E *>(p.out) + row * D + d, Ls > 0.f ? A / Ls : 0.f);
-        if (d == 0 && p.lse != nullptr) p.lse[row] = Ls > 0.f ? (M + log2f(Ls)) * kLn2 : -INFINITY;
-      } else {
-        const long long slot = row * p.ns_ws + c;
-        p.ws_acc[slot * D + d] = A;
-        if (d == 0) {
-          p.ws_m[slot] = Ls > 0.f ? M * kLn2 : -INFINITY;
-          p.ws_l[slot] = Ls;
-        }
-      }
-    }
-
-    if (!single) {
-      // completion ticket for (b, kv head, row block); the CTA finishing the last chunk merges
-      __threadfence();
-      __syncthreads();
-      int *cnt = p.counters + ((long long)b * p.Hkv + kvh) * p.RB + rb;
-      if (tid == 0) {
-        const int before = atomicAdd(cnt, 1);
-        if (before < 0 || before >= NC) report(p.status, TD_DEV_WORKSPACE_DIRTY);
-        s_last = before == NC - 1;
-      }
-      __syncthreads();
-      if (s_last) {
-        __threadfence();
-        long long rowbase[RP], out_row[RP];
-#pragma unroll
-        for (int r = 0; r < RP; ++r) {
-          const int gr = rb * p.R + r;
-          if (r < p.R && gr < GT) {
-            const int hq = kvh * p.G + gr / p.T;
-            const int t = gr % p.T;
-            out_row[r] = (long long)b * rows + (long long)hq * p.T + t;
-            rowbase[r] = out_row[r] * p.ns_ws;
-          } else {
-            out_row[r] = 0;
-            rowbase[r] = -1;
-          }
-        }
-        merge_rows<RP, E>(p.ws_m, p.ws_l, p.ws_acc, rowbase, out_row, NC, D, static_cast<E *>(p.out), p.lse,
-                          merge_scratch, merge_scratch + RP * kMergeBlock);
-        if (tid == 0) *cnt = 0;  // leave the counter area zero for the next call
-      }
-    }
-    __syncthreads();  // combine area and rings are reused by the next item
+    finish_item<E, D, RP, kWarps>(p, combine, kWarps * C::RING_BYTES / 4, &s_merge_bar, merge_phase, b, kvh, rb, c,
+                                  NC, &s_last);
     if (s_abort) break;
   }
 }
