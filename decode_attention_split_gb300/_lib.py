@@ -17,6 +17,7 @@ SYMBOLS = (
     "td_decode_attn",
     "td_verify_attn",
     "td_lse_merge",
+    "td_decode_attn_noalloc",
 )
 
 _lock = threading.Lock()
@@ -49,6 +50,8 @@ def _declare(lib):
     lib.td_verify_attn.restype = i
     lib.td_lse_merge.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, vp, vp, vp]
     lib.td_lse_merge.restype = i
+    lib.td_decode_attn_noalloc.argtypes = [i, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, vp, vp, vp]
+    lib.td_decode_attn_noalloc.restype = i
     return lib
 
 

@@ -138,6 +138,24 @@ td_status td_verify_attn(td_dtype dtype, const void *q, const void *k_cache, con
 td_status td_lse_merge(const float *m, const float *l, const float *acc, const int32_t *seq_lens, int B, int rows,
                        int NS, int D, int split, td_dtype out_dtype, void *out, float *lse, void *stream);
 
+/*
+ * Decode attention without a workspace argument: the same computation and arguments as
+ * td_decode_attn, minus workspace and workspace_bytes. (The pages describe no such call; it
+ * exists for callers of this library that cannot allocate device memory: a plugin or launch
+ * hook handed only input and output pointers, a serving loop that must not allocate once
+ * running, or code working while another runtime owns the device heap.)
+ * Its scratch is a fixed 4 MiB array compiled into the library, which every GPU that loads
+ * the library holds until the process exits; the call allocates nothing. A shape whose
+ * workspace (td_decode_workspace_bytes with q_len 1) exceeds 4 MiB returns TD_ERR_WORKSPACE.
+ * The first call on a device looks up the array's address on that device (make that first
+ * call before any stream capture). Every call zeroes the array's counter area on its stream
+ * before launching. All calls on a device share the one array, so calls that may overlap on
+ * the GPU (different streams without ordering between them) race and must not be issued.
+ */
+td_status td_decode_attn_noalloc(td_dtype dtype, const void *q, const void *k_cache, const void *v_cache,
+                                 const int32_t *seq_lens, int B, int Hq, int Hkv, int Smax, int D, float scale,
+                                 int split, void *out, float *lse, uint32_t *dev_status, void *stream);
+
 #ifdef __cplusplus
 }
 #endif
