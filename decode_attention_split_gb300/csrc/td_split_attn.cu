@@ -15,12 +15,12 @@ constexpr int kKernelSlots = 2 * 2 * 4 + 2 * 2;  // CUDA-core: dtype x D x row p
 struct KernelRef {
   const void *fn;
   int smem;
-  void (*launch)(const SplitParams &, int grid, int smem, cudaStream_t);
+  cudaError_t (*launch)(const SplitParams &, int grid, int smem, cudaStream_t);
 };
 
 template <typename E, int D, int RP>
-void launch_one(const SplitParams &p, int grid, int smem, cudaStream_t stream) {
-  launch_pdl(split_attn_kernel<E, D, RP>, dim3(grid), dim3(kThreads), smem, stream, p);
+cudaError_t launch_one(const SplitParams &p, int grid, int smem, cudaStream_t stream) {
+  return launch_pdl(split_attn_kernel<E, D, RP>, dim3(grid), dim3(kThreads), smem, stream, p);
 }
 
 template <typename E, int D, int RP>
@@ -55,9 +55,42 @@ KernelRef pick_d(int D, int RP) {
   return KernelRef{nullptr, 0, nullptr};
 }
 
+// cuTensorMapEncodeTiled, resolved once through the runtime (no link against the driver).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+// 3-D map over a bf16 cache [B*Hkv][Smax][D]: boxes of 64 columns (128 bytes) x 64 rows,
+// 128-byte swizzle, zero fill outside the tensor.
+bool encode_cache_map(CUtensorMap *map, const void *base, int B, int Hkv, int Smax, int D) {
+  const PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)Smax, (cuuint64_t)B * Hkv};
+  const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)Smax * D * 2};
+  const cuuint32_t box[3] = {64, 64, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int D, int MT>
-void launch_mma(const SplitParams &p, int grid, int smem, cudaStream_t stream) {
-  launch_pdl(split_attn_mma_kernel<D, MT>, dim3(grid), dim3(kThreads), smem, stream, p);
+cudaError_t launch_mma(const SplitParams &p, int grid, int smem, cudaStream_t stream) {
+  MmaArgs a;
+  if (!encode_cache_map(&a.kmap, p.k, p.B, p.Hkv, p.Smax, D) || !encode_cache_map(&a.vmap, p.v, p.B, p.Hkv, p.Smax, D))
+    return cudaErrorInvalidValue;
+  a.p = p;
+  return launch_pdl(split_attn_mma_kernel<D, MT>, dim3(grid), dim3(kThreads), smem, stream, a);
 }
 
 template <int D, int MT>
@@ -181,8 +214,12 @@ td_status plan_split(td_dtype dtype, int B, int Hq, int Hkv, int T, int Smax, in
 cudaError_t launch_split(td_dtype dtype, int D, const SplitPlan &plan, const SplitParams &p, cudaStream_t stream) {
   const KernelRef k = pick(dtype, D, plan.mma, plan.RP);
   if (k.fn == nullptr) return cudaErrorInvalidValue;
-  k.launch(p, plan.grid, plan.smem, stream);
-  return cudaPeekAtLastError() != cudaSuccess ? cudaGetLastError() : cudaSuccess;
+  const cudaError_t e = k.launch(p, plan.grid, plan.smem, stream);
+  if (e != cudaSuccess) {
+    cudaGetLastError();  // clear a launch error so it is reported once, by this call
+    return e;
+  }
+  return cudaSuccess;
 }
 
 }  // namespace td

@@ -5,18 +5,24 @@
 // per (sequence, kv head, row block, chunk) item computes the chunk's partial softmax for
 // every query row reading that kv head, and chunks are merged by log-sum-exp.
 //
-// The grouped-query rows of a kv head (G heads x T verify tokens, up to 32 per CTA) form
-// the M side of mma.sync m16n8k16 tiles, so each K/V tile loaded into shared memory is
-// read once for all of them:
+// The grouped-query rows of a kv head (up to 16 per CTA: G heads x T verify tokens) form
+// the M side of mma.sync m16n8k16 tiles, so each K/V tile in shared memory is read once for
+// all of them:
 //   scores  S[rows x 16 keys] = Q[rows x D] . K^T   (B operand from K rows via ldmatrix)
 //   output  O[rows x D]      += P[rows x 16 keys] . V (B operand via ldmatrix.trans)
 // with fp32 accumulation; P is rounded to bf16 for the second product while the softmax
-// statistics (m, l) stay fp32. K/V stages of 64 rows are copied with 16-byte cp.async
-// (zero-filled past the chunk end) into tiles whose 16-byte chunks are XOR-swizzled by
-// row, so the 8 rows an ldmatrix reads sit in 8 different bank groups. Warps are arranged
-// as (m tile, key slice): with one m tile the 4 warps split every stage's keys 4 ways,
-// with two m tiles 2 ways; warps combine at the end of the item.
+// statistics (m, l) stay fp32.
+//
+// K/V stages of 64 rows are fetched by the TMA engine (cp.async.bulk.tensor: one thread
+// issues one box of 64 rows x 128 bytes per half-row) through a 3-D tensor map over the
+// cache [B*Hkv][Smax][D] with the 128-byte swizzle, so the 8 rows an ldmatrix reads sit in 8
+// different bank groups; completion is counted on one mbarrier per stage, waited on with a
+// bounded wait. Rows past Smax are zero-filled by the TMA unit; rows past a sequence's
+// length inside its last stage are zeroed in shared memory before use. The 4 warps split
+// every stage's keys 4 ways and combine at the end of the item.
 #pragma once
+
+#include <cudaTypedefs.h>
 
 #include "td_mma.cuh"
 #include "td_split_attn.cuh"
@@ -32,55 +38,93 @@ struct MmaCfg {
   static constexpr int NKSTEP = TKW / 16;     // 16-key steps per warp per stage
   static constexpr int ROWB = D * 2;          // bytes per cache row
   static constexpr int NCH = ROWB / 16;       // 16-byte chunks per cache row
+  static constexpr int HALVES = D / 64;       // 128-byte column halves (TMA boxes per tile)
+  static constexpr int BOX_BYTES = TK * 128;  // one box: 64 rows x 128 bytes
   static constexpr int NST = D == 128 ? 3 : 4;
   static constexpr int TILE_BYTES = TK * ROWB;
   static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
-  static constexpr int SMEM_BYTES = NST * STAGE_BYTES;
+  static constexpr int RING_BYTES = NST * STAGE_BYTES;
+  static constexpr int SMEM_BYTES = RING_BYTES + 1024;  // + room to align the ring to 1024 bytes
   static constexpr int NTD = D / 8;           // 8-wide output n tiles
   static constexpr int KSD = D / 16;          // 16-deep score k steps
   static constexpr int COMBINE_FLOATS = KS * ROWS * (D + 2);
   static_assert(TKW % 16 == 0, "each warp takes whole 16-key steps");
-  static_assert(COMBINE_FLOATS * 4 <= SMEM_BYTES, "combine area fits in the ring");
-  static_assert((merge_fixed_floats<D, ROWS>() + part_block_floats(ROWS, D)) * 4 <= SMEM_BYTES,
+  static_assert(D % 64 == 0, "whole 128-byte halves");
+  static_assert(COMBINE_FLOATS * 4 <= RING_BYTES, "combine area fits in the ring");
+  static_assert((merge_fixed_floats<D, ROWS>() + part_block_floats(ROWS, D)) * 4 <= RING_BYTES,
                 "merge stages at least one chunk");
   static_assert(ROWS * D * 2 <= TILE_BYTES, "the query tile fits in one K tile");
   static constexpr bool kFits = SMEM_BYTES + 8448 <= 227 * 1024;
 };
 
-// Byte offset of 16-byte chunk `ch` of row `row` in a swizzled tile.
+// Kernel arguments: tensor maps of the two caches, then the common parameters.
+struct MmaArgs {
+  CUtensorMap kmap;
+  CUtensorMap vmap;
+  SplitParams p;
+};
+
+// Byte offset of 16-byte chunk `ch` of row `row` in the query tile (row-major, chunks XOR-ed
+// with the row's low 3 bits).
 template <int ROWB>
 __device__ __forceinline__ uint32_t swz(int row, int ch) {
   return (uint32_t)(row * ROWB + ((ch ^ (row & 7)) << 4));
 }
 
+// Byte offset of 16-byte chunk `ch` of row `row` in a K/V tile written by the TMA unit with
+// the 128-byte swizzle: the tile is HALVES boxes of [64 rows][128 bytes], each 1024-byte
+// aligned, and inside a box chunk c of row r lives at chunk position c ^ (r & 7).
+template <int TK>
+__device__ __forceinline__ uint32_t tma_swz(int row, int ch) {
+  return (uint32_t)((ch >> 3) * (TK * 128) + row * 128 + (((ch & 7) ^ (row & 7)) << 4));
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, int x, int y, int z, uint32_t bar,
+                                            uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%2, "
+      "%3, %4}], [%5], %6;" ::"r"(dst),
+      "l"(map), "r"(x), "r"(y), "r"(z), "r"(bar), "l"(policy)
+      : "memory");
+}
+
 template <int D, int MT>
-__global__ void __launch_bounds__(kThreads, 2) split_attn_mma_kernel(const SplitParams p) {
+__global__ void __launch_bounds__(kThreads, 2) split_attn_mma_kernel(const __grid_constant__ MmaArgs a) {
   using C = MmaCfg<D, MT>;
   using E = __nv_bfloat16;
-  extern __shared__ __align__(128) unsigned char smem[];
+  const SplitParams &p = a.p;
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
   __shared__ int s_len[TD_MAX_BATCH];
   __shared__ int s_prefix[TD_MAX_BATCH + 1];
   __shared__ long long s_red[2 * kWarps];
-  __shared__ int s_chunk, s_last;
+  __shared__ int s_chunk, s_last, s_abort;
   __shared__ __align__(8) uint64_t s_merge_bar;
+  __shared__ __align__(8) uint64_t s_bars[C::NST];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int gid = lane >> 2, tig = lane & 3;
   const int mt = warp / C::KS, ks = warp % C::KS;
+  // the 128-byte swizzle is a function of the shared-memory address: align the ring to 1024
+  unsigned char *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sbase = smem_u32(smem);
   float *combine = reinterpret_cast<float *>(smem);
   if (tid == 0) {
     mbar_init(smem_u32(&s_merge_bar), 1);
+#pragma unroll
+    for (int i = 0; i < C::NST; ++i) mbar_init(smem_u32(&s_bars[i]), 1);
     fence_mbar_init();
+    s_abort = 0;
   }
   uint32_t merge_phase = 0;
-  griddep_wait();  // inputs may come from the previous kernel in the stream
+  uint32_t seq = 0;  // stages consumed so far by this CTA (mbarrier parity bookkeeping)
+  griddep_wait();    // inputs may come from the previous kernel in the stream
   griddep_launch_dependents();
   plan_items(p, s_len, s_prefix, &s_chunk, s_red);  // ends with __syncthreads
   const int S = s_chunk;
   const int W = s_prefix[p.B];
   const int rows = p.Hq * p.T;
   const int GT = p.G * p.T;
+  const uint64_t policy = l2_evict_first_policy();
 
   // sequences with no key get no item: their rows are 0 with lse = -inf
   for (int b = blockIdx.x; b < p.B; b += gridDim.x) {
@@ -108,28 +152,26 @@ __global__ void __launch_bounds__(kThreads, 2) split_attn_mma_kernel(const Split
     const int c0 = c * S;
     const int c1 = min(c0 + S, L);
     const int nstages = (c1 - c0 + C::TK - 1) / C::TK;
-    const size_t head_off = ((size_t)b * p.Hkv + kvh) * (size_t)p.Smax * C::ROWB;
-    const unsigned char *kg = static_cast<const unsigned char *>(p.k) + head_off;
-    const unsigned char *vg = static_cast<const unsigned char *>(p.v) + head_off;
+    const int zc = b * p.Hkv + kvh;  // tensor-map coordinate of this (sequence, kv head)
 
-    auto load_stage = [&](int sidx) {
-      const int j0 = c0 + sidx * C::TK;
-      const int valid = min(C::TK, c1 - j0);
-      const uint32_t kdst = sbase + (sidx % C::NST) * C::STAGE_BYTES;
+    // stage sidx of this item goes to ring buffer (seq + sidx) % NST
+    auto issue = [&](int sidx) {
+      const int buf = (seq + sidx) % C::NST;
+      const uint32_t bar = smem_u32(&s_bars[buf]);
+      const uint32_t kdst = sbase + buf * C::STAGE_BYTES;
       const uint32_t vdst = kdst + C::TILE_BYTES;
-#pragma unroll 4
-      for (int idx = tid; idx < C::TK * C::NCH; idx += kThreads) {
-        const int row = idx / C::NCH, ch = idx % C::NCH;
-        const bool ok = row < valid;
-        const size_t off = (size_t)(j0 + (ok ? row : 0)) * C::ROWB + ch * 16;
-        const uint32_t so = swz<C::ROWB>(row, ch);
-        cp_async_16(kdst + so, kg + off, ok ? 16u : 0u);
-        cp_async_16(vdst + so, vg + off, ok ? 16u : 0u);
+      const int y = c0 + sidx * C::TK;
+      fence_proxy_async_smem();
+      mbar_arrive_expect_tx(bar, 2 * C::TILE_BYTES);
+#pragma unroll
+      for (int h = 0; h < C::HALVES; ++h) {
+        tma_load_3d(kdst + h * C::BOX_BYTES, &a.kmap, 64 * h, y, zc, bar, policy);
+        tma_load_3d(vdst + h * C::BOX_BYTES, &a.vmap, 64 * h, y, zc, bar, policy);
       }
     };
-    // the query rows of this row block go, swizzled like a K tile, to the K tile of the last
-    // ring buffer, which no stage fills before the first stage has been consumed
-    const uint32_t qtile = sbase + (C::NST - 1) * C::STAGE_BYTES;
+    // the query rows of this row block go to the K tile of the ring buffer the first stage
+    // refills last; they are read into registers before that buffer is refilled
+    const uint32_t qtile = sbase + ((seq + C::NST - 1) % C::NST) * C::STAGE_BYTES;
     for (int idx = tid; idx < C::ROWS * C::NCH; idx += kThreads) {
       const int r = idx / C::NCH, ch = idx % C::NCH;
       const int gr = rb * p.R + r;
@@ -140,10 +182,9 @@ __global__ void __launch_bounds__(kThreads, 2) split_attn_mma_kernel(const Split
           static_cast<const unsigned char *>(p.q) + (((size_t)b * p.Hq + hq) * p.T + t) * C::ROWB;
       cp_async_16(qtile + swz<C::ROWB>(r, ch), qrow + ch * 16, valid ? 16u : 0u);
     }
-#pragma unroll
-    for (int s2 = 0; s2 < C::NST - 1; ++s2) {
-      if (s2 < nstages) load_stage(s2);
-      cp_async_commit();
+    cp_async_commit();
+    if (tid == 0) {
+      for (int s2 = 0; s2 < min(C::NST - 1, nstages); ++s2) issue(s2);
     }
 
     // keys visible to rows r0 = 16*mt + gid and r1 = r0 + 8 of this row block
@@ -155,27 +196,44 @@ __global__ void __launch_bounds__(kThreads, 2) split_attn_mma_kernel(const Split
       const bool valid = r < p.R && gr < GT;
       lim[h] = valid ? min(max(L - p.T + gr % p.T + 1, 0), c1) : 0;
     }
-    uint32_t qa[C::KSD][4];  // query rows as mma A fragments, read once the first group lands
+    uint32_t qa[C::KSD][4];  // query rows as mma A fragments, read once the first stage lands
 
     float o[C::NTD][4];
 #pragma unroll
     for (int nt = 0; nt < C::NTD; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
     float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
 
+    int consumed = 0;
+    bool ok = true;
     for (int st = 0; st < nstages; ++st) {
-      cp_async_wait<C::NST - 2>();
+      const int buf = (seq + st) % C::NST;
+      if (!mbar_wait_bounded(smem_u32(&s_bars[buf]), ((seq + st) / C::NST) & 1u)) {
+        ok = false;
+        break;
+      }
+      const int j0 = c0 + st * C::TK;
+      const int valid = min(C::TK, c1 - j0);
+      const uint32_t kt = sbase + buf * C::STAGE_BYTES;
+      const uint32_t vt = kt + C::TILE_BYTES;
+      if (valid < C::TK) {
+        // rows past the sequence's length were fetched (or zero-filled past Smax): zero the
+        // V rows so a masked probability never meets a non-finite value
+        unsigned char *vrow = smem + buf * C::STAGE_BYTES + C::TILE_BYTES;
+        for (int idx = tid; idx < (C::TK - valid) * C::NCH; idx += kThreads) {
+          const int r = valid + idx / C::NCH, ch = idx % C::NCH;
+          *reinterpret_cast<uint4 *>(vrow + tma_swz<C::TK>(r, ch)) = make_uint4(0u, 0u, 0u, 0u);
+        }
+        fence_proxy_async_smem();  // these writes precede the buffer's next refill by the TMA unit
+      }
+      if (st == 0) cp_async_wait<0>();  // this thread's part of the query tile
       __syncthreads();
       if (st == 0) {
 #pragma unroll
         for (int j = 0; j < C::KSD; ++j)
           ldmatrix_x4(qa[j], qtile + swz<C::ROWB>(mt * 16 + ((lane >> 3) & 1) * 8 + (lane & 7), 2 * j + (lane >> 4)));
-        __syncthreads();  // every warp holds its query fragments before the buffer is refilled
+        __syncthreads();  // every warp holds its query fragments before that buffer is refilled
       }
-      if (st + C::NST - 1 < nstages) load_stage(st + C::NST - 1);
-      cp_async_commit();
-      const uint32_t kt = sbase + (st % C::NST) * C::STAGE_BYTES;
-      const uint32_t vt = kt + C::TILE_BYTES;
-      const int j0 = c0 + st * C::TK;
+      if (tid == 0 && st + C::NST - 1 < nstages) issue(st + C::NST - 1);
 #pragma unroll
       for (int kk = 0; kk < C::NKSTEP; ++kk) {
         const int kr = ks * C::TKW + kk * 16;  // first key row (within the stage) of this step
@@ -189,7 +247,7 @@ __global__ void __launch_bounds__(kThreads, 2) split_attn_mma_kernel(const Split
 #pragma unroll
           for (int i = 0; i < C::KSD / 2; ++i) {
             uint32_t bk[4];
-            ldmatrix_x4(bk, kt + swz<C::ROWB>(kr + nt * 8 + (lane & 7), 4 * i + (lane >> 3)));
+            ldmatrix_x4(bk, kt + tma_swz<C::TK>(kr + nt * 8 + (lane & 7), 4 * i + (lane >> 3)));
             mma_bf16_16816(sc[nt], qa[2 * i], bk[0], bk[1]);
             mma_bf16_16816(sc[nt], qa[2 * i + 1], bk[2], bk[3]);
           }
@@ -240,13 +298,30 @@ __global__ void __launch_bounds__(kThreads, 2) split_attn_mma_kernel(const Split
 #pragma unroll
         for (int i = 0; i < C::NTD / 2; ++i) {
           uint32_t bv[4];
-          ldmatrix_x4_trans(bv, vt + swz<C::ROWB>(kr + (lane & 7) + ((lane >> 3) & 1) * 8, 2 * i + (lane >> 4)));
+          ldmatrix_x4_trans(bv, vt + tma_swz<C::TK>(kr + (lane & 7) + ((lane >> 3) & 1) * 8, 2 * i + (lane >> 4)));
           mma_bf16_16816(o[2 * i], pa, bv[0], bv[1]);
           mma_bf16_16816(o[2 * i + 1], pa, bv[2], bv[3]);
         }
       }
+      consumed = st + 1;
+    }
+    if (!ok) {
+      // a copy never completed: wait (bounded) for the rest of this item's copies in flight,
+      // then drop the item
+      const int issued = min(nstages, consumed + C::NST - 1);
+      for (int st = consumed; st < issued; ++st)
+        mbar_wait_bounded(smem_u32(&s_bars[(seq + st) % C::NST]), ((seq + st) / C::NST) & 1u);
+      if (tid == 0) {
+        report(p.status, TD_DEV_WAIT_TIMEOUT);
+        s_abort = 1;
+      }
+      m_run[0] = m_run[1] = -INFINITY;
+      l_run[0] = l_run[1] = 0.f;
+#pragma unroll
+      for (int nt = 0; nt < C::NTD; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
     }
     cp_async_wait<0>();
+    seq += nstages;
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 1);
@@ -270,8 +345,13 @@ __global__ void __launch_bounds__(kThreads, 2) split_attn_mma_kernel(const Split
       }
     }
     __syncthreads();
-    finish_item<E, D, C::ROWS, C::KS>(p, combine, C::SMEM_BYTES / 4, &s_merge_bar, merge_phase, b, kvh, rb, c, NC,
+    finish_item<E, D, C::ROWS, C::KS>(p, combine, C::RING_BYTES / 4, &s_merge_bar, merge_phase, b, kvh, rb, c, NC,
                                       &s_last);
+    // the combine and merge wrote the ring through the generic proxy; the next item's first
+    // stages refill it through the asynchronous proxy
+    fence_proxy_async_smem();
+    __syncthreads();
+    if (s_abort) break;
   }
 }
 
