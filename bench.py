@@ -236,6 +236,19 @@ def time_graph(graph, stream, reps, warm=2):
     return e0.elapsed_time(e1)
 
 
+def kernel_label(td, w) -> str:
+    """Which split-attention kernel the timed call runs, from the library's own launch plan."""
+    plan = td.td_split_plan(w.torch_dtype, w.B, w.Hq, w.Hkv, w.Smax, w.D, w.T, 0)
+    names = {
+        "tensor_core_persistent": f"split_attn_mma_kernel<{w.D}> (persistent, fused split + workspace merge, "
+                                  f"mma.sync bf16, TMA)",
+        "tensor_core_cluster": f"split_attn_cluster_kernel<{w.D}> (clusters of {plan['cluster']}, on-chip merge, "
+                               f"mma.sync bf16, TMA)",
+        "cuda_core": f"split_attn_kernel<{w.D}> (CUDA cores)",
+    }
+    return f"{names[plan['kernel']]}, grid {plan['grid']}, timed alone"
+
+
 def sweep_point(td, name, L, dev, l2_bytes, peak, budget_calls=200):
     """Attention kernel alone on one workload point: graph of R launches over rotating caches."""
     w = WORKLOADS[name]
@@ -423,7 +436,7 @@ def run_td(args, world, rank, local):
         "gpu_launches": 2 * total_calls,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "kernel": "split_attn_mma_kernel<128,1> (fused split + merge, mma.sync bf16), timed alone",
+                     "kernel": kernel_label(td, w),
                      "us_per_launch": round(us_attn, 3), "peak_kind": f"hbm_gbs of {peak_kind}",
                      "algorithmic_bytes_per_launch": bytes_call},
         "e2e": e2e,

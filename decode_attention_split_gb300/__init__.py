@@ -18,5 +18,6 @@ from .api import (  # noqa: F401
     td_decode_workspace_bytes,
     td_kv_append,
     td_lse_merge,
+    td_split_plan,
     td_verify_attn,
 )

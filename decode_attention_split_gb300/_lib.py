@@ -13,6 +13,7 @@ SYMBOLS = (
     "td_version",
     "td_last_cuda_error",
     "td_decode_workspace_bytes",
+    "td_split_plan",
     "td_kv_append",
     "td_decode_attn",
     "td_verify_attn",
@@ -42,6 +43,8 @@ def _declare(lib):
     lib.td_last_cuda_error.restype = i
     lib.td_decode_workspace_bytes.argtypes = [i, i, i, i, i, i, i]
     lib.td_decode_workspace_bytes.restype = sz
+    lib.td_split_plan.argtypes = [i, i, i, i, i, i, i, i, vp, vp, vp, vp]
+    lib.td_split_plan.restype = i
     lib.td_kv_append.argtypes = [i, vp, vp, vp, vp, vp, i, i, i, i, i, i, vp, vp]
     lib.td_kv_append.restype = i
     lib.td_decode_attn.argtypes = [i, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, vp, vp, sz, vp, vp]

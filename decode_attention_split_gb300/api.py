@@ -10,6 +10,7 @@ and warm the call up once outside the capture.
 """
 from __future__ import annotations
 
+import ctypes
 import math
 import threading
 
@@ -67,6 +68,20 @@ def _stream(stream, device) -> int:
 def td_decode_workspace_bytes(B: int, Hq: int, Hkv: int, Smax: int, D: int, q_len: int = 1, split: int = 0) -> int:
     """Workspace bytes td_decode_attn / td_verify_attn need on the current device (0 = invalid)."""
     return int(lib().td_decode_workspace_bytes(B, Hq, Hkv, Smax, D, q_len, split))
+
+
+KERNEL_NAMES = ("cuda_core", "tensor_core_persistent", "tensor_core_cluster")
+
+
+def td_split_plan(dtype: torch.dtype, B: int, Hq: int, Hkv: int, Smax: int, D: int, q_len: int = 1,
+                  split: int = 0) -> dict:
+    """Which kernel and launch shape the attention call takes on the current device (td.h)."""
+    code = _code(torch.empty(0, dtype=dtype))
+    vals = [ctypes.c_int(0) for _ in range(4)]
+    check("td_split_plan",
+          lib().td_split_plan(code, B, Hq, Hkv, Smax, D, q_len, split, *[ctypes.byref(v) for v in vals]))
+    kernel, grid, cluster, rows = (v.value for v in vals)
+    return dict(kernel=KERNEL_NAMES[kernel], grid=grid, cluster=cluster, rows=rows)
 
 
 def make_workspace(B, Hq, Hkv, Smax, D, q_len=1, split=0, device=None) -> torch.Tensor:

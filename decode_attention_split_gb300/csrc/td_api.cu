@@ -92,6 +92,19 @@ size_t td_decode_workspace_bytes(int B, int Hq, int Hkv, int Smax, int D, int q_
   return bytes;
 }
 
+td_status td_split_plan(td_dtype dtype, int B, int Hq, int Hkv, int Smax, int D, int q_len, int split, int *kernel,
+                        int *grid, int *cluster, int *rows) {
+  td::SplitPlan plan;
+  const td_status st = td::plan_split(dtype, B, Hq, Hkv, q_len, Smax, D, split, &plan);
+  if (st == TD_ERR_CUDA) return cuda_fail(cudaGetLastError());
+  if (st != TD_OK) return st;
+  if (kernel != nullptr) *kernel = !plan.mma ? 0 : plan.cluster > 0 ? 2 : 1;
+  if (grid != nullptr) *grid = plan.grid;
+  if (cluster != nullptr) *cluster = plan.cluster;
+  if (rows != nullptr) *rows = plan.R;
+  return TD_OK;
+}
+
 td_status td_kv_append(td_dtype dtype, const void *k_new, const void *v_new, void *k_cache, void *v_cache,
                        int32_t *seq_lens, int B, int Hkv, int T, int Smax, int D, int advance, uint32_t *dev_status,
                        void *stream) {

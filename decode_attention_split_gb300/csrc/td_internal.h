@@ -22,6 +22,7 @@ struct SplitPlan {
   int grid;      // CTAs launched
   int smem;      // dynamic shared memory per CTA
   int min_chunk; // smallest automatic chunk (keys)
+  int cluster;   // 0: persistent kernel; else CTAs per cluster of the cluster kernel (grid = groups x cluster)
   size_t off_part, bytes;  // workspace layout: counters, then partial blocks
 };
 

@@ -2,6 +2,7 @@
 // 16-byte asynchronous global->shared copies with zero fill, used by the bf16 split kernel.
 #pragma once
 
+#include <cuda_bf16.h>
 #include <stdint.h>
 
 namespace td {

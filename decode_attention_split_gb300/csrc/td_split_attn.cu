@@ -3,6 +3,7 @@
 
 #include "td_internal.h"
 #include "td_split_attn.cuh"
+#include "td_split_cluster.cuh"
 #include "td_split_mma.cuh"
 
 namespace td {
@@ -84,27 +85,68 @@ bool encode_cache_map(CUtensorMap *map, const void *base, int B, int Hkv, int Sm
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D, int MT>
+template <int D>
 cudaError_t launch_mma(const SplitParams &p, int grid, int smem, cudaStream_t stream) {
   MmaArgs a;
   if (!encode_cache_map(&a.kmap, p.k, p.B, p.Hkv, p.Smax, D) || !encode_cache_map(&a.vmap, p.v, p.B, p.Hkv, p.Smax, D))
     return cudaErrorInvalidValue;
   a.p = p;
-  return launch_pdl(split_attn_mma_kernel<D, MT>, dim3(grid), dim3(kThreads), smem, stream, a);
+  return launch_pdl(split_attn_mma_kernel<D>, dim3(grid), dim3(kThreads), smem, stream, a);
 }
 
-template <int D, int MT>
+template <int D>
 KernelRef mma_ref_of() {
-  static_assert(MmaCfg<D, MT>::kFits, "mma kernel shared memory");
-  return KernelRef{reinterpret_cast<const void *>(&split_attn_mma_kernel<D, MT>), MmaCfg<D, MT>::SMEM_BYTES,
-                   &launch_mma<D, MT>};
+  // the ring plus 1024 bytes of slack for its alignment
+  constexpr int smem = MmaCfg<D, kPersistentStages<D>>::RING_BYTES + 1024;
+  static_assert(smem + 8448 <= 227 * 1024, "mma kernel shared memory");
+  return KernelRef{reinterpret_cast<const void *>(&split_attn_mma_kernel<D>), smem, &launch_mma<D>};
 }
 
 KernelRef pick_mma(int D, int MT) {
   if (MT != 1) return KernelRef{nullptr, 0, nullptr};
-  if (D == 64) return mma_ref_of<64, 1>();
-  if (D == 128) return mma_ref_of<128, 1>();
+  if (D == 64) return mma_ref_of<64>();
+  if (D == 128) return mma_ref_of<128>();
   return KernelRef{nullptr, 0, nullptr};
+}
+
+template <int D>
+constexpr int cluster_smem() {
+  return MmaCfg<D, kClusterStages<D>>::RING_BYTES + 1024;  // the ring plus alignment slack
+}
+static_assert(cluster_smem<128>() + 1024 <= 227 * 1024 && cluster_smem<64>() + 1024 <= 227 * 1024,
+              "cluster kernel shared memory");
+
+const void *cluster_fn(int D) {
+  return D == 64 ? reinterpret_cast<const void *>(&split_attn_cluster_kernel<64>)
+                 : reinterpret_cast<const void *>(&split_attn_cluster_kernel<128>);
+}
+
+cudaLaunchConfig_t cluster_config(int D, int grid, int cs, cudaStream_t stream, cudaLaunchAttribute *attr) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = D == 64 ? cluster_smem<64>() : cluster_smem<128>();
+  cfg.stream = stream;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = cs;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cfg;
+}
+
+template <int D>
+cudaError_t launch_cluster(const SplitParams &p, int grid, int cs, cudaStream_t stream) {
+  MmaArgs a;
+  if (!encode_cache_map(&a.kmap, p.k, p.B, p.Hkv, p.Smax, D) || !encode_cache_map(&a.vmap, p.v, p.B, p.Hkv, p.Smax, D))
+    return cudaErrorInvalidValue;
+  a.p = p;
+  cudaLaunchAttribute attr[2];
+  const cudaLaunchConfig_t cfg = cluster_config(D, grid, cs, stream, attr);
+  return cudaLaunchKernelEx(&cfg, split_attn_cluster_kernel<D>, a);
 }
 
 // variant: row padding RP of the CUDA-core kernel, or m tiles MT of the tensor-core kernel
@@ -121,6 +163,7 @@ int slot_of(td_dtype dtype, int D, bool mma, int variant) {
 std::mutex g_mu;
 int g_sms[kMaxDevices];
 int g_blocks[kMaxDevices][kKernelSlots];  // resident CTAs per SM (0 = not yet queried)
+int g_clusters[kMaxDevices][2][4];         // co-resident clusters of 2, 4, 8, 16 CTAs (+1; 0 = not yet queried)
 
 // Sets the shared-memory opt-in once per device and returns the resident CTAs per SM.
 int blocks_per_sm(int device, int slot, const KernelRef &k) {
@@ -130,6 +173,29 @@ int blocks_per_sm(int device, int slot, const KernelRef &k) {
   int n = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k.fn, kThreads, k.smem) != cudaSuccess) return 0;
   if (device >= 0 && device < kMaxDevices) g_blocks[device][slot] = n;
+  return n;
+}
+
+// Clusters of `cs` CTAs (2, 4, 8 or 16) of the cluster kernel that the device holds at once;
+// sets the kernel's shared-memory and cluster-size opt-ins on first use. 0 on error.
+int active_clusters(int device, int D, int cs) {
+  const int di = D == 64 ? 0 : 1, ci = cs == 2 ? 0 : cs == 4 ? 1 : cs == 8 ? 2 : 3;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (device < 0 || device >= kMaxDevices) return 0;
+  if (g_clusters[device][di][ci] > 0) return g_clusters[device][di][ci] - 1;
+  const void *fn = cluster_fn(D);
+  cudaLaunchAttribute attr[2];
+  cudaLaunchConfig_t cfg = cluster_config(D, cs, cs, nullptr, attr);
+  cfg.numAttrs = 1;  // the cluster shape alone
+  int n = 0;
+  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)cfg.dynamicSmemBytes) !=
+          cudaSuccess ||
+      cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess ||
+      cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    n = 0;
+  }
+  g_clusters[device][di][ci] = n + 1;
   return n;
 }
 
@@ -205,6 +271,22 @@ td_status plan_split(td_dtype dtype, int B, int Hq, int Hkv, int T, int Smax, in
   plan->smem = k.smem;
   // a chunk must stream enough keys to amortise its fixed costs (tensor-core kernel: two stages)
   plan->min_chunk = mma ? 128 : 32;
+  // an automatic chunk size and groups (b, kv head, row block) that fit the GPU in one wave
+  // of clusters of at least two CTAs, about two CTAs per SM: one cluster per group, the
+  // largest that fits (its CTAs share the group's keys evenly and merge on chip)
+  plan->cluster = 0;
+  if (mma && split == 0) {
+    const long long groups = (long long)B * U;
+    for (int cs = kMaxCluster; cs >= 2; cs /= 2) {
+      if (groups * cs * 5 < (long long)sms * 8) break;
+      if (groups <= active_clusters(device, D, cs)) {
+        plan->cluster = cs;
+        plan->grid = (int)(groups * cs);
+        plan->smem = D == 64 ? cluster_smem<64>() : cluster_smem<128>();
+        break;
+      }
+    }
+  }
   const size_t counters = align256((size_t)B * U * sizeof(int));
   plan->off_part = counters;
   plan->bytes = plan->off_part + align256((size_t)B * U * ns * part_block_floats(R, D) * sizeof(float));
@@ -212,9 +294,15 @@ td_status plan_split(td_dtype dtype, int B, int Hq, int Hkv, int T, int Smax, in
 }
 
 cudaError_t launch_split(td_dtype dtype, int D, const SplitPlan &plan, const SplitParams &p, cudaStream_t stream) {
-  const KernelRef k = pick(dtype, D, plan.mma, plan.RP);
-  if (k.fn == nullptr) return cudaErrorInvalidValue;
-  const cudaError_t e = k.launch(p, plan.grid, plan.smem, stream);
+  cudaError_t e;
+  if (plan.cluster > 0) {
+    e = D == 64 ? launch_cluster<64>(p, plan.grid, plan.cluster, stream)
+                : launch_cluster<128>(p, plan.grid, plan.cluster, stream);
+  } else {
+    const KernelRef k = pick(dtype, D, plan.mma, plan.RP);
+    if (k.fn == nullptr) return cudaErrorInvalidValue;
+    e = k.launch(p, plan.grid, plan.smem, stream);
+  }
   if (e != cudaSuccess) {
     cudaGetLastError();  // clear a launch error so it is reported once, by this call
     return e;

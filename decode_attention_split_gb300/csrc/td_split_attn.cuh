@@ -136,62 +136,74 @@ static __device__ void plan_items(const SplitParams &p, int *s_len, int *s_prefi
     s_red[kWarps + warp] = lmax;
   }
   __syncthreads();
-  if (tid == 0) {
-    long long all = 0;
-    int longest = 0;
-    for (int w = 0; w < kWarps; ++w) {
-      all += s_red[w];
-      longest = max(longest, (int)s_red[kWarps + w]);
-    }
-    int S;
-    if (p.split > 0) {
-      S = p.split;
-    } else {
-      // keys per item so the items fill the grid once; then every sequence has at most
-      // ceil(p_target / U) chunks, which is what the workspace holds (the guard below only
-      // restates that bound)
-      long long want = (all * U + p.p_target - 1) / p.p_target;
-      want = (want + 15) / 16 * 16;
-      if (want < p.min_chunk) want = p.min_chunk;
-      const long long fits = ((long long)longest + p.ns_ws - 1) / p.ns_ws;
-      if (want < fits) want = fits;
-      S = (int)(want > p.Smax ? p.Smax : want);
-      if (S < 1) S = 1;
-    }
-    *s_chunk = S;
+  long long all = 0;
+  int longest = 0;
+  for (int w = 0; w < kWarps; ++w) {
+    all += s_red[w];
+    longest = max(longest, (int)s_red[kWarps + w]);
   }
-  __syncthreads();
-  const int S = *s_chunk;
-  // per-thread segment sums of items, then a CTA-wide exclusive scan
-  int seg = 0;
+  int S;  // the same value in every thread
+  if (p.split > 0) {
+    S = p.split;
+  } else {
+    // keys per item so the items fill the grid once; then every sequence has at most
+    // ceil(p_target / U) chunks, which is what the workspace holds (the guard below only
+    // restates that bound)
+    long long want = (all * U + p.p_target - 1) / p.p_target;
+    want = (want + 15) / 16 * 16;
+    if (want < p.min_chunk) want = p.min_chunk;
+    const long long fits = ((long long)longest + p.ns_ws - 1) / p.ns_ws;
+    if (want < fits) want = fits;
+    S = (int)(want > p.Smax ? p.Smax : want);
+    if (S < 1) S = 1;
+  }
+  // Per-thread segment sums of items, then a CTA-wide exclusive scan. With an automatic
+  // chunk size, rounding each sequence's chunk count up can push the items past the grid,
+  // leaving a second, mostly idle wave: then S grows, by the overshoot and by at least enough
+  // to take one chunk off the longest sequence, and the scan is redone (a few rounds at
+  // most; it cannot fit once every nonempty sequence is down to one chunk per unit).
+  for (int round = 0;; ++round) {
+    int seg = 0;
 #pragma unroll
-  for (int i = 0; i < kSeg; ++i) {
-    const int b = b0 + i;
-    if (b < p.B) seg += ((s_len[b] + S - 1) / S) * U;
-  }
-  int incl = seg;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += y;
-  }
-  __syncthreads();  // s_red reuse
-  if (lane == 31) s_red[warp] = incl;
-  __syncthreads();
-  int before = incl - seg;
-  for (int w = 0; w < warp; ++w) before += (int)s_red[w];
-#pragma unroll
-  for (int i = 0; i < kSeg; ++i) {
-    const int b = b0 + i;
-    if (b < p.B) {
-      s_prefix[b] = before;
-      before += ((s_len[b] + S - 1) / S) * U;
+    for (int i = 0; i < kSeg; ++i) {
+      const int b = b0 + i;
+      if (b < p.B) seg += ((s_len[b] + S - 1) / S) * U;
     }
-  }
-  if (tid == kThreads - 1) {
-    int all = 0;
-    for (int w = 0; w < kWarps; ++w) all += (int)s_red[w];
-    s_prefix[p.B] = all;
+    int incl = seg;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    __syncthreads();  // s_red reuse
+    if (lane == 31) s_red[warp] = incl;
+    __syncthreads();
+    long long items = 0;
+    for (int w = 0; w < kWarps; ++w) items += s_red[w];
+    if (p.split == 0 && items > p.p_target && S < longest && round < 4) {
+      long long grow = ((long long)S * items + p.p_target - 1) / p.p_target;
+      const int n_long = (longest + S - 1) / S;  // >= 2 since S < longest
+      const long long drop = ((long long)longest + n_long - 2) / (n_long - 1);
+      if (grow < drop) grow = drop;
+      grow = (grow + 15) / 16 * 16;
+      S = (int)(grow > p.Smax ? p.Smax : grow);
+      continue;  // the same decision in every thread
+    }
+    int before = incl - seg;
+    for (int w = 0; w < warp; ++w) before += (int)s_red[w];
+#pragma unroll
+    for (int i = 0; i < kSeg; ++i) {
+      const int b = b0 + i;
+      if (b < p.B) {
+        s_prefix[b] = before;
+        before += ((s_len[b] + S - 1) / S) * U;
+      }
+    }
+    if (tid == 0) {
+      s_prefix[p.B] = (int)items;
+      *s_chunk = S;
+    }
+    break;
   }
   __syncthreads();
 }
@@ -527,7 +539,8 @@ __global__ void __launch_bounds__(kThreads, 2) split_attn_kernel(const SplitPara
     for (int i = 0; i < ntiles; ++i) {
       const int st = (seq + i) % kStages;
       const uint32_t parity = ((seq + i) / kStages) & 1u;
-      if (!mbar_wait_bounded(smem_u32(&bars[st]), parity)) {
+      // one decision for the whole warp: the shuffles below need every lane
+      if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&bars[st]), parity))) {
         ok = false;
         break;
       }

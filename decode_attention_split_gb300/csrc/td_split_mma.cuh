@@ -2,8 +2,8 @@
 //
 // Same method and work decomposition as split_attn_kernel ("tinydecode", section "how the
 // decode step is put together"; "llm-decode-cuda", split-KV attention section): one CTA
-// per (sequence, kv head, row block, chunk) item computes the chunk's partial softmax for
-// every query row reading that kv head, and chunks are merged by log-sum-exp.
+// computes, for one chunk of one (sequence, kv head), the partial softmax of every query row
+// reading that kv head, and chunks are merged by log-sum-exp.
 //
 // The grouped-query rows of a kv head (up to 16 per CTA: G heads x T verify tokens) form
 // the M side of mma.sync m16n8k16 tiles, so each K/V tile in shared memory is read once for
@@ -19,7 +19,10 @@
 // different bank groups; completion is counted on one mbarrier per stage, waited on with a
 // bounded wait. Rows past Smax are zero-filled by the TMA unit; rows past a sequence's
 // length inside its last stage are zeroed in shared memory before use. The 4 warps split
-// every stage's keys 4 ways and combine at the end of the item.
+// every stage's keys 4 ways and combine at the end of the chunk.
+//
+// Two kernels share the chunk code: a persistent one (this file: CTAs walk work items and
+// merge through the workspace) and a cluster one (td_split_cluster.cuh).
 #pragma once
 
 #include <cudaTypedefs.h>
@@ -29,33 +32,34 @@
 
 namespace td {
 
-template <int D, int MT>
+constexpr int kMmaRows = 16;  // query rows per CTA: one m16 tile
+
+template <int D, int NST_>
 struct MmaCfg {
-  static constexpr int KS = kWarps / MT;      // key slices (warps sharing one m tile)
-  static constexpr int ROWS = 16 * MT;        // query rows per CTA
+  static constexpr int NST = NST_;            // ring stages
   static constexpr int TK = 64;               // keys per pipeline stage
-  static constexpr int TKW = TK / KS;         // keys per warp per stage
-  static constexpr int NKSTEP = TKW / 16;     // 16-key steps per warp per stage
+  static constexpr int TKW = TK / kWarps;     // keys per warp per stage
   static constexpr int ROWB = D * 2;          // bytes per cache row
   static constexpr int NCH = ROWB / 16;       // 16-byte chunks per cache row
   static constexpr int HALVES = D / 64;       // 128-byte column halves (TMA boxes per tile)
   static constexpr int BOX_BYTES = TK * 128;  // one box: 64 rows x 128 bytes
-  static constexpr int NST = D == 128 ? 3 : 4;
   static constexpr int TILE_BYTES = TK * ROWB;
   static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
   static constexpr int RING_BYTES = NST * STAGE_BYTES;
-  static constexpr int SMEM_BYTES = RING_BYTES + 1024;  // + room to align the ring to 1024 bytes
   static constexpr int NTD = D / 8;           // 8-wide output n tiles
   static constexpr int KSD = D / 16;          // 16-deep score k steps
-  static constexpr int COMBINE_FLOATS = KS * ROWS * (D + 2);
-  static_assert(TKW % 16 == 0, "each warp takes whole 16-key steps");
+  static constexpr int COMBINE_FLOATS = kWarps * kMmaRows * (D + 2);
+  static_assert(TKW == 16, "each warp takes one 16-key step per stage");
   static_assert(D % 64 == 0, "whole 128-byte halves");
   static_assert(COMBINE_FLOATS * 4 <= RING_BYTES, "combine area fits in the ring");
-  static_assert((merge_fixed_floats<D, ROWS>() + part_block_floats(ROWS, D)) * 4 <= RING_BYTES,
-                "merge stages at least one chunk");
-  static_assert(ROWS * D * 2 <= TILE_BYTES, "the query tile fits in one K tile");
-  static constexpr bool kFits = SMEM_BYTES + 8448 <= 227 * 1024;
+  static_assert(kMmaRows * D * 2 <= TILE_BYTES, "the query tile fits in one K tile");
 };
+
+// Ring depth of the persistent kernel (two CTAs per SM) and of the cluster kernel (one).
+template <int D>
+constexpr int kPersistentStages = D == 128 ? 3 : 4;
+template <int D>
+constexpr int kClusterStages = D == 128 ? 3 : 6;
 
 // Kernel arguments: tensor maps of the two caches, then the common parameters.
 struct MmaArgs {
@@ -88,43 +92,256 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
       : "memory");
 }
 
-template <int D, int MT>
+// Streams keys [c0, c1) of kv head kvh of sequence b (attended length L) for the query rows
+// of row block rb through the ring at `smem` (1024-byte aligned; NST stages with barriers
+// s_bars; `seq` counts the stages this CTA has consumed, for the barrier parities) and leaves
+// the four warps' partial results, in base-2 units, in the combine area at the start of the
+// ring: cm[4][16] (row max), cl[4][16] (row sum), ca[4][16][D] (unnormalised p @ V).
+// Returns false, CTA-uniformly, if a copy never completed: the status bit is set, the other
+// copies in flight have been waited for, and the combine area holds empty partials.
+// Ends with a __syncthreads.
+template <int D, int NST>
+__device__ bool stream_chunk(const MmaArgs &a, unsigned char *smem, uint64_t *s_bars, uint32_t &seq, int b, int kvh,
+                             int rb, int L, int c0, int c1) {
+  using C = MmaCfg<D, NST>;
+  const SplitParams &p = a.p;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int gid = lane >> 2, tig = lane & 3;
+  const uint32_t sbase = smem_u32(smem);
+  const int GT = p.G * p.T;
+  const int nstages = (c1 - c0 + C::TK - 1) / C::TK;
+  const int zc = b * p.Hkv + kvh;  // tensor-map coordinate of this (sequence, kv head)
+  const uint64_t policy = l2_evict_first_policy();
+
+  // stage sidx goes to ring buffer (seq + sidx) % NST
+  auto issue = [&](int sidx) {
+    const int buf = (seq + sidx) % NST;
+    const uint32_t bar = smem_u32(&s_bars[buf]);
+    const uint32_t kdst = sbase + buf * C::STAGE_BYTES;
+    const uint32_t vdst = kdst + C::TILE_BYTES;
+    const int y = c0 + sidx * C::TK;
+    fence_proxy_async_smem();
+    mbar_arrive_expect_tx(bar, 2 * C::TILE_BYTES);
+#pragma unroll
+    for (int h = 0; h < C::HALVES; ++h) {
+      tma_load_3d(kdst + h * C::BOX_BYTES, &a.kmap, 64 * h, y, zc, bar, policy);
+      tma_load_3d(vdst + h * C::BOX_BYTES, &a.vmap, 64 * h, y, zc, bar, policy);
+    }
+  };
+  // the query rows of this row block go to the K tile of the ring buffer the first stage
+  // refills last; they are read into registers before that buffer is refilled
+  const uint32_t qtile = sbase + ((seq + NST - 1) % NST) * C::STAGE_BYTES;
+  for (int idx = tid; idx < kMmaRows * C::NCH; idx += kThreads) {
+    const int r = idx / C::NCH, ch = idx % C::NCH;
+    const int gr = rb * p.R + r;
+    const bool valid = r < p.R && gr < GT;
+    const int hq = kvh * p.G + (valid ? gr / p.T : 0);
+    const int t = valid ? gr % p.T : 0;
+    const unsigned char *qrow =
+        static_cast<const unsigned char *>(p.q) + (((size_t)b * p.Hq + hq) * p.T + t) * C::ROWB;
+    cp_async_16(qtile + swz<C::ROWB>(r, ch), qrow + ch * 16, valid ? 16u : 0u);
+  }
+  cp_async_commit();
+  if (tid == 0) {
+    for (int s2 = 0; s2 < min(NST - 1, nstages); ++s2) issue(s2);
+  }
+
+  // keys visible to rows r0 = gid and r1 = gid + 8 of this row block
+  int lim[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int r = gid + 8 * h;
+    const int gr = rb * p.R + r;
+    const bool valid = r < p.R && gr < GT;
+    lim[h] = valid ? min(max(L - p.T + gr % p.T + 1, 0), c1) : 0;
+  }
+  uint32_t qa[C::KSD][4];  // query rows as mma A fragments, read once the first stage lands
+
+  float o[C::NTD][4];
+#pragma unroll
+  for (int nt = 0; nt < C::NTD; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
+  float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
+
+  int consumed = 0;
+  bool ok = true;
+  for (int st = 0; st < nstages; ++st) {
+    const int buf = (seq + st) % NST;
+    const bool landed = mbar_wait_bounded(smem_u32(&s_bars[buf]), ((seq + st) / NST) & 1u);
+    const int j0 = c0 + st * C::TK;
+    const int valid = min(C::TK, c1 - j0);
+    const uint32_t kt = sbase + buf * C::STAGE_BYTES;
+    const uint32_t vt = kt + C::TILE_BYTES;
+    if (landed && valid < C::TK) {
+      // rows past the sequence's length were fetched (or zero-filled past Smax): zero the
+      // V rows so a masked probability never meets a non-finite value
+      unsigned char *vrow = smem + buf * C::STAGE_BYTES + C::TILE_BYTES;
+      for (int idx = tid; idx < (C::TK - valid) * C::NCH; idx += kThreads) {
+        const int r = valid + idx / C::NCH, ch = idx % C::NCH;
+        *reinterpret_cast<uint4 *>(vrow + tma_swz<C::TK>(r, ch)) = make_uint4(0u, 0u, 0u, 0u);
+      }
+      fence_proxy_async_smem();  // these writes precede the buffer's next refill by the TMA unit
+    }
+    if (st == 0) cp_async_wait<0>();  // this thread's part of the query tile
+    // one decision for the whole CTA: a thread whose wait gave up stops every thread
+    if (!__syncthreads_and(landed)) {
+      ok = false;
+      break;
+    }
+    if (st == 0) {
+#pragma unroll
+      for (int j = 0; j < C::KSD; ++j)
+        ldmatrix_x4(qa[j], qtile + swz<C::ROWB>(((lane >> 3) & 1) * 8 + (lane & 7), 2 * j + (lane >> 4)));
+      __syncthreads();  // every warp holds its query fragments before that buffer is refilled
+    }
+    if (tid == 0 && st + NST - 1 < nstages) issue(st + NST - 1);
+    const int kr = warp * C::TKW;  // first key row (within the stage) of this warp's step
+    const int key0 = j0 + kr;
+    if (key0 < c1) {
+      // S = Q K^T over 16 keys: two 8-key n tiles
+      float sc[2][4];
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+#pragma unroll
+        for (int i = 0; i < C::KSD / 2; ++i) {
+          uint32_t bk[4];
+          ldmatrix_x4(bk, kt + tma_swz<C::TK>(kr + nt * 8 + (lane & 7), 4 * i + (lane >> 3)));
+          mma_bf16_16816(sc[nt], qa[2 * i], bk[0], bk[1]);
+          mma_bf16_16816(sc[nt], qa[2 * i + 1], bk[2], bk[3]);
+        }
+      }
+      // scale to base-2 units, mask, online softmax; row half h holds sc[nt][2h], sc[nt][2h+1]
+      float alpha[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        float mx = -INFINITY;
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int key = key0 + nt * 8 + 2 * tig + e;
+            const float v = key < lim[h] ? sc[nt][2 * h + e] * p.qscale : -INFINITY;
+            sc[nt][2 * h + e] = v;
+            mx = fmaxf(mx, v);
+          }
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        const float m_new = fmaxf(m_run[h], mx);
+        const float base = m_new == -INFINITY ? 0.f : m_new;
+        alpha[h] = exp2f(m_run[h] - base);
+        m_run[h] = m_new;
+        float ps = 0.f;
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const float pv = exp2f(sc[nt][2 * h + e] - base);
+            sc[nt][2 * h + e] = pv;
+            ps += pv;
+          }
+        l_run[h] = l_run[h] * alpha[h] + ps;
+      }
+      if (__any_sync(0xffffffffu, alpha[0] != 1.f || alpha[1] != 1.f)) {
+#pragma unroll
+        for (int nt = 0; nt < C::NTD; ++nt) {
+          o[nt][0] *= alpha[0];
+          o[nt][1] *= alpha[0];
+          o[nt][2] *= alpha[1];
+          o[nt][3] *= alpha[1];
+        }
+      }
+      const uint32_t pa[4] = {pack_bf16x2(sc[0][0], sc[0][1]), pack_bf16x2(sc[0][2], sc[0][3]),
+                              pack_bf16x2(sc[1][0], sc[1][1]), pack_bf16x2(sc[1][2], sc[1][3])};
+      // O += P V over these 16 keys, two 8-wide output tiles per ldmatrix
+#pragma unroll
+      for (int i = 0; i < C::NTD / 2; ++i) {
+        uint32_t bv[4];
+        ldmatrix_x4_trans(bv, vt + tma_swz<C::TK>(kr + (lane & 7) + ((lane >> 3) & 1) * 8, 2 * i + (lane >> 4)));
+        mma_bf16_16816(o[2 * i], pa, bv[0], bv[1]);
+        mma_bf16_16816(o[2 * i + 1], pa, bv[2], bv[3]);
+      }
+    }
+    consumed = st + 1;
+  }
+  if (!ok) {
+    // a copy never completed: wait (bounded) for this chunk's copies in flight, then drop it
+    const int issued = min(nstages, consumed + NST - 1);
+    for (int st = consumed; st < issued; ++st)
+      mbar_wait_bounded(smem_u32(&s_bars[(seq + st) % NST]), ((seq + st) / NST) & 1u);
+    if (tid == 0) report(p.status, TD_DEV_WAIT_TIMEOUT);
+    m_run[0] = m_run[1] = -INFINITY;
+    l_run[0] = l_run[1] = 0.f;
+  }
+  cp_async_wait<0>();
+  seq += nstages;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 1);
+    l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 2);
+  }
+  __syncthreads();  // ring idle: reuse it as the combine area
+  float *combine = reinterpret_cast<float *>(smem);
+  float *cm = combine;
+  float *cl = combine + kWarps * kMmaRows;
+  float *ca = combine + 2 * kWarps * kMmaRows;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int r = gid + 8 * h;
+    if (tig == 0) {
+      cm[warp * kMmaRows + r] = m_run[h];
+      cl[warp * kMmaRows + r] = l_run[h];
+    }
+#pragma unroll
+    for (int nt = 0; nt < C::NTD; ++nt) {
+      float2 v = make_float2(o[nt][2 * h], o[nt][2 * h + 1]);
+      *reinterpret_cast<float2 *>(&ca[(warp * kMmaRows + r) * D + nt * 8 + 2 * tig]) = v;
+    }
+  }
+  __syncthreads();
+  return ok;
+}
+
+// Aligns the dynamic shared memory to 1024 bytes (the 128-byte swizzle is a function of the
+// address); the allocation carries 1024 bytes of slack for this.
+__device__ __forceinline__ unsigned char *align1024(unsigned char *p) {
+  return p + ((1024u - (smem_u32(p) & 1023u)) & 1023u);
+}
+
+// Persistent kernel: CTAs walk the work items of plan_items; chunk partials meet in the
+// workspace and the CTA that completes a group's last chunk merges them (finish_item).
+template <int D>
 __global__ void __launch_bounds__(kThreads, 2) split_attn_mma_kernel(const __grid_constant__ MmaArgs a) {
-  using C = MmaCfg<D, MT>;
+  constexpr int NST = kPersistentStages<D>;
+  using C = MmaCfg<D, NST>;
   using E = __nv_bfloat16;
+  static_assert((merge_fixed_floats<D, kMmaRows>() + part_block_floats(kMmaRows, D)) * 4 <= C::RING_BYTES,
+                "merge stages at least one chunk");
   const SplitParams &p = a.p;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   __shared__ int s_len[TD_MAX_BATCH];
   __shared__ int s_prefix[TD_MAX_BATCH + 1];
   __shared__ long long s_red[2 * kWarps];
-  __shared__ int s_chunk, s_last, s_abort;
+  __shared__ int s_chunk, s_last;
   __shared__ __align__(8) uint64_t s_merge_bar;
-  __shared__ __align__(8) uint64_t s_bars[C::NST];
+  __shared__ __align__(8) uint64_t s_bars[NST];
 
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int gid = lane >> 2, tig = lane & 3;
-  const int mt = warp / C::KS, ks = warp % C::KS;
-  // the 128-byte swizzle is a function of the shared-memory address: align the ring to 1024
-  unsigned char *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  const uint32_t sbase = smem_u32(smem);
+  const int tid = threadIdx.x;
+  unsigned char *smem = align1024(smem_raw);
   float *combine = reinterpret_cast<float *>(smem);
   if (tid == 0) {
     mbar_init(smem_u32(&s_merge_bar), 1);
 #pragma unroll
-    for (int i = 0; i < C::NST; ++i) mbar_init(smem_u32(&s_bars[i]), 1);
+    for (int i = 0; i < NST; ++i) mbar_init(smem_u32(&s_bars[i]), 1);
     fence_mbar_init();
-    s_abort = 0;
   }
   uint32_t merge_phase = 0;
-  uint32_t seq = 0;  // stages consumed so far by this CTA (mbarrier parity bookkeeping)
-  griddep_wait();    // inputs may come from the previous kernel in the stream
+  uint32_t seq = 0;
+  griddep_wait();  // inputs may come from the previous kernel in the stream
   griddep_launch_dependents();
   plan_items(p, s_len, s_prefix, &s_chunk, s_red);  // ends with __syncthreads
   const int S = s_chunk;
   const int W = s_prefix[p.B];
   const int rows = p.Hq * p.T;
-  const int GT = p.G * p.T;
-  const uint64_t policy = l2_evict_first_policy();
 
   // sequences with no key get no item: their rows are 0 with lse = -inf
   for (int b = blockIdx.x; b < p.B; b += gridDim.x) {
@@ -150,208 +367,50 @@ __global__ void __launch_bounds__(kThreads, 2) split_attn_mma_kernel(const __gri
     const int rb = rest % p.RB;
     const int kvh = rest / p.RB;
     const int c0 = c * S;
-    const int c1 = min(c0 + S, L);
-    const int nstages = (c1 - c0 + C::TK - 1) / C::TK;
-    const int zc = b * p.Hkv + kvh;  // tensor-map coordinate of this (sequence, kv head)
-
-    // stage sidx of this item goes to ring buffer (seq + sidx) % NST
-    auto issue = [&](int sidx) {
-      const int buf = (seq + sidx) % C::NST;
-      const uint32_t bar = smem_u32(&s_bars[buf]);
-      const uint32_t kdst = sbase + buf * C::STAGE_BYTES;
-      const uint32_t vdst = kdst + C::TILE_BYTES;
-      const int y = c0 + sidx * C::TK;
-      fence_proxy_async_smem();
-      mbar_arrive_expect_tx(bar, 2 * C::TILE_BYTES);
-#pragma unroll
-      for (int h = 0; h < C::HALVES; ++h) {
-        tma_load_3d(kdst + h * C::BOX_BYTES, &a.kmap, 64 * h, y, zc, bar, policy);
-        tma_load_3d(vdst + h * C::BOX_BYTES, &a.vmap, 64 * h, y, zc, bar, policy);
-      }
-    };
-    // the query rows of this row block go to the K tile of the ring buffer the first stage
-    // refills last; they are read into registers before that buffer is refilled
-    const uint32_t qtile = sbase + ((seq + C::NST - 1) % C::NST) * C::STAGE_BYTES;
-    for (int idx = tid; idx < C::ROWS * C::NCH; idx += kThreads) {
-      const int r = idx / C::NCH, ch = idx % C::NCH;
-      const int gr = rb * p.R + r;
-      const bool valid = r < p.R && gr < GT;
-      const int hq = kvh * p.G + (valid ? gr / p.T : 0);
-      const int t = valid ? gr % p.T : 0;
-      const unsigned char *qrow =
-          static_cast<const unsigned char *>(p.q) + (((size_t)b * p.Hq + hq) * p.T + t) * C::ROWB;
-      cp_async_16(qtile + swz<C::ROWB>(r, ch), qrow + ch * 16, valid ? 16u : 0u);
-    }
-    cp_async_commit();
-    if (tid == 0) {
-      for (int s2 = 0; s2 < min(C::NST - 1, nstages); ++s2) issue(s2);
-    }
-
-    // keys visible to rows r0 = 16*mt + gid and r1 = r0 + 8 of this row block
-    int lim[2];
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int r = mt * 16 + gid + 8 * h;
-      const int gr = rb * p.R + r;
-      const bool valid = r < p.R && gr < GT;
-      lim[h] = valid ? min(max(L - p.T + gr % p.T + 1, 0), c1) : 0;
-    }
-    uint32_t qa[C::KSD][4];  // query rows as mma A fragments, read once the first stage lands
-
-    float o[C::NTD][4];
-#pragma unroll
-    for (int nt = 0; nt < C::NTD; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
-    float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
-
-    int consumed = 0;
-    bool ok = true;
-    for (int st = 0; st < nstages; ++st) {
-      const int buf = (seq + st) % C::NST;
-      if (!mbar_wait_bounded(smem_u32(&s_bars[buf]), ((seq + st) / C::NST) & 1u)) {
-        ok = false;
-        break;
-      }
-      const int j0 = c0 + st * C::TK;
-      const int valid = min(C::TK, c1 - j0);
-      const uint32_t kt = sbase + buf * C::STAGE_BYTES;
-      const uint32_t vt = kt + C::TILE_BYTES;
-      if (valid < C::TK) {
-        // rows past the sequence's length were fetched (or zero-filled past Smax): zero the
-        // V rows so a masked probability never meets a non-finite value
-        unsigned char *vrow = smem + buf * C::STAGE_BYTES + C::TILE_BYTES;
-        for (int idx = tid; idx < (C::TK - valid) * C::NCH; idx += kThreads) {
-          const int r = valid + idx / C::NCH, ch = idx % C::NCH;
-          *reinterpret_cast<uint4 *>(vrow + tma_swz<C::TK>(r, ch)) = make_uint4(0u, 0u, 0u, 0u);
-        }
-        fence_proxy_async_smem();  // these writes precede the buffer's next refill by the TMA unit
-      }
-      if (st == 0) cp_async_wait<0>();  // this thread's part of the query tile
-      __syncthreads();
-      if (st == 0) {
-#pragma unroll
-        for (int j = 0; j < C::KSD; ++j)
-          ldmatrix_x4(qa[j], qtile + swz<C::ROWB>(mt * 16 + ((lane >> 3) & 1) * 8 + (lane & 7), 2 * j + (lane >> 4)));
-        __syncthreads();  // every warp holds its query fragments before that buffer is refilled
-      }
-      if (tid == 0 && st + C::NST - 1 < nstages) issue(st + C::NST - 1);
-#pragma unroll
-      for (int kk = 0; kk < C::NKSTEP; ++kk) {
-        const int kr = ks * C::TKW + kk * 16;  // first key row (within the stage) of this step
-        const int key0 = j0 + kr;
-        if (key0 >= c1) break;
-        // S = Q K^T over 16 keys: two 8-key n tiles
-        float sc[2][4];
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-          sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
-#pragma unroll
-          for (int i = 0; i < C::KSD / 2; ++i) {
-            uint32_t bk[4];
-            ldmatrix_x4(bk, kt + tma_swz<C::TK>(kr + nt * 8 + (lane & 7), 4 * i + (lane >> 3)));
-            mma_bf16_16816(sc[nt], qa[2 * i], bk[0], bk[1]);
-            mma_bf16_16816(sc[nt], qa[2 * i + 1], bk[2], bk[3]);
-          }
-        }
-        // scale to base-2 units, mask, online softmax; row half h holds sc[nt][2h], sc[nt][2h+1]
-        float alpha[2];
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          float mx = -INFINITY;
-#pragma unroll
-          for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const int key = key0 + nt * 8 + 2 * tig + e;
-              const float v = key < lim[h] ? sc[nt][2 * h + e] * p.qscale : -INFINITY;
-              sc[nt][2 * h + e] = v;
-              mx = fmaxf(mx, v);
-            }
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-          const float m_new = fmaxf(m_run[h], mx);
-          const float base = m_new == -INFINITY ? 0.f : m_new;
-          alpha[h] = exp2f(m_run[h] - base);
-          m_run[h] = m_new;
-          float ps = 0.f;
-#pragma unroll
-          for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const float pv = exp2f(sc[nt][2 * h + e] - base);
-              sc[nt][2 * h + e] = pv;
-              ps += pv;
-            }
-          l_run[h] = l_run[h] * alpha[h] + ps;
-        }
-        if (__any_sync(0xffffffffu, alpha[0] != 1.f || alpha[1] != 1.f)) {
-#pragma unroll
-          for (int nt = 0; nt < C::NTD; ++nt) {
-            o[nt][0] *= alpha[0];
-            o[nt][1] *= alpha[0];
-            o[nt][2] *= alpha[1];
-            o[nt][3] *= alpha[1];
-          }
-        }
-        const uint32_t pa[4] = {pack_bf16x2(sc[0][0], sc[0][1]), pack_bf16x2(sc[0][2], sc[0][3]),
-                                pack_bf16x2(sc[1][0], sc[1][1]), pack_bf16x2(sc[1][2], sc[1][3])};
-        // O += P V over these 16 keys, two 8-wide output tiles per ldmatrix
-#pragma unroll
-        for (int i = 0; i < C::NTD / 2; ++i) {
-          uint32_t bv[4];
-          ldmatrix_x4_trans(bv, vt + tma_swz<C::TK>(kr + (lane & 7) + ((lane >> 3) & 1) * 8, 2 * i + (lane >> 4)));
-          mma_bf16_16816(o[2 * i], pa, bv[0], bv[1]);
-          mma_bf16_16816(o[2 * i + 1], pa, bv[2], bv[3]);
-        }
-      }
-      consumed = st + 1;
-    }
-    if (!ok) {
-      // a copy never completed: wait (bounded) for the rest of this item's copies in flight,
-      // then drop the item
-      const int issued = min(nstages, consumed + C::NST - 1);
-      for (int st = consumed; st < issued; ++st)
-        mbar_wait_bounded(smem_u32(&s_bars[(seq + st) % C::NST]), ((seq + st) / C::NST) & 1u);
-      if (tid == 0) {
-        report(p.status, TD_DEV_WAIT_TIMEOUT);
-        s_abort = 1;
-      }
-      m_run[0] = m_run[1] = -INFINITY;
-      l_run[0] = l_run[1] = 0.f;
-#pragma unroll
-      for (int nt = 0; nt < C::NTD; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
-    }
-    cp_async_wait<0>();
-    seq += nstages;
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 1);
-      l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 2);
-    }
-    __syncthreads();  // ring idle: reuse it as the combine area
-    float *cm = combine;
-    float *cl = combine + C::KS * C::ROWS;
-    float *ca = combine + 2 * C::KS * C::ROWS;
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int r = mt * 16 + gid + 8 * h;
-      if (tig == 0) {
-        cm[ks * C::ROWS + r] = m_run[h];
-        cl[ks * C::ROWS + r] = l_run[h];
-      }
-#pragma unroll
-      for (int nt = 0; nt < C::NTD; ++nt) {
-        float2 v = make_float2(o[nt][2 * h], o[nt][2 * h + 1]);
-        *reinterpret_cast<float2 *>(&ca[(ks * C::ROWS + r) * D + nt * 8 + 2 * tig]) = v;
-      }
-    }
-    __syncthreads();
-    finish_item<E, D, C::ROWS, C::KS>(p, combine, C::RING_BYTES / 4, &s_merge_bar, merge_phase, b, kvh, rb, c, NC,
-                                      &s_last);
+    const bool ok = stream_chunk<D, NST>(a, smem, s_bars, seq, b, kvh, rb, L, c0, min(c0 + S, L));
+    finish_item<E, D, kMmaRows, kWarps>(p, combine, C::RING_BYTES / 4, &s_merge_bar, merge_phase, b, kvh, rb, c, NC,
+                                        &s_last);
     // the combine and merge wrote the ring through the generic proxy; the next item's first
     // stages refill it through the asynchronous proxy
     fence_proxy_async_smem();
     __syncthreads();
-    if (s_abort) break;
+    if (!ok) break;  // a copy never completed: stop taking items
+  }
+}
+
+// Combines the kWarps partial sources left by stream_chunk (base-2 units) into one partial
+// block at `dst` (generic address, possibly another CTA's shared memory): acc[R][D], then
+// m[R] (natural-log units) and l[R], for rows r < nv.
+template <int D>
+__device__ void combine_block(const float *combine, float *dst, int R, int nv) {
+  constexpr int D4 = D / 4;
+  const float *cm = combine;
+  const float *cl = combine + kWarps * kMmaRows;
+  const float *ca = combine + 2 * kWarps * kMmaRows;
+  for (int idx = threadIdx.x; idx < nv * D4; idx += kThreads) {
+    const int r = idx / D4, d = (idx % D4) * 4;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, cm[w * kMmaRows + r]);
+    float Ls = 0.f;
+    float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) {
+        const float mw = cm[w * kMmaRows + r];
+        if (mw != -INFINITY) {
+          const float f = exp2f(mw - M);
+          Ls = fmaf(cl[w * kMmaRows + r], f, Ls);
+          const float4 v = *reinterpret_cast<const float4 *>(ca + (w * kMmaRows + r) * D + d);
+          A.x = fmaf(v.x, f, A.x), A.y = fmaf(v.y, f, A.y), A.z = fmaf(v.z, f, A.z), A.w = fmaf(v.w, f, A.w);
+        }
+      }
+    }
+    *reinterpret_cast<float4 *>(dst + r * D + d) = A;
+    if (d == 0) {
+      dst[R * D + r] = Ls > 0.f ? M * kLn2 : -INFINITY;
+      dst[R * D + R + r] = Ls;
+    }
   }
 }
 

@@ -91,6 +91,25 @@ int td_last_cuda_error(void);
 size_t td_decode_workspace_bytes(int B, int Hq, int Hkv, int Smax, int D, int q_len, int split);
 
 /*
+ * The launch td_decode_attn (q_len = 1) or td_verify_attn (q_len = T) makes for these
+ * arguments on the current CUDA device; nothing is launched. Outputs are host pointers,
+ * each nullable:
+ *   *kernel  0: CUDA-core split kernel (fp32 caches);
+ *            1: tensor-core persistent kernel (bf16; CTAs walk (b, kv head, row block, chunk)
+ *               items, partials meet in the workspace and the CTA finishing a group's last
+ *               chunk merges them);
+ *            2: tensor-core cluster kernel (bf16, split = 0, few groups: one thread-block
+ *               cluster per (b, kv head, row block), one chunk per CTA, the merge done in
+ *               distributed shared memory; the workspace is not touched);
+ *   *grid    CTAs launched;  *cluster  CTAs per cluster (0 unless kernel 2);
+ *   *rows    query rows per CTA.
+ * Returns what the attention call would return for a bad shape, TD_ERR_CUDA without a device.
+ */
+td_status td_split_plan(td_dtype dtype, int B, int Hq, int Hkv, int Smax, int D, int q_len, int split, int *kernel,
+                        int *grid, int *cluster, int *rows);
+
+/*
+ * Cache append:/*
  * Cache append: for each b with 0 <= L = seq_lens[b] and L + T <= Smax, copies
  * k_new[b, h, t, :] to k_cache[b, h, L + t, :] (and v likewise) bit for bit for all h < Hkv,
  * t < T. With advance != 0, seq_lens[b] += T afterwards (same launch, after every read of

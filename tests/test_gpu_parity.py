@@ -166,6 +166,44 @@ def test_verify_equals_sequential_decode(td):
         assert_out_close(out[:, :, t], o_t[:, :, 0].double().numpy(), "bf16", what=f"token {t}")
 
 
+# --------------------------------------------------------------------------- cluster kernel
+
+CLUSTER = [
+    # D, Hq, Hkv, Smax, T, lengths: enough (b, kv head, row block) groups for one wave of
+    # clusters, automatic split
+    (128, 24, 8, 4096, 1, [4096, 4000, 1, 0]),                 # 32 groups: clusters of 8
+    (128, 24, 8, 2000, 1, [1999, 1999, 65, 64]),               # ragged last stages
+    (128, 24, 8, 300, 1, [65, 1, 0, 300, 299, 128, 64, 3]),    # 64 groups: clusters of 4
+    (64, 64, 8, 1000, 1, [1000, 999, 500, 17, 1, 0, 640, 64]),  # 8 heads per kv head
+    (64, 32, 8, 700, 1, [700] * 12 + [1, 0, 333, 64]),         # 128 groups: clusters of 2
+    (128, 32, 8, 700, 6, [690, 100]),                          # verify: 24 rows in two row blocks
+    (128, 32, 8, 64, 6, [64, 3]),                              # verify with a short sequence
+    (128, 24, 8, 1000, 1, [1000, 1000, 999, 1000]),            # Smax not a stage multiple
+]
+
+
+@pytest.mark.parametrize("D,Hq,Hkv,Smax,T,lens", CLUSTER)
+def test_cluster_kernel_against_oracle_and_persistent(td, D, Hq, Hkv, Smax, T, lens):
+    B = len(lens)
+    plan = td.td_split_plan(torch.bfloat16, B, Hq, Hkv, Smax, D, T, 0)
+    assert plan["kernel"] == "tensor_core_cluster", plan
+    assert plan["grid"] % plan["cluster"] == 0 and plan["cluster"] in (2, 4, 8, 16)
+    case = small_case(dtype="bf16", B=B, Hq=Hq, Hkv=Hkv, D=D, Smax=Smax, T=T, seq_lens=lens, seed=Smax + T,
+                      heavy=0.02)
+    out_c, lse_c = check_case(td, case, split=0)
+    # the persistent kernel (fixed chunks) on the same inputs agrees within the same tolerance
+    assert td.td_split_plan(torch.bfloat16, B, Hq, Hkv, Smax, D, T, 128)["kernel"] == "tensor_core_persistent"
+    out_p, lse_p = check_case(td, case, split=128)
+    assert_out_close(out_c, out_p.double().numpy(), "bf16", what="cluster vs persistent")
+
+
+def test_automatic_split_fills_one_wave(td):
+    """Uniform batches whose per-sequence chunk round-up would overshoot the grid still match."""
+    for B, L in ((8, 3000), (4, 2900)):
+        case = small_case(dtype="bf16", B=B, Hq=32, Hkv=8, D=128, Smax=L, seq_lens=[L] * B, seed=B, heavy=0.01)
+        check_case(td, case, split=0)
+
+
 # ------------------------------------------------------------------------- full-size workloads
 
 @pytest.mark.parametrize("name", ["tiny_fp32", "smollm2_360m", "llama3b"])

@@ -124,7 +124,7 @@ def test_hot_kernels_have_no_spills(lib):
     log = open(td_build.PTXAS_LOG).read()
     entries = re.findall(r"Compiling entry function '(\w+)'.*?\n(?:.*?\n)*?\s+(\d+) bytes stack frame, (\d+) bytes "
                          r"spill stores, (\d+) bytes spill loads", log)
-    hot = {"split_attn_mma_kernelILi128ELi1E", "split_attn_mma_kernelILi64ELi1E", "split_attn_kernelIfLi64ELi2E"}
+    hot = {"split_attn_mma_kernelILi128EEEv", "split_attn_mma_kernelILi64EEEv", "split_attn_kernelIfLi64ELi2E"}
     seen = set()
     for name, _stack, st, ld in entries:
         for h in hot:
