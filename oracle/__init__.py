@@ -11,7 +11,8 @@ oracle widens them exactly). Layouts are the library's: q/out [B, Hq, T, D], cac
 [B, Hkv, Smax, D], seq_lens int32 [B].
 
 Sources: "tinydecode", sections "how the decode step is put together" and "speculative
-decoding"; "llm-decode-cuda", the split-KV ("flash-decoding") attention section.
+decoding"; "llm-decode-cuda", the split-KV ("flash-decoding") attention section and the
+"RoPE + KV-cache write" step of its decode loop.
 """
 from __future__ import annotations
 
@@ -95,6 +96,8 @@ class Oracle:
         lib.orc_lse_merge.restype = None
         lib.orc_kv_append.argtypes = [i, vp, vp, vp, vp, vp, i, i, i, i, i, i]
         lib.orc_kv_append.restype = ctypes.c_uint
+        lib.orc_rope.argtypes = [i, vp, ctypes.c_int64, i, vp, vp, vp, vp]
+        lib.orc_rope.restype = None
         lib.orc_num_threads.restype = i
         lib.orc_mutant.restype = i
         self.lib = lib
@@ -168,3 +171,52 @@ class Oracle:
             raise TypeError("seq_lens must be a contiguous int32 array")
         return int(self.lib.orc_kv_append(k_new.dtype.itemsize, _ptr(k_new), _ptr(v_new), _ptr(k_cache),
                                            _ptr(v_cache), _ptr(seq_lens), B, Hkv, T, Smax, D, int(bool(advance))))
+
+    def rope(self, x, pos, cos_t, sin_t):
+        """Rotary embedding of rows x[..., D] at positions pos (shape x.shape[:-1]), rotate-half
+        pairs, angles from fp32 tables [positions, D/2]; exact, rounded once to x's type."""
+        x = np.ascontiguousarray(x)
+        D = x.shape[-1]
+        pos = np.ascontiguousarray(np.broadcast_to(pos, x.shape[:-1]), dtype=np.int32)
+        cos_t = np.ascontiguousarray(cos_t, dtype=np.float32)
+        sin_t = np.ascontiguousarray(sin_t, dtype=np.float32)
+        if D % 2 or cos_t.shape != sin_t.shape or cos_t.shape[1] != D // 2:
+            raise ValueError("tables must be [positions, D/2]")
+        if pos.size and (pos.min() < 0 or pos.max() >= cos_t.shape[0]):
+            raise ValueError("position outside the tables")
+        y = np.empty_like(x)
+        self.lib.orc_rope(_code(x), _ptr(x), pos.size, D, _ptr(pos), _ptr(cos_t), _ptr(sin_t), _ptr(y))
+        return y
+
+    def rope_append_attention(self, q, k_new, v_new, k_cache, v_cache, seq_lens, scale: float, cos_t=None,
+                              sin_t=None, advance: bool = True):
+        """One decode (T = 1) or verify (T > 1) step: token t of sequence b sits at position
+        P = seq_lens[b] + t; q and k_new are rotated there (when tables are given), the rotated
+        keys and the values are written into the caches, and every query row attends over the
+        L_b + T keys it may see. Caches (and seq_lens, with advance) change in place.
+
+        A sequence whose rows do not fit (seq_lens[b] < 0 or seq_lens[b] + T > Smax) is left
+        untouched, flagged APPEND_OVERFLOW, and its rows give out = 0, lse = -inf.
+        Returns (out float64 [B, Hq, T, D], lse float64 [B, Hq, T], status bits)."""
+        B, Hq, T, D = q.shape
+        Smax = k_cache.shape[2]
+        pre = np.array(seq_lens, dtype=np.int64)
+        fits = (pre >= 0) & (pre + T <= Smax)
+        pos = np.where(fits, pre, 0)[:, None] + np.arange(T)[None, :]  # [B, T]
+        if cos_t is not None:
+            q = self.rope(q, np.broadcast_to(pos[:, None, :], (B, Hq, T)), cos_t, sin_t)
+            k_new = self.rope(k_new, np.broadcast_to(pos[:, None, :], (B, k_new.shape[1], T)), cos_t, sin_t)
+        work = np.ascontiguousarray(seq_lens, dtype=np.int32).copy()
+        status = self.kv_append(np.ascontiguousarray(k_new), np.ascontiguousarray(v_new), k_cache, v_cache, work,
+                                advance=True)
+        out = np.zeros((B, Hq, T, D), np.float64)
+        lse = np.full((B, Hq, T), -np.inf)
+        idx = np.nonzero(fits)[0]
+        if idx.size:
+            o, l, st = self.attention(np.ascontiguousarray(q[idx]), np.ascontiguousarray(k_cache[idx]),
+                                      np.ascontiguousarray(v_cache[idx]), work[idx], scale)
+            out[idx], lse[idx] = o, l
+            status |= st
+        if advance:
+            seq_lens[...] = work
+        return out, lse, int(status)

@@ -21,6 +21,11 @@
  *       section: the context is split into chunks, one block per (kv head, chunk) serves
  *       every query head sharing that kv head and computes a partial softmax, and the chunks
  *       are merged with the log-sum-exp trick.
+ *   [rope]  "tinydecode" lists an in-place rope kernel for its llama models (loaded from
+ *       Hugging Face llama checkpoints); "llm-decode-cuda" fuses "RoPE + KV-cache write"
+ *       into its decode step. Neither prints the rotation; the reading taken is the llama
+ *       checkpoints' layout (pairs (i, i + D/2), "rotate half"), with the angles given as
+ *       cos/sin tables indexed by position.
  *
  * Layouts (row-major, contiguous):
  *   q, out      [B, Hq, T, D]      (T = 1 for single-token decode)
@@ -34,7 +39,10 @@
  *   - row t of a T-token chunk sees keys j < L - T + t + 1, where L counts the T new tokens.
  *   - a row that sees no key has out = 0 and lse = -inf.
  *   - partial acc is stored unnormalised (the pages name the triple (m, l, acc)).
+ *   - a rotated row is evaluated exactly and rounded once, to nearest even, to the stored
+ *     type (the rotated key is what the cache holds; the rotated query is what attends).
  */
+#include <float.h>
 #include <math.h>
 #include <stdint.h>
 #include <stdlib.h>
@@ -334,4 +342,76 @@ unsigned orc_kv_append(int elem_bytes, const void *k_new, const void *v_new, voi
 #endif
   }
   return status;
+}
+
+/* An exact value rounded to the stored element type, to nearest with ties to even. fp32 by
+ * the C conversion (the default rounding mode); bf16 directly from the fp64 value: 8
+ * significant bits in the binary32 exponent range (multiples of 2^-133 below 2^-126). */
+static void narrow(int dtype, void *base, int64_t i, double x) {
+  if (dtype == ORC_F32) {
+    ((float *)base)[i] = (float)x;
+    return;
+  }
+  if (dtype == ORC_F64) {
+    ((double *)base)[i] = x;
+    return;
+  }
+  uint16_t h;
+  const uint16_t sign = signbit(x) ? 0x8000u : 0u;
+  const double a = fabs(x);
+  if (isnan(x)) {
+    h = 0x7FC0u;
+  } else if (a == 0.0) {
+    h = sign;
+  } else {
+    double y;
+    if (a < ldexp(1.0, -126)) {
+      y = ldexp(nearbyint(ldexp(a, 133)), -133);
+    } else {
+      int e;
+      const double m = frexp(a, &e); /* a = m 2^e, m in [0.5, 1) */
+      y = ldexp(nearbyint(ldexp(m, 8)), e - 8);
+    }
+    if (y >= ldexp(1.0, 128)) {
+      h = (uint16_t)(sign | 0x7F80u); /* infinity */
+    } else {
+      const float f = (float)y; /* exact: at most 8 significant bits */
+      uint32_t u;
+      memcpy(&u, &f, sizeof u);
+      h = (uint16_t)(sign | (u >> 16));
+    }
+  }
+  ((uint16_t *)base)[i] = h;
+}
+
+/* Rotary position embedding [rope] of `rows` rows of D elements, row r at position pos[r]:
+ * for i < D/2 the pair (x[i], x[i + D/2]) turns by the angle whose cosine and sine are
+ * cos_t[pos][i] and sin_t[pos][i] (fp32 tables [positions][D/2]):
+ *   y[i]       = x[i] cos - x[i + D/2] sin
+ *   y[i + D/2] = x[i + D/2] cos + x[i] sin
+ * evaluated in fp64 from the stored inputs and rounded once to the stored type. */
+void orc_rope(int dtype, const void *x, int64_t rows, int D, const int32_t *pos, const float *cos_t,
+              const float *sin_t, void *y) {
+  const int half = D / 2;
+  for (int64_t r = 0; r < rows; ++r) {
+    const int64_t p = pos[r];
+    for (int i = 0; i < half; ++i) {
+#if ORC_MUTANT == 15
+      /* planted: neighbouring elements (2i, 2i + 1) taken as the pair */
+      const int64_t a = r * D + 2 * i, b = r * D + 2 * i + 1;
+#else
+      const int64_t a = r * D + i, b = r * D + i + half;
+#endif
+      const double c = (double)cos_t[p * half + i], s = (double)sin_t[p * half + i];
+      const double x0 = widen(dtype, x, a), x1 = widen(dtype, x, b);
+#if ORC_MUTANT == 14
+      /* planted: turns the other way */
+      narrow(dtype, y, a, x0 * c + x1 * s);
+      narrow(dtype, y, b, x1 * c - x0 * s);
+#else
+      narrow(dtype, y, a, x0 * c - x1 * s);
+      narrow(dtype, y, b, x1 * c + x0 * s);
+#endif
+    }
+  }
 }

@@ -10,6 +10,11 @@ oracle (wrong head mapping, dropped scale, off-by-one mask, lse without its max,
 without rescale, transposed cache, wrong 16-bit format, append position or advance)
 fails at least one of them; the mutant test checks exactly that.
 
+Rotary embedding (a reading: the pages name an in-place rope kernel and a fused
+"RoPE + KV-cache write" but print no formula) is pinned to complex multiplication by
+e^{i angle} in numpy, to an exact quarter turn, to the identity at angle 0 and to the
+relative-position property of the attention scores; the fused step is pinned to its parts.
+
 Sources: "tinydecode", sections "how the decode step is put together" (static cache,
 seq_lens mask, split chunks merged by log-sum-exp, q head -> kv head index math) and
 "speculative decoding" (verify chunk causal among the new tokens, rollback by seq_lens);
@@ -305,6 +310,84 @@ def pin_append_overflow(orc):
     assert st == orc_mod.APPEND_OVERFLOW
     assert np.array_equal(seq, [6, 8, -1])
     assert k2[0].sum() == 0 and k2[2].sum() == 0 and k2[1, 0, 5:8].sum() == 3 * 4
+
+
+# --- rotary embedding and the fused step ------------------------------------------------------
+
+def _tables(P, D, base=10000.0):
+    """cos/sin tables [P, D/2] of the angles p * base^(-2i/D), computed in fp64, stored fp32."""
+    ang = np.arange(P, dtype=F64)[:, None] * base ** (-np.arange(0, D, 2, dtype=F64) / D)[None, :]
+    return np.cos(ang).astype(np.float32), np.sin(ang).astype(np.float32)
+
+
+def _half_ulp(y, mant_bits):
+    """Half a unit in the last place of a float with `mant_bits` stored mantissa bits, at |y|."""
+    _, e = np.frexp(np.abs(y))  # |y| in [2^(e-1), 2^e)
+    return np.ldexp(1.0, e - 2 - mant_bits)
+
+
+def pin_rope_quarter_turn(orc):
+    """D=2: a quarter turn sends (1, 0) to (0, 1) and (0, 1) to (-1, 0); angle 0 is the identity."""
+    x = np.array([[1.0, 0.0], [0.0, 1.0], [0.3, -2.0]], np.float32)
+    cos_t = np.array([[1.0], [0.0]], np.float32)
+    sin_t = np.array([[0.0], [1.0]], np.float32)
+    y = orc.rope(x, np.array([1, 1, 0]), cos_t, sin_t)
+    assert np.array_equal(y, np.array([[0.0, 1.0], [-1.0, 0.0], [0.3, -2.0]], np.float32))
+
+
+def pin_rope_is_complex_multiplication(orc):
+    """Pair (x[i], x[i + D/2]) as x[i] + j x[i + D/2], times cos + j sin (numpy complex128):
+    the stored result is that product rounded to nearest (within half an ulp), bf16 and fp32."""
+    rng = np.random.default_rng(3)
+    D, n, P = 16, 40, 64
+    cos_t, sin_t = _tables(P, D)
+    pos = rng.integers(0, P, n)
+    for dtype, mant in (("bf16", 7), ("f32", 23)):
+        xt = torch.from_numpy(rng.standard_normal((n, D)).astype(np.float32))
+        x = _np(xt.to(torch.bfloat16)) if dtype == "bf16" else xt.numpy()
+        xv = (xt.to(torch.bfloat16) if dtype == "bf16" else xt).double().numpy()
+        z = (xv[:, :D // 2] + 1j * xv[:, D // 2:]) * (cos_t[pos].astype(F64) + 1j * sin_t[pos].astype(F64))
+        ref = np.concatenate([z.real, z.imag], axis=1)
+        y = orc.rope(x, pos, cos_t, sin_t)
+        yv = torch.from_numpy(y.view(np.int16)).view(torch.bfloat16).double().numpy() if dtype == "bf16" else \
+            y.astype(F64)
+        assert np.all(np.abs(yv - ref) <= _half_ulp(ref, mant) * (1 + 1e-12)), dtype
+
+
+def pin_rope_relative_position(orc):
+    """With tables of angles p * theta_i, the score of a query at position m and a key at n
+    depends only on m - n: <rope(q, m), rope(k, n)> = <rope(q, m - n), k>."""
+    rng = np.random.default_rng(4)
+    D, P = 32, 200
+    cos_t, sin_t = _tables(P, D)
+    q = rng.standard_normal((1, D)).astype(np.float32)
+    k = rng.standard_normal((1, D)).astype(np.float32)
+    for m, n in ((7, 3), (150, 20), (64, 64)):
+        lhs = float(orc.rope(q, [m], cos_t, sin_t)[0].astype(F64) @ orc.rope(k, [n], cos_t, sin_t)[0].astype(F64))
+        rhs = float(orc.rope(q, [m - n], cos_t, sin_t)[0].astype(F64) @ k[0].astype(F64))
+        assert abs(lhs - rhs) <= 1e-4 * (1 + abs(rhs)), (m, n, lhs, rhs)
+
+
+def pin_fused_step_is_its_parts(orc):
+    """rope_append_attention = rotate (pinned above) + cache write + attention, token t of
+    sequence b at position seq_lens[b] + t; a sequence that does not fit is untouched,
+    flagged, and gives out = 0, lse = -inf."""
+    case = small_case(dtype="bf16", B=3, Hq=4, Hkv=2, D=16, Smax=20, T=2, seq_lens=[5, 18, 0], seed=7)
+    cos_t, sin_t = _tables(20, 16)
+    rng = np.random.default_rng(5)
+    k_new = _np(torch.from_numpy(rng.standard_normal((3, 2, 2, 16)).astype(np.float32)).to(torch.bfloat16))
+    v_new = _np(torch.from_numpy(rng.standard_normal((3, 2, 2, 16)).astype(np.float32)).to(torch.bfloat16))
+    kc, vc, sl = _np(case.k_cache).copy(), _np(case.v_cache).copy(), np.array([5, 19, 0], np.int32)
+    out, lse, st = orc.rope_append_attention(_np(case.q), k_new, v_new, kc, vc, sl, 0.25, cos_t, sin_t)
+    assert st == orc_mod.APPEND_OVERFLOW and sl.tolist() == [7, 19, 2]
+    for b, L in ((0, 5), (2, 0)):
+        pos = np.array([L, L + 1])
+        assert np.array_equal(kc[b, :, L:L + 2], orc.rope(k_new[b], np.broadcast_to(pos, (2, 2)), cos_t, sin_t))
+        assert np.array_equal(vc[b, :, L:L + 2], v_new[b])
+        qr = orc.rope(_np(case.q)[b:b + 1], np.broadcast_to(pos, (1, 4, 2)), cos_t, sin_t)
+        ref, ref_lse, _ = orc.attention(qr, kc[b:b + 1], vc[b:b + 1], np.array([L + 2], np.int32), 0.25)
+        assert np.array_equal(out[b:b + 1], ref) and np.array_equal(lse[b:b + 1], ref_lse)
+    assert np.array_equal(kc[1], _np(case.k_cache)[1]) and np.all(out[1] == 0) and np.all(np.isneginf(lse[1]))
 
 
 PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_") and callable(v)]

@@ -18,6 +18,8 @@ MUTANTS = {
     11: "append does not advance seq_lens",
     12: "decode reads one row past seq_len",
     13: "bf16 bits read as IEEE half",
+    14: "rotary pairs turned the wrong way",
+    15: "rotary pairs taken as neighbours (2i, 2i+1)",
 }
 
 
