@@ -3,10 +3,12 @@
 
 Workload (one layer of a 3B Llama-style model): B=1, Hq=24, Hkv=8, D=128, bf16 KV cache
 of Smax=32768 rows, attended length 32768, automatic split. One *call* is the hot path
-for one decode token: append the new key/value row (td_kv_append) and attend
-(td_decode_attn). One *step* is a batch of R such calls, each on its own query and new
-row, rotating over C copies of the cache so that every call's 134 MB of KV reads come from
-HBM (C * 134 MB > 4x L2), captured once as a CUDA graph and replayed.
+for one decode token: write the new key/value row into the cache and attend, in one launch
+(td_rope_append_attn without rotation tables; the same result as td_kv_append followed by
+td_decode_attn, whose timing is reported beside it). One *step* is a batch of R such calls,
+each on its own query and new row, rotating over C copies of the cache so that every
+call's 134 MB of KV reads come from HBM (C * 134 MB > 4x L2), captured once as a CUDA graph
+and replayed.
 
   value      KV-read GB/s = KV bytes attended / device time, inputs resident in HBM
   e2e        the same through the Python API with host buffers: every call copies its q
@@ -325,10 +327,21 @@ def run_td(args, world, rank, local):
     ws = td.make_workspace(w.B, w.Hq, w.Hkv, w.Smax, w.D, 1, 0, device=dev)
     s = torch.cuda.Stream(dev)
 
-    def calls(append=True):
+    from decode_attention_split_gb300.workloads import rope_tables
+    cos_t, sin_t = (t.to(dev) for t in rope_tables(w.Smax, w.D))
+
+    def calls(mode="fused"):
+        """fused: one launch per call (cache write + attention); rope: the same with the query and
+        key rotated; separate: td_kv_append then td_decode_attn; attn: the attention alone."""
         for i in range(R):
             c = i % C
-            if append:
+            if mode in ("fused", "rope"):
+                rot = mode == "rope"
+                td.td_rope_append_attn(q[i][:, :, None], kn[i], vn[i], kc[c], vc[c], sl_pre, case.scale, 0,
+                                       cos_t=cos_t if rot else None, sin_t=sin_t if rot else None, advance=False,
+                                       out=out[i][:, :, None], workspace=ws, stream=s)
+                continue
+            if mode == "separate":
                 td.td_kv_append(kn[i], vn[i], kc[c], vc[c], sl_pre, advance=False, stream=s)
             td.td_decode_attn(q[i], kc[c], vc[c], sl_post, case.scale, 0, out=out[i], workspace=ws, stream=s)
 
@@ -340,19 +353,23 @@ def run_td(args, world, rank, local):
                 c = i % C
                 td.td_kv_append(kn[i], vn[i], kc[c], vc[c], sl_pre, advance=False, stream=s)
                 td.td_decode_attn(q[i], kc[c], vc[c], sl_post, case.scale, 0, out=out[i], workspace=ws, stream=s)
+            for i in range(args.profile_launches):
+                c = i % C
+                td.td_rope_append_attn(q[i][:, :, None], kn[i], vn[i], kc[c], vc[c], sl_pre, case.scale, 0,
+                                       advance=False, out=out[i][:, :, None], workspace=ws, stream=s)
         s.synchronize()
         print(json.dumps({"profile_launches": args.profile_launches, "ok": True}))
         return
 
-    with torch.cuda.stream(s):
-        calls()
-    s.synchronize()
-    g_step = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g_step, stream=s):
-        calls(append=True)
-    g_attn = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g_attn, stream=s):
-        calls(append=False)
+    graphs = {}
+    for mode in ("separate", "rope", "attn", "fused"):  # the timed step's graph is captured last
+        with torch.cuda.stream(s):
+            calls(mode)
+        s.synchronize()
+        graphs[mode] = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graphs[mode], stream=s):
+            calls(mode)
+    g_step, g_attn = graphs["fused"], graphs["attn"]
 
     with torch.cuda.stream(s):  # graph replays launch on the current stream
         for _ in range(args.warmup):
@@ -371,6 +388,9 @@ def run_td(args, world, rank, local):
         e1.synchronize()
         torch.cuda.synchronize()
         ms_attn = time_graph(g_attn, s, args.steps, warm=2)
+        ms_separate = time_graph(graphs["separate"], s, max(3, args.steps // 4), warm=2) * args.steps / \
+            max(3, args.steps // 4)
+        ms_rope = time_graph(graphs["rope"], s, max(3, args.steps // 4), warm=2) * args.steps / max(3, args.steps // 4)
     ms = e0.elapsed_time(e1)
     if world > 1:
         t = torch.tensor([ms, ms_attn], dtype=torch.float64, device=dev)
@@ -378,16 +398,19 @@ def run_td(args, world, rank, local):
         ms, ms_attn = float(t[0]), float(t[1])
         torch.distributed.barrier()
 
-    # correctness of what was timed: call 0 of the last replay against the oracle
+    # correctness of what was timed: one more replay of the step graph, then its call 0 (which
+    # wrote its own new row into copy 0 and attended over it) against the oracle
     checked = None
+    with torch.cuda.stream(s):
+        g_step.replay()
+    s.synchronize()
     if rank == 0:
         import numpy as np
         import oracle
         ek = to_numpy(case.k_cache).copy()
         ev = to_numpy(case.v_cache).copy()
-        last = ((R - 1) // C) * C  # the last call that appended into copy 0 before out[0] was computed
-        ek[:, :, L - 1] = to_numpy(knh[last])[:, :, 0]
-        ev[:, :, L - 1] = to_numpy(vnh[last])[:, :, 0]
+        ek[:, :, L - 1] = to_numpy(knh[0])[:, :, 0]
+        ev[:, :, L - 1] = to_numpy(vnh[0])[:, :, 0]
         ref, _, _ = oracle.load().attention(to_numpy(qh[0]), ek, ev, np.array([L], np.int32), case.scale)
         got = out[0].double().cpu().numpy()
         checked = bool(np.all(np.abs(got - ref) <= 2e-2 + 1e-2 * np.abs(ref)))
@@ -433,7 +456,12 @@ def run_td(args, world, rank, local):
         "frac_of_measured_hbm": round(value / world / peak, 4),
         "checked_against_oracle": checked,
         "clocks": clk.summary(),
-        "gpu_launches": 2 * total_calls,
+        "gpu_launches": total_calls,
+        "step_variants_us_per_call": {
+            "fused (timed step: one launch, cache write + attention)": round(ms * 1e3 / total_calls, 3),
+            "fused with rotary embedding of q and k": round(ms_rope * 1e3 / total_calls, 3),
+            "separate launches (td_kv_append, td_decode_attn)": round(ms_separate * 1e3 / total_calls, 3),
+            "attention alone": round(us_attn, 3)},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
                      "kernel": kernel_label(td, w),
@@ -469,8 +497,8 @@ def run_e2e(td, args, w, case, kc, vc, C, R, sl_pre, sl_post, ws, dev, bytes_cal
                 qd.copy_(qh[i], non_blocking=True)
                 knd.copy_(knh[i], non_blocking=True)
                 vnd.copy_(vnh[i], non_blocking=True)
-                td.td_kv_append(knd, vnd, kc[c], vc[c], sl_pre, advance=False, stream=s)
-                td.td_decode_attn(qd, kc[c], vc[c], sl_post, case.scale, 0, out=outd, workspace=ws, stream=s)
+                td.td_rope_append_attn(qd[:, :, None], knd, vnd, kc[c], vc[c], sl_pre, case.scale, 0, advance=False,
+                                       out=outd[:, :, None], workspace=ws, stream=s)
                 outh[i].copy_(outd, non_blocking=True)
 
     one_step()
@@ -490,7 +518,7 @@ def run_e2e(td, args, w, case, kc, vc, C, R, sl_pre, sl_post, ws, dev, bytes_cal
     return {"value": round(world * steps * R * bytes_call / (ms * 1e-3) / 1e9, 1), "unit": "GB/s",
             "h2d_bytes_per_step": R * per_call_in, "d2h_bytes_per_step": R * outh[0].numel() * 2,
             "steps": steps, "us_per_call": round(ms * 1e3 / (steps * R), 3),
-            "path": "python binding td_kv_append + td_decode_attn, pinned host q/new rows in, out back"}
+            "path": "python binding td_rope_append_attn (one launch per call), pinned host q/new rows in, out back"}
 
 
 def cpu_baseline(case, w, L, seconds):

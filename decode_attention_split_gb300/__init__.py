@@ -18,6 +18,8 @@ from .api import (  # noqa: F401
     td_decode_workspace_bytes,
     td_kv_append,
     td_lse_merge,
+    td_rope_append_attn,
+    td_rope_kv_append,
     td_split_plan,
     td_verify_attn,
 )

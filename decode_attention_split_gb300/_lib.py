@@ -14,6 +14,8 @@ SYMBOLS = (
     "td_last_cuda_error",
     "td_decode_workspace_bytes",
     "td_split_plan",
+    "td_rope_kv_append",
+    "td_rope_append_attn",
     "td_kv_append",
     "td_decode_attn",
     "td_verify_attn",
@@ -45,6 +47,11 @@ def _declare(lib):
     lib.td_decode_workspace_bytes.restype = sz
     lib.td_split_plan.argtypes = [i, i, i, i, i, i, i, i, vp, vp, vp, vp]
     lib.td_split_plan.restype = i
+    lib.td_rope_kv_append.argtypes = [i, vp, vp, i, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, vp, vp]
+    lib.td_rope_kv_append.restype = i
+    lib.td_rope_append_attn.argtypes = [i, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, i, vp, vp, vp,
+                                        sz, vp, vp]
+    lib.td_rope_append_attn.restype = i
     lib.td_kv_append.argtypes = [i, vp, vp, vp, vp, vp, i, i, i, i, i, i, vp, vp]
     lib.td_kv_append.restype = i
     lib.td_decode_attn.argtypes = [i, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, vp, vp, sz, vp, vp]

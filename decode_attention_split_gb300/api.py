@@ -218,3 +218,88 @@ def td_lse_merge(m, l, acc, seq_lens, split: int, out_dtype=torch.float32, out=N
                                 _ptr(out), _ptr(lse), _stream(stream, dev))
     check("td_lse_merge", st)
     return (out, lse) if (return_lse or lse is not None) else out
+
+
+def _rope_tables(cos_t, sin_t, Smax, D, required):
+    if cos_t is None and sin_t is None and not required:
+        return None, None
+    if cos_t is None or sin_t is None:
+        raise ValueError("give both rope tables (cos and sin) or neither")
+    for t in (cos_t, sin_t):
+        if t.dtype != torch.float32 or t.dim() != 2 or t.shape[1] != D // 2 or t.shape[0] < Smax:
+            raise TypeError("rope tables must be float32 [>= Smax, D/2]")
+    return cos_t, sin_t
+
+
+def td_rope_kv_append(k_new, v_new, k_cache, v_cache, seq_lens, cos_t, sin_t, q=None, q_out=None,
+                      advance: bool = True, dev_status=None, stream=None):
+    """Rotate k_new [B,Hkv,T,D] to positions seq_lens[b]+t, write it and v_new into the caches;
+    with q [B,Hq,T,D], also return q rotated the same way (into q_out, which may be q)."""
+    dev = _cuda(k_new, v_new, k_cache, v_cache, seq_lens, cos_t, sin_t, q, q_out, dev_status)
+    B, Hkv, T, D = k_new.shape
+    Smax = k_cache.shape[2]
+    if v_new.shape != k_new.shape or k_cache.shape != (B, Hkv, Smax, D) or v_cache.shape != k_cache.shape:
+        raise ValueError("shape mismatch between new rows and caches")
+    if not (k_new.dtype == v_new.dtype == k_cache.dtype == v_cache.dtype):
+        raise TypeError("new rows and caches must share a dtype")
+    if seq_lens.dtype != torch.int32 or seq_lens.shape != (B,):
+        raise TypeError("seq_lens must be int32 [B]")
+    _rope_tables(cos_t, sin_t, Smax, D, required=True)
+    Hq = 0
+    if q is not None:
+        if q.dim() != 4 or q.shape[0] != B or q.shape[2:] != (T, D) or q.dtype != k_new.dtype:
+            raise ValueError("q must be [B, Hq, T, D] in the caches' dtype")
+        Hq = q.shape[1]
+        if q_out is None:
+            q_out = torch.empty_like(q)
+        if q_out.shape != q.shape or q_out.dtype != q.dtype:
+            raise TypeError("q_out must match q")
+    with torch.cuda.device(dev):
+        st = lib().td_rope_kv_append(_code(k_cache), _ptr(q), _ptr(q_out), Hq, _ptr(k_new), _ptr(v_new), _ptr(cos_t),
+                                     _ptr(sin_t), _ptr(k_cache), _ptr(v_cache), _ptr(seq_lens), B, Hkv, T, Smax, D,
+                                     int(bool(advance)), _ptr(dev_status), _stream(stream, dev))
+    check("td_rope_kv_append", st)
+    return q_out
+
+
+def td_rope_append_attn(q, k_new, v_new, k_cache, v_cache, seq_lens, scale: float | None = None, split: int = 0,
+                        cos_t=None, sin_t=None, advance: bool = True, out=None, lse=None, workspace=None,
+                        dev_status=None, stream=None, return_lse: bool = False):
+    """One layer's decode/verify step in one launch: q [B,Hq,T,D] and k_new [B,Hkv,T,D] rotated to
+    positions seq_lens[b]+t (when tables are given), k/v rows written into the caches, attention
+    over seq_lens[b]+T keys -> out [B,Hq,T,D] (+ lse [B,Hq,T]); seq_lens advanced if asked."""
+    if q.dim() != 4:
+        raise ValueError("q must be [B, Hq, T, D]")
+    dev = _cuda(q, k_new, v_new, k_cache, v_cache, seq_lens, cos_t, sin_t, out, lse, workspace, dev_status)
+    B, Hq, T, D = q.shape
+    _, Hkv, Smax, Dk = k_cache.shape
+    if k_new.shape != (B, Hkv, T, D) or v_new.shape != k_new.shape or Dk != D or v_cache.shape != k_cache.shape:
+        raise ValueError("q, new rows and cache shapes disagree")
+    if not (q.dtype == k_new.dtype == v_new.dtype == k_cache.dtype == v_cache.dtype):
+        raise TypeError("q, new rows and caches must share a dtype")
+    if seq_lens.dtype != torch.int32 or seq_lens.shape != (B,):
+        raise TypeError("seq_lens must be int32 [B]")
+    _rope_tables(cos_t, sin_t, Smax, D, required=False)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty(B, Hq, T, dtype=torch.float32, device=q.device)
+    if lse is not None and (lse.dtype != torch.float32 or lse.shape != (B, Hq, T)):
+        raise TypeError("lse must be float32 [B, Hq, T]")
+    if out.shape != q.shape or out.dtype != q.dtype:
+        raise TypeError("out must match q")
+    with torch.cuda.device(dev):
+        sp = _stream(stream, dev)
+        if workspace is None:
+            need = td_decode_workspace_bytes(B, Hq, Hkv, Smax, D, T, split)
+            workspace = _cached_workspace(need, dev, sp, (B, Hq, Hkv, Smax, D, T, split))
+        if workspace.dtype != torch.uint8:
+            raise TypeError("workspace must be a uint8 tensor")
+        st = lib().td_rope_append_attn(_code(q), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(cos_t), _ptr(sin_t),
+                                       _ptr(k_cache), _ptr(v_cache), _ptr(seq_lens), B, Hq, Hkv, T, Smax, D,
+                                       float(scale), int(split), int(bool(advance)), _ptr(out), _ptr(lse),
+                                       _ptr(workspace), workspace.numel(), _ptr(dev_status), sp)
+    check("td_rope_append_attn", st)
+    return (out, lse) if (return_lse or lse is not None) else out

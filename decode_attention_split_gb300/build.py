@@ -73,7 +73,8 @@ def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | N
         cmd = [nvcc(), *ARCH, "-shared", "-cudart", "static", "-Xlinker", "--exclude-libs=ALL", *objs, "-o", tmp_lib]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
-            os.unlink(tmp_lib)
+            if os.path.exists(tmp_lib):
+                os.unlink(tmp_lib)
             raise RuntimeError(f"link failed:\n{r.stderr}")
         os.replace(tmp_lib, LIB)
         with open(PTXAS_LOG, "w") as f:

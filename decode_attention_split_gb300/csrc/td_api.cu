@@ -18,45 +18,58 @@ bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0
 
 size_t elem_size(td_dtype d) { return d == TD_F32 ? 4 : 2; }
 
-td_status attn(td_dtype dtype, const void *q, const void *k_cache, const void *v_cache, const int32_t *seq_lens,
-               int B, int Hq, int Hkv, int T, int Smax, int D, float scale, int split, void *out, float *lse,
-               void *workspace, size_t workspace_bytes, uint32_t *dev_status, void *stream) {
+// Checks shared by the attention calls and fills the launch parameters; TD_OK or an error.
+td_status prepare(td_dtype dtype, const void *q, const void *k_cache, const void *v_cache, const int32_t *seq_lens,
+                  int B, int Hq, int Hkv, int T, int Smax, int D, float scale, int split, void *out, float *lse,
+                  void *workspace, size_t workspace_bytes, uint32_t *dev_status, td::SplitPlan *plan,
+                  td::SplitParams *p) {
   if (q == nullptr || k_cache == nullptr || v_cache == nullptr || seq_lens == nullptr || out == nullptr)
     return TD_ERR_INVALID_ARG;
   if (!isfinite(scale)) return TD_ERR_INVALID_ARG;
-  td::SplitPlan plan;
-  const td_status st = td::plan_split(dtype, B, Hq, Hkv, T, Smax, D, split, &plan);
+  const td_status st = td::plan_split(dtype, B, Hq, Hkv, T, Smax, D, split, plan);
   if (st == TD_ERR_CUDA) return cuda_fail(cudaGetLastError());
   if (st != TD_OK) return st;
   if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) || !aligned4(seq_lens) ||
       (lse != nullptr && !aligned4(lse)) || (dev_status != nullptr && !aligned4(dev_status)))
     return TD_ERR_UNSUPPORTED;
-  if (workspace == nullptr || workspace_bytes < plan.bytes || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+  if (workspace == nullptr || workspace_bytes < plan->bytes || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
     return TD_ERR_WORKSPACE;
   unsigned char *ws = static_cast<unsigned char *>(workspace);
+  *p = td::SplitParams{};
+  p->q = q;
+  p->k = k_cache;
+  p->v = v_cache;
+  p->seq_lens = seq_lens;
+  p->out = out;
+  p->lse = lse;
+  p->ws_part = reinterpret_cast<float *>(ws + plan->off_part);
+  p->counters = reinterpret_cast<int *>(ws);
+  p->status = dev_status;
+  p->B = B;
+  p->Hq = Hq;
+  p->Hkv = Hkv;
+  p->G = Hq / Hkv;
+  p->T = T;
+  p->Smax = Smax;
+  p->R = plan->R;
+  p->RB = plan->RB;
+  p->split = split;
+  p->ns_ws = plan->ns_ws;
+  p->p_target = plan->p_target;
+  p->min_chunk = plan->min_chunk;
+  p->qscale = scale * td::kLog2e;
+  p->done = p->counters + (size_t)B * Hkv * plan->RB;
+  return TD_OK;
+}
+
+td_status attn(td_dtype dtype, const void *q, const void *k_cache, const void *v_cache, const int32_t *seq_lens,
+               int B, int Hq, int Hkv, int T, int Smax, int D, float scale, int split, void *out, float *lse,
+               void *workspace, size_t workspace_bytes, uint32_t *dev_status, void *stream) {
+  td::SplitPlan plan;
   td::SplitParams p;
-  p.q = q;
-  p.k = k_cache;
-  p.v = v_cache;
-  p.seq_lens = seq_lens;
-  p.out = out;
-  p.lse = lse;
-  p.ws_part = reinterpret_cast<float *>(ws + plan.off_part);
-  p.counters = reinterpret_cast<int *>(ws);
-  p.status = dev_status;
-  p.B = B;
-  p.Hq = Hq;
-  p.Hkv = Hkv;
-  p.G = Hq / Hkv;
-  p.T = T;
-  p.Smax = Smax;
-  p.R = plan.R;
-  p.RB = plan.RB;
-  p.split = split;
-  p.ns_ws = plan.ns_ws;
-  p.p_target = plan.p_target;
-  p.min_chunk = plan.min_chunk;
-  p.qscale = scale * td::kLog2e;
+  const td_status st = prepare(dtype, q, k_cache, v_cache, seq_lens, B, Hq, Hkv, T, Smax, D, scale, split, out, lse,
+                               workspace, workspace_bytes, dev_status, &plan, &p);
+  if (st != TD_OK) return st;
   const cudaError_t e = td::launch_split(dtype, D, plan, p, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? TD_OK : cuda_fail(e);
 }
@@ -149,6 +162,54 @@ td_status td_lse_merge(const float *m, const float *l, const float *acc, const i
     return TD_ERR_UNSUPPORTED;
   const cudaError_t e = td::launch_merge(m, l, acc, seq_lens, B, rows, NS, D, split, out_dtype, out, lse,
                                          static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? TD_OK : cuda_fail(e);
+}
+
+}  // extern "C"
+
+extern "C" {
+
+td_status td_rope_kv_append(td_dtype dtype, const void *q, void *q_out, int Hq, const void *k_new, const void *v_new,
+                            const float *cos_t, const float *sin_t, void *k_cache, void *v_cache, int32_t *seq_lens,
+                            int B, int Hkv, int T, int Smax, int D, int advance, uint32_t *dev_status, void *stream) {
+  if (dtype != TD_F32 && dtype != TD_BF16) return TD_ERR_UNSUPPORTED;
+  if (k_new == nullptr || v_new == nullptr || k_cache == nullptr || v_cache == nullptr || seq_lens == nullptr ||
+      cos_t == nullptr || sin_t == nullptr || (q == nullptr) != (q_out == nullptr))
+    return TD_ERR_INVALID_ARG;
+  if (B < 1 || Hkv < 1 || T < 1 || Smax < 1 || D < 2 || (q != nullptr && Hq < 1)) return TD_ERR_INVALID_ARG;
+  // rows are rotated as pairs of 16-byte vectors (i, i + D/2)
+  if (B > 65535 || ((size_t)D * elem_size(dtype)) % 32 != 0) return TD_ERR_UNSUPPORTED;
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(cos_t) ||
+      !aligned16(sin_t) || !aligned4(seq_lens) || (q != nullptr && (!aligned16(q) || !aligned16(q_out))) ||
+      (dev_status != nullptr && !aligned4(dev_status)))
+    return TD_ERR_UNSUPPORTED;
+  const cudaError_t e = td::launch_rope_append(elem_size(dtype), q, q_out, Hq, k_new, v_new, cos_t, sin_t, k_cache,
+                                               v_cache, seq_lens, B, Hkv, T, Smax, D, advance, dev_status,
+                                               static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? TD_OK : cuda_fail(e);
+}
+
+td_status td_rope_append_attn(td_dtype dtype, const void *q, const void *k_new, const void *v_new, const float *cos_t,
+                              const float *sin_t, void *k_cache, void *v_cache, int32_t *seq_lens, int B, int Hq,
+                              int Hkv, int T, int Smax, int D, float scale, int split, int advance, void *out,
+                              float *lse, void *workspace, size_t workspace_bytes, uint32_t *dev_status,
+                              void *stream) {
+  if (k_new == nullptr || v_new == nullptr || (cos_t == nullptr) != (sin_t == nullptr)) return TD_ERR_INVALID_ARG;
+  if (dtype != TD_BF16) return TD_ERR_UNSUPPORTED;  // the tensor-core kernels carry the fused step
+  if (!aligned16(k_new) || !aligned16(v_new) || (cos_t != nullptr && (!aligned16(cos_t) || !aligned16(sin_t))))
+    return TD_ERR_UNSUPPORTED;
+  td::SplitPlan plan;
+  td::SplitParams p;
+  const td_status st = prepare(dtype, q, k_cache, v_cache, seq_lens, B, Hq, Hkv, T, Smax, D, scale, split, out, lse,
+                               workspace, workspace_bytes, dev_status, &plan, &p);
+  if (st != TD_OK) return st;
+  if (!plan.mma) return TD_ERR_UNSUPPORTED;
+  p.k_new = k_new;
+  p.v_new = v_new;
+  p.rope_cos = cos_t;
+  p.rope_sin = sin_t;
+  p.advance_lens = advance ? seq_lens : nullptr;
+  const cudaError_t e = td::launch_split(dtype, D, plan, p, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? TD_OK : cuda_fail(e);
 }
 

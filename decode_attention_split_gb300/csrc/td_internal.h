@@ -38,6 +38,11 @@ cudaError_t launch_append(size_t elem_bytes, const void *k_new, const void *v_ne
                           int32_t *seq_lens, int B, int Hkv, int T, int Smax, int D, int advance,
                           uint32_t *dev_status, cudaStream_t stream);
 
+cudaError_t launch_rope_append(size_t elem_bytes, const void *q, void *q_out, int Hq, const void *k_new,
+                               const void *v_new, const float *cos_t, const float *sin_t, void *k_cache,
+                               void *v_cache, int32_t *seq_lens, int B, int Hkv, int T, int Smax, int D, int advance,
+                               uint32_t *dev_status, cudaStream_t stream);
+
 // SM count of the current device (cached per device).
 int device_sm_count(int device);
 

@@ -69,7 +69,7 @@ extern "C" td_status td_decode_attn_noalloc(td_dtype dtype, const void *q, const
   // partial results where this layout keeps its counters
   if (cudaMemsetAsync(scratch, 0, plan.off_part, s) != cudaSuccess) return TD_ERR_CUDA;
   unsigned char *ws = static_cast<unsigned char *>(scratch);
-  td::SplitParams p;
+  td::SplitParams p = {};
   p.q = q;
   p.k = k_cache;
   p.v = v_cache;

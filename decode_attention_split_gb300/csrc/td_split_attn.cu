@@ -287,7 +287,8 @@ td_status plan_split(td_dtype dtype, int B, int Hq, int Hkv, int T, int Smax, in
       }
     }
   }
-  const size_t counters = align256((size_t)B * U * sizeof(int));
+  // completion counters, one per (b, kv head, row block), then the fused step's read count
+  const size_t counters = align256(((size_t)B * U + 1) * sizeof(int));
   plan->off_part = counters;
   plan->bytes = plan->off_part + align256((size_t)B * U * ns * part_block_floats(R, D) * sizeof(float));
   return TD_OK;

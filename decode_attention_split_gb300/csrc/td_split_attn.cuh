@@ -53,7 +53,33 @@ struct SplitParams {
   int p_target;         // CTAs the automatic chunk size aims to fill
   int min_chunk;        // smallest automatic chunk (keys)
   float qscale;         // scale * log2(e)
+  // Fused step (tensor-core kernels only; k_new == null for plain attention): the T new rows
+  // of each (b, kv head) go to cache rows seq_lens[b] .. seq_lens[b]+T-1 in this launch, the
+  // query and key rows rotated there first when rope tables are given, and every query row
+  // attends over seq_lens[b] + T keys.
+  const void *k_new;    // [B, Hkv, T, D]
+  const void *v_new;
+  const float *rope_cos;   // [Smax, D/2], or null: no rotation
+  const float *rope_sin;
+  int32_t *advance_lens;   // the seq_lens array, to advance by T once every CTA has read it; or null
+  int *done;               // grid-wide count of CTAs that have read the lengths (workspace, zero)
 };
+
+// Attended length of a sequence whose stored length is `raw`, with the status bits its
+// reading raises. Plain attention: raw clamped into [0, Smax]. Fused step: raw + T, or 0
+// (nothing attended, nothing written) when the new rows do not fit.
+__device__ __forceinline__ int attended_len(const SplitParams &p, int32_t raw, uint32_t &bits) {
+  if (p.k_new != nullptr) {
+    const bool fits = raw >= 0 && (long long)raw + p.T <= p.Smax;
+    if (!fits) bits |= TD_DEV_APPEND_OVERFLOW;
+    return fits ? raw + p.T : 0;
+  }
+  const int L = raw < 0 ? 0 : (raw > p.Smax ? p.Smax : raw);
+  if (raw < 0) bits |= TD_DEV_NEGATIVE_SEQLEN;
+  if (raw > p.Smax) bits |= TD_DEV_SEQLEN_CLAMPED;
+  if (p.T > 1 && L < p.T) bits |= TD_DEV_VERIFY_SHORT;
+  return L;
+}
 
 // A chunk's partial result for its row block: acc[R][D] (unnormalised p @ V sums), then
 // m[R] (natural-log units) and l[R]; padded to whole 16-byte units so blocks can be
@@ -97,8 +123,6 @@ struct SplitCfg {
   static constexpr bool kFits = SMEM_BYTES + 8448 <= 227 * 1024;
 };
 
-__device__ __forceinline__ int clamp_len(int32_t L, int Smax) { return L < 0 ? 0 : (L > Smax ? Smax : L); }
-
 // Exclusive prefix over the per-sequence item counts, computed by the whole CTA.
 // s_len[b] receives the clamped length; returns the chunk size through *s_chunk and the
 // item total in s_prefix[B]. s_red holds 2 * kWarps values.
@@ -114,11 +138,7 @@ static __device__ void plan_items(const SplitParams &p, int *s_len, int *s_prefi
   for (int i = 0; i < kSeg; ++i) {
     const int b = b0 + i;
     if (b < p.B) {
-      const int32_t raw = p.seq_lens[b];
-      const int L = clamp_len(raw, p.Smax);
-      if (raw < 0) bits |= TD_DEV_NEGATIVE_SEQLEN;
-      if (raw > p.Smax) bits |= TD_DEV_SEQLEN_CLAMPED;
-      if (p.T > 1 && L < p.T) bits |= TD_DEV_VERIFY_SHORT;
+      const int L = attended_len(p, p.seq_lens[b], bits);
       s_len[b] = L;
       tot += L;
       lmax = max(lmax, L);
@@ -206,6 +226,26 @@ static __device__ void plan_items(const SplitParams &p, int *s_len, int *s_prefi
     break;
   }
   __syncthreads();
+}
+
+// Fused step with advance: the last CTA of the grid to have read the lengths moves every
+// sequence that took its new rows forward by T. Every CTA calls this once, after its last
+// read of seq_lens; the count lives in the workspace and is left zero again.
+static __device__ void advance_after_reads(const SplitParams &p, int *s_flag) {
+  if (p.advance_lens == nullptr) return;
+  if (threadIdx.x == 0) {
+    const int prev = ticket_acq_rel(p.done);
+    if (prev < 0 || prev >= (int)gridDim.x) report(p.status, TD_DEV_WORKSPACE_DIRTY);
+    *s_flag = prev == (int)gridDim.x - 1;
+  }
+  __syncthreads();
+  if (*s_flag) {
+    for (int b = threadIdx.x; b < p.B; b += kThreads) {
+      const int32_t raw = p.advance_lens[b];
+      if (raw >= 0 && (long long)raw + p.T <= p.Smax) p.advance_lens[b] = raw + p.T;
+    }
+    if (threadIdx.x == 0) *p.done = 0;
+  }
 }
 
 // Shared memory (floats) the fused merge needs besides the staged partial blocks.

@@ -3,15 +3,14 @@
 // Same method as split_attn_mma_kernel ("tinydecode", section "how the decode step is put
 // together"; "llm-decode-cuda", split-KV attention section): the keys of one
 // (sequence b, kv head, row block) group are cut into chunks whose partial softmax results
-// are merged by log-sum-exp. Here a group is one cluster of CS CTAs (one per SM, deeper
-// rings than the persistent kernel): CTA `rank` streams chunk `rank`, combines its warps'
-// partials into one block in its own shared memory, and after a cluster barrier CTA 0 reads
-// the CS blocks through distributed shared memory and writes out and lse. No workspace, no
-// atomics, no second pass over L2; a second cluster barrier keeps every CTA's shared memory
-// alive until CTA 0 has read it.
+// are merged by log-sum-exp. Here a group is one cluster of CS CTAs: CTA `rank` streams
+// chunk `rank`, combines its warps' partials into one block in its own shared memory, and
+// after a cluster barrier CTA 0 reads the CS blocks through distributed shared memory and
+// writes out and lse. No partials in global memory, no atomics, no second pass over L2; a
+// second cluster barrier keeps every CTA's shared memory alive until CTA 0 has read it.
 //
-// Used when the groups fit the GPU in one wave of clusters (few sequences, e.g. batch 1):
-// the grid is groups x CS CTAs, fixed by the arguments.
+// Used when the groups fill the GPU in one wave of clusters at about two CTAs per SM
+// (batches of a few sequences); the grid is groups x CS CTAs, fixed by the arguments.
 #pragma once
 
 #include "td_split_mma.cuh"
@@ -66,6 +65,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_attn_cluster_kernel(const _
   __shared__ __align__(8) uint64_t s_bars[NST];
   __shared__ float s_w[kMaxCluster][kMmaRows];  // CTA 0: merge weight of each block's rows
   __shared__ float s_lse[kMmaRows];
+  __shared__ int s_flag;
 
   const int tid = threadIdx.x;
   unsigned char *smem = align1024(smem_raw);
@@ -84,16 +84,11 @@ __global__ void __launch_bounds__(kThreads, 1) split_attn_cluster_kernel(const _
   }
   griddep_wait();  // seq_lens and the cache may come from the previous kernel in the stream
   griddep_launch_dependents();
-  const int32_t raw = p.seq_lens[b];
-  const int L = clamp_len(raw, p.Smax);
-  if (tid == 0 && rank == 0 && kvh == 0 && rb == 0) {
-    uint32_t bits = 0;
-    if (raw < 0) bits |= TD_DEV_NEGATIVE_SEQLEN;
-    if (raw > p.Smax) bits |= TD_DEV_SEQLEN_CLAMPED;
-    if (p.T > 1 && L < p.T) bits |= TD_DEV_VERIFY_SHORT;
-    report(p.status, bits);
-  }
+  uint32_t bits = 0;
+  const int L = attended_len(p, p.seq_lens[b], bits);
+  if (tid == 0 && rank == 0 && kvh == 0 && rb == 0) report(p.status, bits);
   __syncthreads();  // barrier initialisation is visible before any wait
+  advance_after_reads(p, &s_flag);  // fused step: the lengths move on once every CTA has read them
   // chunk of this CTA: whole 64-key stages, the group's keys spread over the cluster
   const int S = ((L + CS - 1) / CS + C::TK - 1) / C::TK * C::TK;
   const int c0 = min((int)rank * S, L);

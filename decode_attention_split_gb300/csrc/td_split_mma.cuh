@@ -28,6 +28,7 @@
 #include <cudaTypedefs.h>
 
 #include "td_mma.cuh"
+#include "td_rope.cuh"
 #include "td_split_attn.cuh"
 
 namespace td {
@@ -92,6 +93,60 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
       : "memory");
 }
 
+// Fused step: cache rows [L - T, L) of (b, kvh) are this launch's new rows, whose copies in
+// global memory are not written yet (or are being written). Where they fall inside the
+// stage that holds rows [j0, j0 + valid), they are placed into the landed K/V tiles at
+// `stage` from k_new / v_new, the keys rotated to their positions when rope tables are given;
+// the CTAs of row block 0 also write them to the cache (each new row lies in exactly one
+// chunk, so exactly one CTA writes it). Every thread that writes shared memory fences it
+// against the TMA unit's next refill of the stage.
+template <int D, int NST>
+__device__ void place_new_rows(const SplitParams &p, unsigned char *stage, int b, int kvh, int rb, int L, int j0,
+                               int valid) {
+  using C = MmaCfg<D, NST>;
+  constexpr int NH = C::NCH / 2;
+  const int n0 = max(L - p.T, j0), n1 = min(L, j0 + valid);
+  if (n0 >= n1) return;
+  const bool rope = p.rope_cos != nullptr;
+  const int kitems = rope ? NH : C::NCH;  // key work items per row (vector pairs or vectors)
+  const int per_row = kitems + C::NCH;
+  const size_t hb = (size_t)b * p.Hkv + kvh;
+  const uint4 *kn = static_cast<const uint4 *>(p.k_new) + hb * p.T * C::NCH;
+  const uint4 *vn = static_cast<const uint4 *>(p.v_new) + hb * p.T * C::NCH;
+  // the caches are written only in the fused step, whose caller passes them writable
+  uint4 *kc = static_cast<uint4 *>(const_cast<void *>(p.k)) + hb * p.Smax * C::NCH;
+  uint4 *vc = static_cast<uint4 *>(const_cast<void *>(p.v)) + hb * p.Smax * C::NCH;
+  unsigned char *ktile = stage, *vtile = stage + C::TILE_BYTES;
+  const bool writer = rb == 0;
+  for (int idx = threadIdx.x; idx < (n1 - n0) * per_row; idx += kThreads) {
+    const int j = n0 + idx / per_row, it = idx % per_row;
+    const int t = j - (L - p.T), srow = j - j0;
+    if (it < kitems) {
+      if (rope) {
+        uint4 lo = kn[(size_t)t * C::NCH + it], hi = kn[(size_t)t * C::NCH + it + NH];
+        const size_t tab = (size_t)j * (D / 2) + it * 8;
+        rope_vec16<__nv_bfloat16>(lo, hi, p.rope_cos + tab, p.rope_sin + tab);
+        *reinterpret_cast<uint4 *>(ktile + tma_swz<C::TK>(srow, it)) = lo;
+        *reinterpret_cast<uint4 *>(ktile + tma_swz<C::TK>(srow, it + NH)) = hi;
+        if (writer) {
+          kc[(size_t)j * C::NCH + it] = lo;
+          kc[(size_t)j * C::NCH + it + NH] = hi;
+        }
+      } else {
+        const uint4 x = kn[(size_t)t * C::NCH + it];
+        *reinterpret_cast<uint4 *>(ktile + tma_swz<C::TK>(srow, it)) = x;
+        if (writer) kc[(size_t)j * C::NCH + it] = x;
+      }
+    } else {
+      const int ch = it - kitems;
+      const uint4 x = vn[(size_t)t * C::NCH + ch];
+      *reinterpret_cast<uint4 *>(vtile + tma_swz<C::TK>(srow, ch)) = x;
+      if (writer) vc[(size_t)j * C::NCH + ch] = x;
+    }
+  }
+  fence_proxy_async_smem();
+}
+
 // Streams keys [c0, c1) of kv head kvh of sequence b (attended length L) for the query rows
 // of row block rb through the ring at `smem` (1024-byte aligned; NST stages with barriers
 // s_bars; `seq` counts the stages this CTA has consumed, for the barrier parities) and leaves
@@ -131,15 +186,37 @@ __device__ bool stream_chunk(const MmaArgs &a, unsigned char *smem, uint64_t *s_
   // the query rows of this row block go to the K tile of the ring buffer the first stage
   // refills last; they are read into registers before that buffer is refilled
   const uint32_t qtile = sbase + ((seq + NST - 1) % NST) * C::STAGE_BYTES;
-  for (int idx = tid; idx < kMmaRows * C::NCH; idx += kThreads) {
-    const int r = idx / C::NCH, ch = idx % C::NCH;
-    const int gr = rb * p.R + r;
-    const bool valid = r < p.R && gr < GT;
-    const int hq = kvh * p.G + (valid ? gr / p.T : 0);
-    const int t = valid ? gr % p.T : 0;
-    const unsigned char *qrow =
-        static_cast<const unsigned char *>(p.q) + (((size_t)b * p.Hq + hq) * p.T + t) * C::ROWB;
-    cp_async_16(qtile + swz<C::ROWB>(r, ch), qrow + ch * 16, valid ? 16u : 0u);
+  if (p.rope_cos == nullptr) {
+    for (int idx = tid; idx < kMmaRows * C::NCH; idx += kThreads) {
+      const int r = idx / C::NCH, ch = idx % C::NCH;
+      const int gr = rb * p.R + r;
+      const bool valid = r < p.R && gr < GT;
+      const int hq = kvh * p.G + (valid ? gr / p.T : 0);
+      const int t = valid ? gr % p.T : 0;
+      const unsigned char *qrow =
+          static_cast<const unsigned char *>(p.q) + (((size_t)b * p.Hq + hq) * p.T + t) * C::ROWB;
+      cp_async_16(qtile + swz<C::ROWB>(r, ch), qrow + ch * 16, valid ? 16u : 0u);
+    }
+  } else {
+    // fused step: query row (hq, t) rotated to its position L - T + t on the way in
+    constexpr int NH = C::NCH / 2;
+    unsigned char *qt = smem + ((seq + NST - 1) % NST) * C::STAGE_BYTES;
+    for (int idx = tid; idx < kMmaRows * NH; idx += kThreads) {
+      const int r = idx / NH, ch = idx % NH;
+      const int gr = rb * p.R + r;
+      uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = lo;
+      if (r < p.R && gr < GT) {
+        const int hq = kvh * p.G + gr / p.T, t = gr % p.T;
+        const uint4 *qrow = static_cast<const uint4 *>(p.q) + (((size_t)b * p.Hq + hq) * p.T + t) * C::NCH;
+        lo = qrow[ch];
+        hi = qrow[ch + NH];
+        const size_t tab = (size_t)(L - p.T + t) * (D / 2) + ch * 8;
+        rope_vec16<__nv_bfloat16>(lo, hi, p.rope_cos + tab, p.rope_sin + tab);
+      }
+      *reinterpret_cast<uint4 *>(qt + swz<C::ROWB>(r, ch)) = lo;
+      *reinterpret_cast<uint4 *>(qt + swz<C::ROWB>(r, ch + NH)) = hi;
+    }
+    fence_proxy_async_smem();  // these writes precede the buffer's refill by the TMA unit
   }
   cp_async_commit();
   if (tid == 0) {
@@ -181,6 +258,7 @@ __device__ bool stream_chunk(const MmaArgs &a, unsigned char *smem, uint64_t *s_
       }
       fence_proxy_async_smem();  // these writes precede the buffer's next refill by the TMA unit
     }
+    if (landed && p.k_new != nullptr) place_new_rows<D, NST>(p, smem + buf * C::STAGE_BYTES, b, kvh, rb, L, j0, valid);
     if (st == 0) cp_async_wait<0>();  // this thread's part of the query tile
     // one decision for the whole CTA: a thread whose wait gave up stops every thread
     if (!__syncthreads_and(landed)) {
@@ -339,6 +417,7 @@ __global__ void __launch_bounds__(kThreads, 2) split_attn_mma_kernel(const __gri
   griddep_wait();  // inputs may come from the previous kernel in the stream
   griddep_launch_dependents();
   plan_items(p, s_len, s_prefix, &s_chunk, s_red);  // ends with __syncthreads
+  advance_after_reads(p, &s_last);  // fused step: the lengths move on once every CTA has read them
   const int S = s_chunk;
   const int W = s_prefix[p.B];
   const int rows = p.Hq * p.T;

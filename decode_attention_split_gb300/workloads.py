@@ -11,6 +11,7 @@ sharing any of the method. Everything is drawn on the CPU from
     then the new key/value rows (workloads that append),
 
 and cast to the storage dtype last (bf16: round to nearest even, torch's cast).
+``rope_tables`` gives the rotary-embedding cos/sin tables (an input, like a weight).
 
 Workloads (shapes from the pages' models; the data is synthetic, no weights are used):
 
@@ -165,3 +166,12 @@ def to_numpy(t: torch.Tensor):
     if t.dtype == torch.bfloat16:
         return t.view(torch.int16).numpy().view("uint16")
     return t.numpy()
+
+
+def rope_tables(positions: int, D: int, base: float = 500000.0):
+    """Rotary-embedding input tables (cos, sin), fp32 [positions, D/2], of the angles
+    p * base^(-2i/D) (the llama frequency ladder; 500000 is Llama 3's base). They are an
+    input of the rotation like any weight, computed here in fp64 and stored fp32."""
+    inv = base ** (-torch.arange(0, D, 2, dtype=torch.float64) / D)
+    ang = torch.arange(positions, dtype=torch.float64)[:, None] * inv[None, :]
+    return torch.cos(ang).to(torch.float32), torch.sin(ang).to(torch.float32)

@@ -19,6 +19,11 @@
  *                  themselves ("tinydecode", "speculative decoding": the verify pass over
  *                  k+1 tokens with the head group folded so the cache is read once).
  *   td_lse_merge   the log-sum-exp merge of per-split partials on its own.
+ *   td_rope_kv_append    the cache write with the new keys (and optionally the queries)
+ *                  rotated to their positions first ("llm-decode-cuda" fuses "RoPE +
+ *                  KV-cache write" in its decode step; "tinydecode" lists an in-place rope).
+ *   td_rope_append_attn  the whole decode or verify step of one layer in one launch:
+ *                  rotation, cache write and split attention.
  *
  * Layouts (row-major, contiguous, element type given by td_dtype):
  *   q, out         [B, Hq, D] for decode; [B, Hq, T, D] for verify
@@ -156,6 +161,47 @@ td_status td_verify_attn(td_dtype dtype, const void *q, const void *k_cache, con
  */
 td_status td_lse_merge(const float *m, const float *l, const float *acc, const int32_t *seq_lens, int B, int rows,
                        int NS, int D, int split, td_dtype out_dtype, void *out, float *lse, void *stream);
+
+/*
+ * Rotary position embedding: the pages name the kernel but print no formula; the layout of
+ * the llama checkpoints is used. For i < D/2 the pair (x[i], x[i + D/2]) of a row at position
+ * P turns by the angle whose cosine and sine are cos_t[P * D/2 + i] and sin_t[P * D/2 + i]:
+ *   y[i] = x[i] cos - x[i + D/2] sin,   y[i + D/2] = x[i + D/2] cos + x[i] sin,
+ * in fp32, rounded to nearest even into the element type. cos_t, sin_t: fp32 [Smax, D/2]
+ * device tables (any angles: the caller chooses the frequencies and any scaling).
+ */
+
+/*
+ * RoPE + cache append. For each b with 0 <= L = seq_lens[b] and L + T <= Smax, token t sits
+ * at position L + t:
+ *   k_cache[b, h, L+t, :] = rope(k_new[b, h, t, :], L+t),  v_cache[b, h, L+t, :] = v_new[b, h, t, :],
+ *   q_out[b, hq, t, :]    = rope(q[b, hq, t, :], L+t)     (when q is given; q_out may be q),
+ * then seq_lens[b] += T if advance (same launch, after the read). A sequence that does not
+ * fit is left untouched (its q_out rows too) and sets TD_DEV_APPEND_OVERFLOW.
+ * q, q_out: [B, Hq, T, D] or both NULL; k_new, v_new [B, Hkv, T, D]; caches [B, Hkv, Smax, D].
+ * D * element size must be a multiple of 32 bytes; tables and row pointers 16-byte aligned.
+ */
+td_status td_rope_kv_append(td_dtype dtype, const void *q, void *q_out, int Hq, const void *k_new, const void *v_new,
+                            const float *cos_t, const float *sin_t, void *k_cache, void *v_cache, int32_t *seq_lens,
+                            int B, int Hkv, int T, int Smax, int D, int advance, uint32_t *dev_status, void *stream);
+
+/*
+ * One layer's decode (T = 1) or verify (T > 1) step in one launch: for every b whose new rows
+ * fit (0 <= L = seq_lens[b], L + T <= Smax), the result of
+ *   td_rope_kv_append(q -> rotated q, k_new, v_new at L .. L+T-1)   (no rotation if cos_t is NULL)
+ *   td_verify_attn(rotated q, caches, lengths L + T)
+ * with out/lse as td_verify_attn defines them, and seq_lens[b] = L + T afterwards if advance.
+ * The new rows reach the attention without a round trip through memory, the cache rows are
+ * written in the same launch, and the lengths are advanced once every CTA has read them.
+ * A sequence whose rows do not fit is left untouched, gives out = 0 and lse = -inf, and sets
+ * TD_DEV_APPEND_OVERFLOW. bf16 only (TD_ERR_UNSUPPORTED otherwise), D 64 or 128.
+ * q, out [B, Hq, T, D]; lse [B, Hq, T] (nullable); workspace as td_decode_workspace_bytes(q_len = T).
+ */
+td_status td_rope_append_attn(td_dtype dtype, const void *q, const void *k_new, const void *v_new, const float *cos_t,
+                              const float *sin_t, void *k_cache, void *v_cache, int32_t *seq_lens, int B, int Hq,
+                              int Hkv, int T, int Smax, int D, float scale, int split, int advance, void *out,
+                              float *lse, void *workspace, size_t workspace_bytes, uint32_t *dev_status,
+                              void *stream);
 
 /*
  * Decode attention without a workspace argument: the same computation and arguments as
