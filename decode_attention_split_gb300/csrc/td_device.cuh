@@ -83,6 +83,20 @@ __device__ __forceinline__ uint64_t l2_evict_first_policy() {
   return pol;
 }
 
+// Warms L2 with `bytes` (a multiple of 16) from a 16-byte aligned global address. A hint:
+// nothing waits for it.
+__device__ __forceinline__ void prefetch_l2_bulk(const void *src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
+// A load that may race with another grid's store to the same word (the value is only used
+// as a guess).
+__device__ __forceinline__ int32_t ld_relaxed(const int32_t *p) {
+  int32_t v;
+  asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
 // One bulk copy global -> shared through the TMA engine; completion is counted on `bar`
 // in bytes. dst, src and bytes must be multiples of 16.
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar,

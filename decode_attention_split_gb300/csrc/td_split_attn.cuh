@@ -123,6 +123,21 @@ struct SplitCfg {
   static constexpr bool kFits = SMEM_BYTES + 8448 <= 227 * 1024;
 };
 
+// Chunk size before the overshoot check of plan_items: the caller's split, or keys per item
+// so the items fill the grid once; then every sequence has at most ceil(p_target / U) chunks,
+// which is what the workspace holds (the guard on `longest` only restates that bound).
+__device__ __forceinline__ int first_chunk_size(const SplitParams &p, long long all, int longest) {
+  if (p.split > 0) return p.split;
+  const int U = p.Hkv * p.RB;
+  long long want = (all * U + p.p_target - 1) / p.p_target;
+  want = (want + 15) / 16 * 16;
+  if (want < p.min_chunk) want = p.min_chunk;
+  const long long fits = ((long long)longest + p.ns_ws - 1) / p.ns_ws;
+  if (want < fits) want = fits;
+  int S = (int)(want > p.Smax ? p.Smax : want);
+  return S < 1 ? 1 : S;
+}
+
 // Exclusive prefix over the per-sequence item counts, computed by the whole CTA.
 // s_len[b] receives the clamped length; returns the chunk size through *s_chunk and the
 // item total in s_prefix[B]. s_red holds 2 * kWarps values.
@@ -162,21 +177,7 @@ static __device__ void plan_items(const SplitParams &p, int *s_len, int *s_prefi
     all += s_red[w];
     longest = max(longest, (int)s_red[kWarps + w]);
   }
-  int S;  // the same value in every thread
-  if (p.split > 0) {
-    S = p.split;
-  } else {
-    // keys per item so the items fill the grid once; then every sequence has at most
-    // ceil(p_target / U) chunks, which is what the workspace holds (the guard below only
-    // restates that bound)
-    long long want = (all * U + p.p_target - 1) / p.p_target;
-    want = (want + 15) / 16 * 16;
-    if (want < p.min_chunk) want = p.min_chunk;
-    const long long fits = ((long long)longest + p.ns_ws - 1) / p.ns_ws;
-    if (want < fits) want = fits;
-    S = (int)(want > p.Smax ? p.Smax : want);
-    if (S < 1) S = 1;
-  }
+  int S = first_chunk_size(p, all, longest);  // the same value in every thread
   // Per-thread segment sums of items, then a CTA-wide exclusive scan. With an automatic
   // chunk size, rounding each sequence's chunk count up can push the items past the grid,
   // leaving a second, mostly idle wave: then S grows, by the overshoot and by at least enough

@@ -82,6 +82,15 @@ __global__ void __launch_bounds__(kThreads, 1) split_attn_cluster_kernel(const _
     for (int i = 0; i < NST; ++i) mbar_init(smem_u32(&s_bars[i]), 1);
     fence_mbar_init();
   }
+  if (tid == 0) {
+    // a guess of this CTA's chunk from the length as it reads before the wait (see
+    // prefetch_first_item): warm L2 with its first stages
+    uint32_t guess_bits = 0;
+    const int Lg = attended_len(p, ld_relaxed(p.seq_lens + b), guess_bits);
+    const int Sg = ((Lg + CS - 1) / CS + C::TK - 1) / C::TK * C::TK;
+    const int g0 = min((int)rank * Sg, Lg);
+    prefetch_chunk_l2<D>(p, b, kvh, g0, min(g0 + Sg, Lg), prefetch_stages(p));
+  }
   griddep_wait();  // seq_lens and the cache may come from the previous kernel in the stream
   griddep_launch_dependents();
   uint32_t bits = 0;

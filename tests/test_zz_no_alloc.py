@@ -49,18 +49,18 @@ def test_noalloc_matches_workspace_entry_point_twice():
 
 
 def test_noalloc_rejects_shapes_beyond_its_scratch():
-    """A batch of 8 sequences of 8192 rows needs more than the 4 MiB array: refused before launch."""
+    """A batch of 16 sequences of 8192 rows needs more than the 4 MiB array: refused before launch."""
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     from decode_attention_split_gb300 import _lib, build
     build.build()
     import decode_attention_split_gb300 as td
     lib = _lib.lib()
-    assert td.td_decode_workspace_bytes(8, 32, 8, 8192, 128) > 4 << 20
-    q = torch.zeros(8, 32, 128, dtype=torch.bfloat16, device="cuda")
-    kc = torch.zeros(8, 8, 8192, 128, dtype=torch.bfloat16, device="cuda")
-    sl = torch.full((8,), 8192, dtype=torch.int32, device="cuda")
+    assert td.td_decode_workspace_bytes(16, 32, 8, 8192, 128) > 4 << 20
+    q = torch.zeros(16, 32, 128, dtype=torch.bfloat16, device="cuda")
+    kc = torch.zeros(16, 8, 8192, 128, dtype=torch.bfloat16, device="cuda")
+    sl = torch.full((16,), 8192, dtype=torch.int32, device="cuda")
     out = torch.empty_like(q)
-    lse = torch.empty(8, 32, dtype=torch.float32, device="cuda")
+    lse = torch.empty(16, 32, dtype=torch.float32, device="cuda")
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     assert _noalloc(lib, q, kc, kc, sl, 0.1, out, lse, status) == 3  # TD_ERR_WORKSPACE
