@@ -346,17 +346,12 @@ def run_td(args, world, rank, local):
             td.td_decode_attn(q[i], kc[c], vc[c], sl_post, case.scale, 0, out=out[i], workspace=ws, stream=s)
 
     if args.profile_launches:
+        # the timed step's call, launched plainly (no graph): W warm-up calls, then the ones to profile
         with torch.cuda.stream(s):
-            for _ in range(args.warmup):
-                td.td_decode_attn(q[0], kc[0], vc[0], sl_post, case.scale, 0, out=out[0], workspace=ws, stream=s)
-            for i in range(args.profile_launches):
+            for i in range(args.warmup + args.profile_launches):
                 c = i % C
-                td.td_kv_append(kn[i], vn[i], kc[c], vc[c], sl_pre, advance=False, stream=s)
-                td.td_decode_attn(q[i], kc[c], vc[c], sl_post, case.scale, 0, out=out[i], workspace=ws, stream=s)
-            for i in range(args.profile_launches):
-                c = i % C
-                td.td_rope_append_attn(q[i][:, :, None], kn[i], vn[i], kc[c], vc[c], sl_pre, case.scale, 0,
-                                       advance=False, out=out[i][:, :, None], workspace=ws, stream=s)
+                td.td_rope_append_attn(q[i % R][:, :, None], kn[i % R], vn[i % R], kc[c], vc[c], sl_pre, case.scale,
+                                       0, advance=False, out=out[i % R][:, :, None], workspace=ws, stream=s)
         s.synchronize()
         print(json.dumps({"profile_launches": args.profile_launches, "ok": True}))
         return
