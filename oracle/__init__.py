@@ -4,7 +4,8 @@ TEST INFRASTRUCTURE. Only the test suite, ``__graft_entry__.smoke()`` and the
 benchmark's CPU-baseline leg import this package. The product (the CUDA library and
 its Python binding) never imports it, and it never imports the product: the two share
 no code. The arithmetic lives in ``attention.c`` (plain C, fp64, OpenMP over rows);
-this module compiles it with gcc and marshals numpy arrays to it.
+this module compiles it (and ``speculative.c``, the accept/reject step that follows a verify
+pass) with gcc and marshals numpy arrays to it.
 
 Arrays are numpy: float32 or float64 values, or uint16 holding bf16 bit patterns (the
 oracle widens them exactly). Layouts are the library's: q/out [B, Hq, T, D], caches
@@ -25,7 +26,7 @@ import threading
 import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-_SRC = os.path.join(_HERE, "attention.c")
+_SRCS = [os.path.join(_HERE, "attention.c"), os.path.join(_HERE, "speculative.c")]
 _BUILD = os.path.join(_HERE, "_build")
 
 # status bits reported for data errors (the CUDA library uses the same meanings)
@@ -33,6 +34,7 @@ SEQLEN_CLAMPED = 1
 APPEND_OVERFLOW = 2
 VERIFY_SHORT = 4
 NEGATIVE_SEQLEN = 8
+BAD_TOKEN = 64
 
 _DTYPE_CODE = {np.dtype(np.float32): 0, np.dtype(np.uint16): 1, np.dtype(np.float64): 2}
 _lock = threading.Lock()
@@ -46,12 +48,12 @@ def build(mutant: int = 0, force: bool = False) -> str:
     shows the oracle's pins catch such mistakes)."""
     name = "liboracle.so" if mutant == 0 else f"liboracle_mut{mutant}.so"
     out = os.path.join(_BUILD, name)
-    if not force and os.path.exists(out) and os.path.getmtime(out) >= os.path.getmtime(_SRC):
+    if not force and os.path.exists(out) and all(os.path.getmtime(out) >= os.path.getmtime(p) for p in _SRCS):
         return out
     os.makedirs(_BUILD, exist_ok=True)
     fd, tmp = tempfile.mkstemp(suffix=".so", dir=_BUILD)
     os.close(fd)
-    base = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", f"-DORC_MUTANT={int(mutant)}", _SRC, "-o", tmp, "-lm"]
+    base = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", f"-DORC_MUTANT={int(mutant)}", *_SRCS, "-o", tmp, "-lm"]
     try:
         r = subprocess.run(base[:1] + ["-fopenmp"] + base[1:], capture_output=True, text=True)
         if r.returncode != 0:  # a compiler without OpenMP still builds the serial oracle
@@ -98,6 +100,8 @@ class Oracle:
         lib.orc_kv_append.restype = ctypes.c_uint
         lib.orc_rope.argtypes = [i, vp, ctypes.c_int64, i, vp, vp, vp, vp]
         lib.orc_rope.restype = None
+        lib.orc_spec_accept.argtypes = [vp, vp, vp, vp, i, i, i, d, vp, vp]
+        lib.orc_spec_accept.restype = ctypes.c_uint
         lib.orc_num_threads.restype = i
         lib.orc_mutant.restype = i
         self.lib = lib
@@ -220,3 +224,29 @@ class Oracle:
         if advance:
             seq_lens[...] = work
         return out, lse, int(status)
+
+    def spec_accept(self, target_logits, draft_logits, draft_tokens, uniforms, temperature: float):
+        """Speculative accept/reject (Leviathan et al. Algorithm 1; greedy at temperature 0).
+
+        target_logits float32 [B, G+1, V], draft_logits float32 [B, G, V] (None when greedy),
+        draft_tokens int32 [B, G], uniforms float64 [B, G+1] in [0, 1) (None when greedy).
+        Returns (n_accepted int32 [B], next_token int32 [B], status bits)."""
+        target_logits = np.ascontiguousarray(target_logits, dtype=np.float32)
+        B, G1, V = target_logits.shape
+        G = G1 - 1
+        draft_tokens = np.ascontiguousarray(draft_tokens, dtype=np.int32).reshape(B, G)
+        if draft_logits is not None:
+            draft_logits = np.ascontiguousarray(draft_logits, dtype=np.float32)
+            if draft_logits.shape != (B, G, V):
+                raise ValueError("draft logits must be [B, G, V]")
+        if uniforms is not None:
+            uniforms = np.ascontiguousarray(uniforms, dtype=np.float64)
+            if uniforms.shape != (B, G + 1):
+                raise ValueError("uniforms must be [B, G+1]")
+        if temperature != 0 and (draft_logits is None or uniforms is None):
+            raise ValueError("sampling needs the draft logits and the uniforms")
+        n = np.empty(B, np.int32)
+        nxt = np.empty(B, np.int32)
+        st = self.lib.orc_spec_accept(_ptr(target_logits), _ptr(draft_logits), _ptr(draft_tokens), _ptr(uniforms),
+                                      B, G, V, float(temperature), _ptr(n), _ptr(nxt))
+        return n, nxt, int(st)

@@ -390,4 +390,128 @@ def pin_fused_step_is_its_parts(orc):
     assert np.array_equal(kc[1], _np(case.k_cache)[1]) and np.all(out[1] == 0) and np.all(np.isneginf(lse[1]))
 
 
+# --- speculative accept/reject ----------------------------------------------------------------
+
+_CHI2_1PCT_5DOF = 15.086  # chi-square 1% critical value, 5 degrees of freedom
+
+
+def _softmax(logits, T):
+    z = logits.astype(F64) / T
+    z = np.exp(z - z.max(axis=-1, keepdims=True))
+    return z / z.sum(axis=-1, keepdims=True)
+
+
+def _chi2(samples, p):
+    counts = np.bincount(samples, minlength=len(p)).astype(F64)
+    exp_ = p * len(samples)
+    return float(((counts - exp_) ** 2 / exp_).sum())
+
+
+def _spec_batch(orc, p_logits, q_logits, G, N, T, seed):
+    """N independent steps with context-free target/draft rows; drafts drawn from q."""
+    rng = np.random.default_rng(seed)
+    V = len(p_logits)
+    q = _softmax(q_logits, T)
+    tokens = np.stack([rng.choice(V, size=N, p=q) for _ in range(G)], axis=1).astype(np.int32)
+    target = np.broadcast_to(p_logits.astype(np.float32), (N, G + 1, V)).copy()
+    draft = np.broadcast_to(q_logits.astype(np.float32), (N, G, V)).copy()
+    u = rng.random((N, G + 1))
+    n, nxt, st = orc.spec_accept(target, draft, tokens, u, T)
+    return tokens, n, nxt, st
+
+
+def pin_spec_output_follows_target(orc):
+    """The pages' chi-squared check: vocabulary 6, N = 30,000, draft q != target p, gamma 1
+    and 4; the first emitted token (and with gamma 4 the second) is distributed as p
+    (temperature 0.7 applied to both)."""
+    p_logits = np.array([1.2, -0.3, 0.4, 2.0, -1.0, 0.1])
+    q_logits = np.array([-0.5, 1.5, 0.3, 0.2, 1.0, -0.2])
+    T = 0.7
+    p = _softmax(p_logits, T)
+    for G, seed in ((1, 11), (4, 12)):
+        tokens, n, nxt, st = _spec_batch(orc, p_logits, q_logits, G, 30000, T, seed)
+        assert st == 0
+        first = np.where(n >= 1, tokens[:, 0], nxt)
+        assert _chi2(first, p) < _CHI2_1PCT_5DOF, ("first token", G)
+        if G >= 2:
+            has2 = n >= 1
+            second = np.where(n[has2] >= 2, tokens[has2, 1], nxt[has2])
+            assert _chi2(second, p) < _CHI2_1PCT_5DOF, ("second token", G)
+
+
+def pin_spec_acceptance_rate(orc):
+    """P(first draft accepted) = sum_x min(p(x), q(x)) (Leviathan et al.'s alpha), within
+    four binomial standard deviations."""
+    p_logits = np.array([0.5, 0.0, -1.0, 1.5, 0.2, -0.4])
+    q_logits = np.array([0.0, 1.0, 0.5, -0.5, 0.2, 0.3])
+    p, q = _softmax(p_logits, 1.0), _softmax(q_logits, 1.0)
+    alpha = float(np.minimum(p, q).sum())
+    N = 20000
+    _, n, _, _ = _spec_batch(orc, p_logits, q_logits, 1, N, 1.0, 13)
+    rate = float((n >= 1).mean())
+    assert abs(rate - alpha) < 4 * math.sqrt(alpha * (1 - alpha) / N), (rate, alpha)
+
+
+def pin_spec_residual_distribution(orc):
+    """A draft token the target gives probability 0 is always rejected, and the extra token
+    then follows max(0, p - q) / ||max(0, p - q)||_1."""
+    p_logits = np.array([0.3, -np.inf, 1.0, 0.2, -0.5, 0.8])
+    q_logits = np.array([0.0, 2.0, 0.1, 0.4, 0.0, 0.3])
+    p, q = _softmax(p_logits, 1.0), _softmax(q_logits, 1.0)
+    res = np.maximum(0.0, p - q)
+    res /= res.sum()
+    N = 30000
+    rng = np.random.default_rng(14)
+    target = np.broadcast_to(p_logits.astype(np.float32), (N, 2, 6)).copy()
+    draft = np.broadcast_to(q_logits.astype(np.float32), (N, 1, 6)).copy()
+    tokens = np.full((N, 1), 1, np.int32)
+    n, nxt, st = orc.spec_accept(target, draft, tokens, rng.random((N, 2)), 1.0)
+    assert st == 0 and np.all(n == 0)
+    keep = res > 0
+    assert np.all(keep[nxt])  # never a token outside the residual's support
+    counts = np.bincount(nxt, minlength=6)[keep].astype(F64)
+    exp_ = res[keep] * N
+    assert float(((counts - exp_) ** 2 / exp_).sum()) < 13.277  # 1% point, 4 degrees of freedom
+
+
+def pin_spec_draft_equals_target(orc):
+    """q = p: every draft token is accepted and the extra token is the inverse-CDF draw from
+    the bonus row (checked against numpy's cumulative sum)."""
+    rng = np.random.default_rng(15)
+    B, G, V = 64, 3, 50
+    logits = rng.standard_normal((B, G + 1, V)).astype(np.float32)
+    tokens = rng.integers(0, V, (B, G)).astype(np.int32)
+    u = rng.random((B, G + 1))
+    n, nxt, st = orc.spec_accept(logits, logits[:, :G].copy(), tokens, u, 1.0)
+    assert st == 0 and np.all(n == G)
+    cdf = np.cumsum(_softmax(logits[:, G], 1.0), axis=1)
+    ref = np.array([int(np.searchsorted(cdf[b], u[b, G] * cdf[b, -1], side="right")) for b in range(B)])
+    assert np.array_equal(nxt, ref)
+
+
+def pin_spec_greedy_prefix(orc):
+    """Temperature 0: accept while the draft token is the target's argmax; the extra token is
+    the target's argmax after the accepted prefix (ties to the lowest id)."""
+    V, G = 8, 3
+    target = np.zeros((3, G + 1, V), np.float32)
+    arg = np.array([[2, 5, 1, 7], [4, 4, 0, 3], [6, 1, 2, 2]])
+    for b in range(3):
+        for i in range(G + 1):
+            target[b, i, arg[b, i]] = 1.0
+    target[2, 3, 0] = 1.0  # a tie at the bonus row: id 0 wins over 2
+    draft = np.full((3, G, V), 0.0, np.float32)
+    draft[:, :, 3] = 5.0  # the draft's own argmax is 3 everywhere
+    tokens = np.array([[2, 5, 0], [4, 4, 0], [6, 1, 2]], np.int32)
+    n, nxt, st = orc.spec_accept(target, draft, tokens, None, 0.0)
+    assert st == 0 and n.tolist() == [2, 3, 3] and nxt.tolist() == [1, 3, 0]
+
+
+def pin_spec_bad_token(orc):
+    """A draft token outside [0, V) stops acceptance there and raises the status bit."""
+    target = np.zeros((1, 3, 4), np.float32)
+    draft = np.zeros((1, 2, 4), np.float32)
+    n, _, st = orc.spec_accept(target, draft, np.array([[1, 9]], np.int32), np.array([[0.1, 0.1, 0.5]]), 1.0)
+    assert st == orc_mod.BAD_TOKEN and n.tolist() == [1]
+
+
 PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_") and callable(v)]

@@ -20,6 +20,9 @@ MUTANTS = {
     13: "bf16 bits read as IEEE half",
     14: "rotary pairs turned the wrong way",
     15: "rotary pairs taken as neighbours (2i, 2i+1)",
+    16: "acceptance ratio inverted (q/p)",
+    17: "residual taken as max(0, q - p)",
+    18: "greedy compares with the draft's argmax",
 }
 
 
