@@ -251,6 +251,42 @@ def kernel_label(td, w) -> str:
     return f"{names[plan['kernel']]}, grid {plan['grid']}, timed alone"
 
 
+def spec_point(td, dev, l2_bytes, peak, B=1, G=4, V=128256, budget_calls=200):
+    """The speculative accept/reject step alone (a NEXT row): graph of R launches over rotating
+    copies of fp32 logits (a Llama-3-sized vocabulary); algorithmic bytes = every target and
+    draft row read once, (2G+1) * V * 4 per sequence."""
+    gen = torch.Generator().manual_seed(5)
+    bytes_call = B * (2 * G + 1) * V * 4
+    C = max(2, math.ceil(4 * l2_bytes / bytes_call))
+    target = torch.randn(C, B, G + 1, V, generator=gen).to(dev)
+    draft = (target[:, :, :G] + 0.5 * torch.randn(C, B, G, V, generator=gen).to(dev)).contiguous()
+    tokens = torch.randint(0, V, (B, G), generator=gen, dtype=torch.int32).to(dev)
+    u = torch.rand(B, G + 1, generator=gen).to(dev)
+    n = torch.empty(B, dtype=torch.int32, device=dev)
+    nxt = torch.empty(B, dtype=torch.int32, device=dev)
+    R = max(C, budget_calls)
+    s = torch.cuda.Stream(dev)
+
+    def calls():
+        for i in range(R):
+            td.td_spec_accept(target[i % C], tokens, draft[i % C], u, 1.0, n_accepted=n, next_token=nxt, stream=s)
+
+    with torch.cuda.stream(s):
+        calls()
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        calls()
+    ms = min(time_graph(g, s, 3) for _ in range(3))
+    us = ms * 1e3 / (3 * R)
+    del target, draft
+    torch.cuda.empty_cache()
+    gbs = bytes_call / (us * 1e-6) / 1e9
+    return {"row": "speculative accept/reject (td_spec_accept)", "B": B, "draft_tokens": G, "vocab": V,
+            "temperature": 1.0, "us_per_call": round(us, 3), "logit_gbs": round(gbs, 1),
+            "frac_of_measured_hbm": round(gbs / peak, 4), "bytes_per_call": bytes_call}
+
+
 def sweep_point(td, name, L, dev, l2_bytes, peak, budget_calls=200):
     """Attention kernel alone on one workload point: graph of R launches over rotating caches."""
     w = WORKLOADS[name]
@@ -422,7 +458,7 @@ def run_td(args, world, rank, local):
     if rank != 0:
         return
     cpu = None if (args.no_cpu or world > 1) else cpu_baseline(case, w, L, args.cpu_seconds)
-    sweep = None
+    sweep = next_rows = None
     if not args.no_sweep:
         del kc, vc
         torch.cuda.empty_cache()
@@ -432,6 +468,7 @@ def run_td(args, world, rank, local):
                 sweep.append(sweep_point(td, name, Ls, dev, l2, peak))
         sweep.append(sweep_point(td, "ragged8", None, dev, l2, peak))
         sweep.append(sweep_point(td, "verify6", 16390, dev, l2, peak))
+        next_rows = [spec_point(td, dev, l2, peak), spec_point(td, dev, l2, peak, B=8)]
     traffic = recorded_traffic("split_attn_kernel", f"{w.name}:{L}")
     line = {
         "metric": METRIC,
@@ -465,6 +502,7 @@ def run_td(args, world, rank, local):
         "e2e": e2e,
         "cpu_baseline": cpu,
         "sweep": sweep,
+        "next_rows": next_rows,
         "kernel_source": kernel_source_hash(),
         "device": props.name,
     }

@@ -8,6 +8,7 @@ missing.
 """
 from .api import (  # noqa: F401
     DEV_APPEND_OVERFLOW,
+    DEV_BAD_TOKEN,
     DEV_NEGATIVE_SEQLEN,
     DEV_SEQLEN_CLAMPED,
     DEV_VERIFY_SHORT,
@@ -20,6 +21,7 @@ from .api import (  # noqa: F401
     td_lse_merge,
     td_rope_append_attn,
     td_rope_kv_append,
+    td_spec_accept,
     td_split_plan,
     td_verify_attn,
 )

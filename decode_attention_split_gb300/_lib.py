@@ -16,6 +16,8 @@ SYMBOLS = (
     "td_split_plan",
     "td_rope_kv_append",
     "td_rope_append_attn",
+    "td_spec_accept",
+    "td_spec_workspace_bytes",
     "td_kv_append",
     "td_decode_attn",
     "td_verify_attn",
@@ -52,6 +54,10 @@ def _declare(lib):
     lib.td_rope_append_attn.argtypes = [i, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, i, vp, vp, vp,
                                         sz, vp, vp]
     lib.td_rope_append_attn.restype = i
+    lib.td_spec_accept.argtypes = [vp, vp, vp, vp, i, i, i, f, vp, vp, vp, sz, vp, vp]
+    lib.td_spec_workspace_bytes.argtypes = [i, i, i]
+    lib.td_spec_workspace_bytes.restype = sz
+    lib.td_spec_accept.restype = i
     lib.td_kv_append.argtypes = [i, vp, vp, vp, vp, vp, i, i, i, i, i, i, vp, vp]
     lib.td_kv_append.restype = i
     lib.td_decode_attn.argtypes = [i, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, vp, vp, sz, vp, vp]

@@ -26,6 +26,7 @@ DEV_VERIFY_SHORT = 4
 DEV_NEGATIVE_SEQLEN = 8
 DEV_WAIT_TIMEOUT = 16
 DEV_WORKSPACE_DIRTY = 32
+DEV_BAD_TOKEN = 64
 
 _ws_lock = threading.Lock()
 _ws_cache: dict[tuple[int, int], torch.Tensor] = {}
@@ -303,3 +304,41 @@ def td_rope_append_attn(q, k_new, v_new, k_cache, v_cache, seq_lens, scale: floa
                                        _ptr(workspace), workspace.numel(), _ptr(dev_status), sp)
     check("td_rope_append_attn", st)
     return (out, lse) if (return_lse or lse is not None) else out
+
+
+def td_spec_accept(target_logits, draft_tokens, draft_logits=None, uniforms=None, temperature: float = 1.0,
+                   n_accepted=None, next_token=None, workspace=None, dev_status=None, stream=None):
+    """Speculative accept/reject (td.h): target_logits fp32 [B, G+1, V], draft_tokens int32
+    [B, G], draft_logits fp32 [B, G, V] and uniforms fp32 [B, G+1] (both unused when
+    temperature is 0) -> (n_accepted int32 [B], next_token int32 [B])."""
+    dev = _cuda(target_logits, draft_tokens, draft_logits, uniforms, n_accepted, next_token, dev_status)
+    if target_logits.dim() != 3 or target_logits.dtype != torch.float32:
+        raise TypeError("target_logits must be float32 [B, G+1, V]")
+    B, G1, V = target_logits.shape
+    G = G1 - 1
+    if draft_tokens.dtype != torch.int32 or tuple(draft_tokens.shape) != (B, G):
+        raise TypeError("draft_tokens must be int32 [B, G]")
+    if temperature != 0:
+        if draft_logits is None or uniforms is None:
+            raise ValueError("sampling needs draft_logits and uniforms")
+        if draft_logits.dtype != torch.float32 or tuple(draft_logits.shape) != (B, G, V):
+            raise TypeError("draft_logits must be float32 [B, G, V]")
+        if uniforms.dtype != torch.float32 or tuple(uniforms.shape) != (B, G + 1):
+            raise TypeError("uniforms must be float32 [B, G+1]")
+    if n_accepted is None:
+        n_accepted = torch.empty(B, dtype=torch.int32, device=target_logits.device)
+    if next_token is None:
+        next_token = torch.empty(B, dtype=torch.int32, device=target_logits.device)
+    with torch.cuda.device(dev):
+        sp = _stream(stream, dev)
+        if workspace is None:
+            need = int(lib().td_spec_workspace_bytes(B, G, V))
+            workspace = _cached_workspace(need, dev, sp, ("spec", B, G, V))
+        if workspace.dtype != torch.uint8:
+            raise TypeError("workspace must be a uint8 tensor")
+        st = lib().td_spec_accept(_ptr(target_logits), _ptr(draft_logits if temperature != 0 else None),
+                                  _ptr(draft_tokens), _ptr(uniforms if temperature != 0 else None), B, G, V,
+                                  float(temperature), _ptr(n_accepted), _ptr(next_token), _ptr(workspace),
+                                  workspace.numel(), _ptr(dev_status), sp)
+    check("td_spec_accept", st)
+    return n_accepted, next_token

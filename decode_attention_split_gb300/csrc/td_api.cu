@@ -214,3 +214,35 @@ td_status td_rope_append_attn(td_dtype dtype, const void *q, const void *k_new, 
 }
 
 }  // extern "C"
+
+extern "C" size_t td_spec_workspace_bytes(int B, int G, int V) {
+  if (B < 1 || G < 0 || G > td::kMaxDraft || V < 1) return 0;
+  return td::spec_workspace_bytes(B, G, V);
+}
+
+extern "C" td_status td_spec_accept(const float *target_logits, const float *draft_logits,
+                                    const int32_t *draft_tokens, const float *uniforms, int B, int G, int V,
+                                    float temperature, int32_t *n_accepted, int32_t *next_token, void *workspace,
+                                    size_t workspace_bytes, uint32_t *dev_status, void *stream) {
+  const bool greedy = temperature == 0.f;
+  if (target_logits == nullptr || n_accepted == nullptr || next_token == nullptr ||
+      (G > 0 && draft_tokens == nullptr) || (!greedy && (uniforms == nullptr || (G > 0 && draft_logits == nullptr))))
+    return TD_ERR_INVALID_ARG;
+  if (B < 1 || G < 0 || V < 1 || !(temperature >= 0.f) || !isfinite(temperature)) return TD_ERR_INVALID_ARG;
+  if (G > td::kMaxDraft) return TD_ERR_UNSUPPORTED;
+  if ((long long)B * td::spec_slices(V) > 0x7fffffffLL) return TD_ERR_UNSUPPORTED;
+  if (!aligned4(target_logits) || (draft_logits != nullptr && !aligned4(draft_logits)) ||
+      (draft_tokens != nullptr && !aligned4(draft_tokens)) || (uniforms != nullptr && !aligned4(uniforms)) ||
+      !aligned4(n_accepted) || !aligned4(next_token) || (dev_status != nullptr && !aligned4(dev_status)))
+    return TD_ERR_UNSUPPORTED;
+  // 16-byte loads need 16-byte aligned rows
+  if ((V & 3) == 0 && (!aligned16(target_logits) || (!greedy && G > 0 && !aligned16(draft_logits))))
+    return TD_ERR_UNSUPPORTED;
+  if (workspace == nullptr || workspace_bytes < td::spec_workspace_bytes(B, G, V) ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return TD_ERR_WORKSPACE;
+  const cudaError_t e = td::launch_spec_accept(target_logits, greedy ? nullptr : draft_logits, draft_tokens,
+                                               greedy ? nullptr : uniforms, B, G, V, temperature, n_accepted,
+                                               next_token, dev_status, workspace, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? TD_OK : cuda_fail(e);
+}

@@ -115,6 +115,52 @@ __device__ __forceinline__ void bulk_g2s_plain(uint32_t dst, const void *src, ui
                : "memory");
 }
 
+// Ticket on a completion counter: release (the CTA's partial writes, ordered before this by
+// a barrier, become visible first) and acquire (other CTAs' released writes are visible
+// after it). Returns the previous count.
+__device__ __forceinline__ int ticket_acq_rel(int *cnt) {
+  int prev;
+  asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], 1;" : "=r"(prev) : "l"(cnt) : "memory");
+  return prev;
+}
+
+// ---- thread-block clusters ---------------------------------------------------------
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t cluster_nctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t cluster_id_x() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+  return r;
+}
+
+// Every thread of every CTA of the cluster: writes before it (shared or global) are visible
+// to the cluster after it.
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile(
+      "barrier.cluster.arrive.release.aligned;\n\t"
+      "barrier.cluster.wait.acquire.aligned;" ::
+          : "memory");
+}
+
+// Generic address of the variable at `p` (this CTA's shared memory) in CTA `rank`.
+template <typename T>
+__device__ __forceinline__ const T *map_to_rank(const T *p, uint32_t rank) {
+  uint64_t out;
+  asm volatile("mapa.u64 %0, %1, %2;" : "=l"(out) : "l"(p), "r"(rank));
+  return reinterpret_cast<const T *>(out);
+}
+
 // ---- widening of stored elements to fp32 ----------------------------------------------
 
 // A bf16 value is the upper half of a binary32 value.

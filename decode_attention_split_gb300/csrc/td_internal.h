@@ -43,6 +43,15 @@ cudaError_t launch_rope_append(size_t elem_bytes, const void *q, void *q_out, in
                                void *v_cache, int32_t *seq_lens, int B, int Hkv, int T, int Smax, int D, int advance,
                                uint32_t *dev_status, cudaStream_t stream);
 
+// Speculative accept/reject: most draft tokens per step, and the launch.
+constexpr int kMaxDraft = 16;
+constexpr int kMaxCluster = 16;  // CTAs per cluster, at most
+int spec_slices(int V);
+size_t spec_workspace_bytes(int B, int G, int V);
+cudaError_t launch_spec_accept(const float *target, const float *draft, const int32_t *tokens, const float *uniforms,
+                               int B, int G, int V, float temperature, int32_t *n_out, int32_t *tok_out,
+                               uint32_t *status, void *workspace, cudaStream_t stream);
+
 // SM count of the current device (cached per device).
 int device_sm_count(int device);
 

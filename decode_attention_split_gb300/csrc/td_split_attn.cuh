@@ -86,14 +86,6 @@ __device__ __forceinline__ int attended_len(const SplitParams &p, int32_t raw, u
 // bulk-copied and every acc row is 16-byte aligned.
 __host__ __device__ constexpr int part_block_floats(int R, int D) { return (R * (D + 2) + 3) / 4 * 4; }
 
-// Ticket on a completion counter: release (the CTA's partial writes, ordered before this by
-// a barrier, become visible first) and acquire (other CTAs' released writes are visible
-// after it). Returns the previous count.
-__device__ __forceinline__ int ticket_acq_rel(int *cnt) {
-  int prev;
-  asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], 1;" : "=r"(prev) : "l"(cnt) : "memory");
-  return prev;
-}
 
 template <typename E, int D, int RP>
 struct SplitCfg {

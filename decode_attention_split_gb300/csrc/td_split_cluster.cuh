@@ -13,46 +13,10 @@
 // (batches of a few sequences); the grid is groups x CS CTAs, fixed by the arguments.
 #pragma once
 
+#include "td_internal.h"
 #include "td_split_mma.cuh"
 
 namespace td {
-
-constexpr int kMaxCluster = 16;
-
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-
-__device__ __forceinline__ uint32_t cluster_nctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
-  return r;
-}
-
-__device__ __forceinline__ uint32_t cluster_id_x() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
-  return r;
-}
-
-// Every thread of every CTA of the cluster: writes before it (shared or global) are visible
-// to the cluster after it.
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile(
-      "barrier.cluster.arrive.release.aligned;\n\t"
-      "barrier.cluster.wait.acquire.aligned;" ::
-          : "memory");
-}
-
-// Generic address of the variable at `p` (this CTA's shared memory) in CTA `rank`.
-template <typename T>
-__device__ __forceinline__ const T *map_to_rank(const T *p, uint32_t rank) {
-  uint64_t out;
-  asm volatile("mapa.u64 %0, %1, %2;" : "=l"(out) : "l"(p), "r"(rank));
-  return reinterpret_cast<const T *>(out);
-}
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1) split_attn_cluster_kernel(const __grid_constant__ MmaArgs a) {

@@ -24,6 +24,8 @@
  *                  KV-cache write" in its decode step; "tinydecode" lists an in-place rope).
  *   td_rope_append_attn  the whole decode or verify step of one layer in one launch:
  *                  rotation, cache write and split attention.
+ *   td_spec_accept the accept/reject step after a verify pass ("tinydecode", "speculative
+ *                  decoding"; "FlashSpec", "How it works": Leviathan et al. Algorithm 1).
  *
  * Layouts (row-major, contiguous, element type given by td_dtype):
  *   q, out         [B, Hq, D] for decode; [B, Hq, T, D] for verify
@@ -74,6 +76,7 @@ typedef enum td_dtype { TD_F32 = 0, TD_BF16 = 1 } td_dtype;
 #define TD_DEV_WAIT_TIMEOUT 16u    /* a bounded wait for an asynchronous copy gave up: output invalid */
 #define TD_DEV_WORKSPACE_DIRTY 32u /* a completion counter was not zero: workspace not zeroed for this
                                       layout; output invalid (zero the workspace and call again) */
+#define TD_DEV_BAD_TOKEN 64u       /* speculative accept: a draft token outside [0, V), counted as rejected */
 
 /* Largest batch a call accepts. */
 #define TD_MAX_BATCH 1024
@@ -202,6 +205,34 @@ td_status td_rope_append_attn(td_dtype dtype, const void *q, const void *k_new, 
                               int Hkv, int T, int Smax, int D, float scale, int split, int advance, void *out,
                               float *lse, void *workspace, size_t workspace_bytes, uint32_t *dev_status,
                               void *stream);
+
+/*
+ * Speculative accept/reject for B sequences, each with G draft tokens (0 <= G <= 16) over a
+ * vocabulary of V:
+ *   target_logits [B, G+1, V] fp32   row i: the target's next-token logits after the prefix
+ *                                     and draft tokens 0..i-1 (row G: the bonus row)
+ *   draft_logits  [B, G, V] fp32     row i: the logits draft token i was drawn from
+ *   draft_tokens  [B, G] int32
+ *   uniforms      [B, G+1] fp32 in [0, 1): entry i < G decides draft token i, entry G draws
+ *                                     the extra token (the caller's random numbers)
+ * With p = softmax(target / temperature), q = softmax(draft / temperature): draft token i is
+ * kept while uniforms[i] < min(1, p_i(x_i) / q_i(x_i)) (tested in log space); n_accepted[b]
+ * counts the kept prefix. next_token[b] is drawn by inverse CDF (the smallest id whose
+ * running weight exceeds u * total) from max(0, p_n - q_n) when a token was rejected at n,
+ * else from p_G; a residual with no weight falls back to p_n. temperature == 0 is greedy:
+ * keep while the draft token is the target's argmax (lowest id on ties); next_token is
+ * the argmax of row n; draft_logits and uniforms may then be NULL. A draft token outside
+ * [0, V) counts as rejected and sets TD_DEV_BAD_TOKEN. All pointers are device pointers,
+ * 4-byte aligned (logits 16-byte aligned when V % 4 == 0); n_accepted, next_token int32 [B].
+ * workspace: td_spec_workspace_bytes(B, G, V) bytes, 256-byte aligned, zero-filled before its
+ * first use; every call leaves it ready for the next on the same stream (any shape up to the
+ * size it was sized for). Two launches (the second only when sampling).
+ */
+size_t td_spec_workspace_bytes(int B, int G, int V);
+td_status td_spec_accept(const float *target_logits, const float *draft_logits, const int32_t *draft_tokens,
+                         const float *uniforms, int B, int G, int V, float temperature, int32_t *n_accepted,
+                         int32_t *next_token, void *workspace, size_t workspace_bytes, uint32_t *dev_status,
+                         void *stream);
 
 /*
  * Decode attention without a workspace argument: the same computation and arguments as
