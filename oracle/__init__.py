@@ -100,6 +100,8 @@ class Oracle:
         lib.orc_kv_append.restype = ctypes.c_uint
         lib.orc_rope.argtypes = [i, vp, ctypes.c_int64, i, vp, vp, vp, vp]
         lib.orc_rope.restype = None
+        lib.orc_quantize_q8.argtypes = [i, vp, ctypes.c_int64, i, vp, vp]
+        lib.orc_quantize_q8.restype = None
         lib.orc_spec_accept.argtypes = [vp, vp, vp, vp, i, i, i, d, vp, vp]
         lib.orc_spec_accept.restype = ctypes.c_uint
         lib.orc_num_threads.restype = i
@@ -250,3 +252,29 @@ class Oracle:
         st = self.lib.orc_spec_accept(_ptr(target_logits), _ptr(draft_logits), _ptr(draft_tokens), _ptr(uniforms),
                                       B, G, V, float(temperature), _ptr(n), _ptr(nxt))
         return n, nxt, int(st)
+
+    def quantize_q8(self, x):
+        """Per-row symmetric int8 codes of rows x[..., D] (bf16 bits or fp32): returns
+        (codes int8 shaped like x, scales float32 x.shape[:-1]); decided in fp32."""
+        x = np.ascontiguousarray(x)
+        D = x.shape[-1]
+        rows = x.size // D
+        codes = np.empty(x.shape, np.int8)
+        scales = np.empty(x.shape[:-1], np.float32)
+        self.lib.orc_quantize_q8(_code(x), _ptr(x), rows, D, _ptr(codes), _ptr(scales))
+        return codes, scales
+
+    @staticmethod
+    def dequantize_q8(codes, scales):
+        """The rows the codes stand for, exactly: code * scale in fp64."""
+        return codes.astype(np.float64) * scales.astype(np.float64)[..., None]
+
+    def attention_q8(self, q, k_codes, k_scales, v_codes, v_scales, seq_lens, scale: float):
+        """Attention over a quantised cache: the exact attention of q (widened) over the
+        dequantised rows. Same conventions as attention()."""
+        qd = q
+        if q.dtype == np.uint16:
+            qd = (q.astype(np.uint32) << 16).view(np.float32)
+        qd = np.ascontiguousarray(qd, dtype=np.float64)
+        return self.attention(qd, np.ascontiguousarray(self.dequantize_q8(k_codes, k_scales)),
+                              np.ascontiguousarray(self.dequantize_q8(v_codes, v_scales)), seq_lens, scale)

@@ -415,3 +415,43 @@ void orc_rope(int dtype, const void *x, int64_t rows, int D, const int32_t *pos,
     }
   }
 }
+
+/* Symmetric 8-bit quantisation of cache rows, one scale per row (the quantised KV cache:
+ * "llm-decode-cuda" quantises its weights to INT8, one scale per row, dequantised in
+ * registers after the load; the same scheme is read here for the K and V rows, which bound
+ * the decode step). For each row of D elements, in fp32 (the precision the kernels decide
+ * the codes in, so both sides reach the same integers):
+ *   amax  = max_i |x_i|
+ *   scale = amax / 127                      (IEEE division, rounded to nearest)
+ *   code  = clamp(rint(x_i / scale), -127, 127), 0 when scale == 0
+ * and the row reads back as code_i * scale. */
+void orc_quantize_q8(int dtype, const void *x, int64_t rows, int D, int8_t *codes, float *scales) {
+  for (int64_t r = 0; r < rows; ++r) {
+    float amax = 0.0f;
+    for (int i = 0; i < D; ++i) {
+      const float v = (float)widen(dtype, x, r * D + i);
+      const float a = v < 0.0f ? -v : v;
+      if (a > amax) amax = a;
+    }
+#if ORC_MUTANT == 19
+    const float scale = amax / 128.0f; /* planted: the wrong full-scale code */
+#else
+    const float scale = amax / 127.0f;
+#endif
+    scales[r] = scale;
+    for (int i = 0; i < D; ++i) {
+      float c = 0.0f;
+      if (scale > 0.0f) {
+        const float q = (float)widen(dtype, x, r * D + i) / scale;
+#if ORC_MUTANT == 20
+        c = truncf(q); /* planted: truncation instead of rounding */
+#else
+        c = nearbyintf(q);
+#endif
+        if (c > 127.0f) c = 127.0f;
+        if (c < -127.0f) c = -127.0f;
+      }
+      codes[r * D + i] = (int8_t)c;
+    }
+  }
+}

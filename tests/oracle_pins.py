@@ -514,4 +514,58 @@ def pin_spec_bad_token(orc):
     assert st == orc_mod.BAD_TOKEN and n.tolist() == [1]
 
 
+# --- quantised KV cache ---------------------------------------------------------------------
+
+def pin_q8_round_trip_bound(orc):
+    """Every element reads back within half a step of the row's scale; codes are integers in
+    [-127, 127] and the largest magnitude of the row takes the full-scale code."""
+    rng = np.random.default_rng(21)
+    x = (rng.standard_normal((50, 64)) * rng.uniform(0.01, 100, (50, 1))).astype(np.float32)
+    codes, scales = orc.quantize_q8(x)
+    back = orc.dequantize_q8(codes, scales)
+    assert codes.min() >= -127 and codes.max() <= 127
+    assert np.all(np.abs(back - x) <= scales[:, None].astype(F64) * (0.5 + 1e-6))
+    top = np.abs(x).argmax(axis=1)
+    assert np.all(np.abs(codes[np.arange(50), top]) == 127)
+    xb = torch.from_numpy(x).to(torch.bfloat16)
+    cb, sb = orc.quantize_q8(_np(xb))
+    assert np.all(np.abs(orc.dequantize_q8(cb, sb) - xb.double().numpy()) <= sb[:, None].astype(F64) * (0.5 + 1e-6))
+
+
+def pin_q8_ties_to_even_and_symmetry(orc):
+    """With amax 127 the scale is exactly 1: halves round to even; negating the row negates the
+    codes; doubling it keeps the codes and doubles the scale exactly; a zero row is all zero."""
+    x = np.array([[127.0, 0.5, 1.5, 2.5, -0.5, -2.5, 3.49, -126.6]], np.float32)
+    codes, scales = orc.quantize_q8(x)
+    assert scales[0] == 1.0 and codes[0].tolist() == [127, 0, 2, 2, 0, -2, 3, -127]
+    rng = np.random.default_rng(22)
+    y = rng.standard_normal((10, 32)).astype(np.float32)
+    c1, s1 = orc.quantize_q8(y)
+    c2, s2 = orc.quantize_q8(-y)
+    c3, s3 = orc.quantize_q8(2 * y)
+    assert np.array_equal(c2, -c1) and np.array_equal(s2, s1)
+    assert np.array_equal(c3, c1) and np.array_equal(s3, 2 * s1)
+    c0, s0 = orc.quantize_q8(np.zeros((2, 16), np.float32))
+    assert not c0.any() and not s0.any()
+
+
+def pin_q8_attention_reads_the_dequantised_cache(orc):
+    """A cache whose rows are small integers with scale 1 quantises to itself, and attention
+    over the codes equals attention over the original bf16 cache."""
+    rng = np.random.default_rng(23)
+    B, Hq, Hkv, S, D = 2, 4, 2, 40, 16
+    k = rng.integers(-127, 128, (B, Hkv, S, D)).astype(np.float32)
+    v = rng.integers(-127, 128, (B, Hkv, S, D)).astype(np.float32)
+    k[..., 0] = 127.0  # full-scale element in every row: scale exactly 1
+    v[..., 0] = -127.0
+    q = rng.standard_normal((B, Hq, D)).astype(np.float32) * 0.01
+    kc, ks = orc.quantize_q8(k)
+    vc, vs = orc.quantize_q8(v)
+    assert np.all(ks == 1.0) and np.all(vs == 1.0) and np.array_equal(kc, k.astype(np.int8))
+    sl = np.array([40, 7], np.int32)
+    out, lse, _ = orc.attention_q8(q, kc, ks, vc, vs, sl, 0.5)
+    ref, ref_lse, _ = orc.attention(q, k, v, sl, 0.5)
+    assert np.allclose(out, ref, rtol=0, atol=1e-12) and np.allclose(lse, ref_lse, rtol=0, atol=1e-12)
+
+
 PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_") and callable(v)]

@@ -23,6 +23,8 @@ MUTANTS = {
     16: "acceptance ratio inverted (q/p)",
     17: "residual taken as max(0, q - p)",
     18: "greedy compares with the draft's argmax",
+    19: "int8 scale from a full-scale code of 128",
+    20: "int8 codes truncated instead of rounded",
 }
 
 
