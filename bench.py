@@ -287,6 +287,49 @@ def spec_point(td, dev, l2_bytes, peak, B=1, G=4, V=128256, budget_calls=200):
             "frac_of_measured_hbm": round(gbs / peak, 4), "bytes_per_call": bytes_call}
 
 
+def q8_point(td, name, L, dev, l2_bytes, peak, budget_calls=200):
+    """Decode over the 8-bit cache (a NEXT row): the workload's cache quantised on the GPU, then
+    a graph of R attention launches over rotating copies. Algorithmic bytes: every visible K
+    and V row's codes and scale, L * Hkv * 2 * (D + 4) per sequence."""
+    w = WORKLOADS[name]
+    case = make_case(w, seq_len=L)
+    kc, ks = td.td_quantize_q8(case.k_cache.to(dev))
+    vc, vs = td.td_quantize_q8(case.v_cache.to(dev))
+    bytes_call = sum(case.seq_lens.tolist()) * w.Hkv * 2 * (w.D + 4)
+    C = max(2, math.ceil(4 * l2_bytes / bytes_call))
+    per_copy = (kc.numel() + ks.numel() * 4) * 2
+    C = min(C, max(2, int(24e9 // per_copy)))
+    kcs, kss, vcs, vss = (rotating_copies(t, C) for t in (kc, ks, vc, vs))
+    q = case.q.to(dev)[:, :, 0]
+    sl = case.seq_lens.to(dev)
+    out = torch.empty_like(q)
+    ws = td.make_workspace(w.B, w.Hq, w.Hkv, w.Smax, w.D, 1, 0, device=dev)
+    R = max(C, budget_calls)
+    s = torch.cuda.Stream(dev)
+
+    def calls():
+        for i in range(R):
+            c = i % C
+            td.td_decode_attn_q8(q, kcs[c], kss[c], vcs[c], vss[c], sl, case.scale, 0, out=out, workspace=ws,
+                                 stream=s)
+
+    with torch.cuda.stream(s):
+        calls()
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        calls()
+    ms = min(time_graph(g, s, 3) for _ in range(3))
+    us = ms * 1e3 / (3 * R)
+    del kcs, kss, vcs, vss
+    torch.cuda.empty_cache()
+    gbs = bytes_call / (us * 1e-6) / 1e9
+    bf16_bytes = kv_read_bytes(w, case.seq_lens.tolist())
+    return {"row": "int8 KV cache (td_decode_attn_q8)", "workload": name, "seq_len": L, "us_per_call": round(us, 3),
+            "kv_gbs": round(gbs, 1), "frac_of_measured_hbm": round(gbs / peak, 4), "kv_bytes": bytes_call,
+            "bf16_equivalent_gbs": round(bf16_bytes / (us * 1e-6) / 1e9, 1)}
+
+
 def sweep_point(td, name, L, dev, l2_bytes, peak, budget_calls=200):
     """Attention kernel alone on one workload point: graph of R launches over rotating caches."""
     w = WORKLOADS[name]
@@ -469,6 +512,7 @@ def run_td(args, world, rank, local):
         sweep.append(sweep_point(td, "ragged8", None, dev, l2, peak))
         sweep.append(sweep_point(td, "verify6", 16390, dev, l2, peak))
         next_rows = [spec_point(td, dev, l2, peak), spec_point(td, dev, l2, peak, B=8)]
+        next_rows += [q8_point(td, "llama3b", Ls, dev, l2, peak) for Ls in (4096, 16384, 32768)]
     traffic = recorded_traffic("split_attn_kernel", f"{w.name}:{L}")
     line = {
         "metric": METRIC,

@@ -16,12 +16,16 @@ from .api import (  # noqa: F401
     DEV_WORKSPACE_DIRTY,
     make_workspace,
     td_decode_attn,
+    td_decode_attn_q8,
     td_decode_workspace_bytes,
     td_kv_append,
+    td_kv_append_q8,
     td_lse_merge,
     td_rope_append_attn,
     td_rope_kv_append,
+    td_quantize_q8,
     td_spec_accept,
     td_split_plan,
     td_verify_attn,
+    td_verify_attn_q8,
 )

@@ -18,6 +18,10 @@ SYMBOLS = (
     "td_rope_append_attn",
     "td_spec_accept",
     "td_spec_workspace_bytes",
+    "td_quantize_q8",
+    "td_kv_append_q8",
+    "td_decode_attn_q8",
+    "td_verify_attn_q8",
     "td_kv_append",
     "td_decode_attn",
     "td_verify_attn",
@@ -57,6 +61,15 @@ def _declare(lib):
     lib.td_spec_accept.argtypes = [vp, vp, vp, vp, i, i, i, f, vp, vp, vp, sz, vp, vp]
     lib.td_spec_workspace_bytes.argtypes = [i, i, i]
     lib.td_spec_workspace_bytes.restype = sz
+    ll = ctypes.c_longlong
+    lib.td_quantize_q8.argtypes = [i, vp, ll, i, vp, vp, vp]
+    lib.td_quantize_q8.restype = i
+    lib.td_kv_append_q8.argtypes = [i, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, vp, vp]
+    lib.td_kv_append_q8.restype = i
+    lib.td_decode_attn_q8.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, vp, vp, sz, vp, vp]
+    lib.td_decode_attn_q8.restype = i
+    lib.td_verify_attn_q8.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp, vp, vp, sz, vp, vp]
+    lib.td_verify_attn_q8.restype = i
     lib.td_spec_accept.restype = i
     lib.td_kv_append.argtypes = [i, vp, vp, vp, vp, vp, i, i, i, i, i, i, vp, vp]
     lib.td_kv_append.restype = i

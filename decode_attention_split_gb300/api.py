@@ -342,3 +342,72 @@ def td_spec_accept(target_logits, draft_tokens, draft_logits=None, uniforms=None
                                   workspace.numel(), _ptr(dev_status), sp)
     check("td_spec_accept", st)
     return n_accepted, next_token
+
+
+def td_quantize_q8(x, codes=None, scales=None, stream=None):
+    """Per-row int8 codes and fp32 scales of x [..., D] (float32 or bfloat16), as td.h defines."""
+    dev = _cuda(x, codes, scales)
+    D = x.shape[-1]
+    rows = x.numel() // D
+    if codes is None:
+        codes = torch.empty(x.shape, dtype=torch.int8, device=x.device)
+    if scales is None:
+        scales = torch.empty(x.shape[:-1], dtype=torch.float32, device=x.device)
+    with torch.cuda.device(dev):
+        st = lib().td_quantize_q8(_code(x), _ptr(x), rows, D, _ptr(codes), _ptr(scales), _stream(stream, dev))
+    check("td_quantize_q8", st)
+    return codes, scales
+
+
+def td_kv_append_q8(k_new, v_new, k_codes, k_scales, v_codes, v_scales, seq_lens, advance: bool = True,
+                    dev_status=None, stream=None) -> None:
+    """Quantise k_new/v_new [B,Hkv,T,D] into an int8 cache at rows seq_lens[b].. (td_kv_append's rules)."""
+    dev = _cuda(k_new, v_new, k_codes, k_scales, v_codes, v_scales, seq_lens, dev_status)
+    B, Hkv, T, D = k_new.shape
+    Smax = k_codes.shape[2]
+    if k_codes.dtype != torch.int8 or v_codes.dtype != torch.int8 or k_codes.shape != (B, Hkv, Smax, D):
+        raise TypeError("codes must be int8 [B, Hkv, Smax, D]")
+    if k_scales.shape != (B, Hkv, Smax) or k_scales.dtype != torch.float32 or v_scales.shape != k_scales.shape:
+        raise TypeError("scales must be float32 [B, Hkv, Smax]")
+    with torch.cuda.device(dev):
+        st = lib().td_kv_append_q8(_code(k_new), _ptr(k_new), _ptr(v_new), _ptr(k_codes), _ptr(k_scales),
+                                   _ptr(v_codes), _ptr(v_scales), _ptr(seq_lens), B, Hkv, T, Smax, D,
+                                   int(bool(advance)), _ptr(dev_status), _stream(stream, dev))
+    check("td_kv_append_q8", st)
+
+
+def td_verify_attn_q8(q, k_codes, k_scales, v_codes, v_scales, seq_lens, scale: float | None = None, split: int = 0,
+                      out=None, lse=None, workspace=None, dev_status=None, stream=None, return_lse: bool = False):
+    """Attention over an int8 cache: q [B,Hq,T,D] or [B,Hq,D] (decode) bf16 -> out like q."""
+    decode = q.dim() == 3
+    q4 = q.unsqueeze(2) if decode else q
+    dev = _cuda(q4, k_codes, k_scales, v_codes, v_scales, seq_lens, out, lse, workspace, dev_status)
+    B, Hq, T, D = q4.shape
+    _, Hkv, Smax, _ = k_codes.shape
+    if q.dtype != torch.bfloat16 or k_codes.dtype != torch.int8 or v_codes.dtype != torch.int8:
+        raise TypeError("q must be bfloat16 and the codes int8")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device)
+    with torch.cuda.device(dev):
+        sp = _stream(stream, dev)
+        if workspace is None:
+            need = td_decode_workspace_bytes(B, Hq, Hkv, Smax, D, T, split)
+            workspace = _cached_workspace(need, dev, sp, ("q8", B, Hq, Hkv, Smax, D, T, split))
+        st = lib().td_verify_attn_q8(_ptr(q4), _ptr(k_codes), _ptr(k_scales), _ptr(v_codes), _ptr(v_scales),
+                                     _ptr(seq_lens), B, Hq, Hkv, T, Smax, D, float(scale), int(split), _ptr(out),
+                                     _ptr(lse), _ptr(workspace), workspace.numel(), _ptr(dev_status), sp)
+    check("td_verify_attn_q8", st)
+    return (out, lse) if (return_lse or lse is not None) else out
+
+
+def td_decode_attn_q8(q, k_codes, k_scales, v_codes, v_scales, seq_lens, scale: float | None = None, split: int = 0,
+                      out=None, lse=None, workspace=None, dev_status=None, stream=None, return_lse: bool = False):
+    """Single-token decode over an int8 cache: q [B,Hq,D] bf16 -> out [B,Hq,D]."""
+    if q.dim() != 3:
+        raise ValueError("q must be [B, Hq, D]")
+    return td_verify_attn_q8(q, k_codes, k_scales, v_codes, v_scales, seq_lens, scale, split, out, lse, workspace,
+                             dev_status, stream, return_lse)

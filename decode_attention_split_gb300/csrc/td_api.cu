@@ -22,11 +22,11 @@ size_t elem_size(td_dtype d) { return d == TD_F32 ? 4 : 2; }
 td_status prepare(td_dtype dtype, const void *q, const void *k_cache, const void *v_cache, const int32_t *seq_lens,
                   int B, int Hq, int Hkv, int T, int Smax, int D, float scale, int split, void *out, float *lse,
                   void *workspace, size_t workspace_bytes, uint32_t *dev_status, td::SplitPlan *plan,
-                  td::SplitParams *p) {
+                  td::SplitParams *p, bool q8 = false) {
   if (q == nullptr || k_cache == nullptr || v_cache == nullptr || seq_lens == nullptr || out == nullptr)
     return TD_ERR_INVALID_ARG;
   if (!isfinite(scale)) return TD_ERR_INVALID_ARG;
-  const td_status st = td::plan_split(dtype, B, Hq, Hkv, T, Smax, D, split, plan);
+  const td_status st = td::plan_split(dtype, B, Hq, Hkv, T, Smax, D, split, plan, q8);
   if (st == TD_ERR_CUDA) return cuda_fail(cudaGetLastError());
   if (st != TD_OK) return st;
   if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) || !aligned4(seq_lens) ||
@@ -102,6 +102,9 @@ size_t td_decode_workspace_bytes(int B, int Hq, int Hkv, int Smax, int D, int q_
     if (td::plan_split(dt, B, Hq, Hkv, q_len, Smax, D, split, &plan) != TD_OK) return 0;
     if (plan.bytes > bytes) bytes = plan.bytes;
   }
+  td::SplitPlan plan;  // the 8-bit cache kernel's layout (its grid may differ)
+  if (td::plan_split(TD_BF16, B, Hq, Hkv, q_len, Smax, D, split, &plan, true) == TD_OK && plan.bytes > bytes)
+    bytes = plan.bytes;
   return bytes;
 }
 
@@ -246,3 +249,60 @@ extern "C" td_status td_spec_accept(const float *target_logits, const float *dra
                                                next_token, dev_status, workspace, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? TD_OK : cuda_fail(e);
 }
+
+extern "C" {
+
+td_status td_quantize_q8(td_dtype dtype, const void *x, long long rows, int D, int8_t *codes, float *scales,
+                         void *stream) {
+  if (dtype != TD_F32 && dtype != TD_BF16) return TD_ERR_UNSUPPORTED;
+  if (x == nullptr || codes == nullptr || scales == nullptr || rows < 1 || D < 1) return TD_ERR_INVALID_ARG;
+  if (!aligned4(scales)) return TD_ERR_UNSUPPORTED;
+  const cudaError_t e = td::launch_quantize_q8(elem_size(dtype), x, rows, D, codes, scales,
+                                               static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? TD_OK : cuda_fail(e);
+}
+
+td_status td_kv_append_q8(td_dtype dtype, const void *k_new, const void *v_new, int8_t *k_codes, float *k_scales,
+                          int8_t *v_codes, float *v_scales, int32_t *seq_lens, int B, int Hkv, int T, int Smax, int D,
+                          int advance, uint32_t *dev_status, void *stream) {
+  if (dtype != TD_F32 && dtype != TD_BF16) return TD_ERR_UNSUPPORTED;
+  if (k_new == nullptr || v_new == nullptr || k_codes == nullptr || k_scales == nullptr || v_codes == nullptr ||
+      v_scales == nullptr || seq_lens == nullptr)
+    return TD_ERR_INVALID_ARG;
+  if (B < 1 || Hkv < 1 || T < 1 || Smax < 1 || D < 1) return TD_ERR_INVALID_ARG;
+  if (B > 65535 || !aligned4(seq_lens) || !aligned4(k_scales) || !aligned4(v_scales) ||
+      (dev_status != nullptr && !aligned4(dev_status)))
+    return TD_ERR_UNSUPPORTED;
+  const cudaError_t e = td::launch_append_q8(elem_size(dtype), k_new, v_new, k_codes, k_scales, v_codes, v_scales,
+                                             seq_lens, B, Hkv, T, Smax, D, advance, dev_status,
+                                             static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? TD_OK : cuda_fail(e);
+}
+
+td_status td_verify_attn_q8(const void *q, const int8_t *k_codes, const float *k_scales, const int8_t *v_codes,
+                            const float *v_scales, const int32_t *seq_lens, int B, int Hq, int Hkv, int T, int Smax,
+                            int D, float scale, int split, void *out, float *lse, void *workspace,
+                            size_t workspace_bytes, uint32_t *dev_status, void *stream) {
+  if (k_scales == nullptr || v_scales == nullptr) return TD_ERR_INVALID_ARG;
+  // the scale maps step by whole 16-byte units along a sequence
+  if (Smax % 4 != 0 || !aligned16(k_scales) || !aligned16(v_scales)) return TD_ERR_UNSUPPORTED;
+  td::SplitPlan plan;
+  td::SplitParams p;
+  const td_status st = prepare(TD_BF16, q, k_codes, v_codes, seq_lens, B, Hq, Hkv, T, Smax, D, scale, split, out,
+                               lse, workspace, workspace_bytes, dev_status, &plan, &p, true);
+  if (st != TD_OK) return st;
+  p.k_scales = k_scales;
+  p.v_scales = v_scales;
+  const cudaError_t e = td::launch_split(TD_BF16, D, plan, p, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? TD_OK : cuda_fail(e);
+}
+
+td_status td_decode_attn_q8(const void *q, const int8_t *k_codes, const float *k_scales, const int8_t *v_codes,
+                            const float *v_scales, const int32_t *seq_lens, int B, int Hq, int Hkv, int Smax, int D,
+                            float scale, int split, void *out, float *lse, void *workspace, size_t workspace_bytes,
+                            uint32_t *dev_status, void *stream) {
+  return td_verify_attn_q8(q, k_codes, k_scales, v_codes, v_scales, seq_lens, B, Hq, Hkv, 1, Smax, D, scale, split,
+                           out, lse, workspace, workspace_bytes, dev_status, stream);
+}
+
+}  // extern "C"

@@ -163,6 +163,9 @@ __device__ __forceinline__ const T *map_to_rank(const T *p, uint32_t rank) {
 
 // ---- widening of stored elements to fp32 ----------------------------------------------
 
+__device__ __forceinline__ float widen_elem(float x) { return x; }
+__device__ __forceinline__ float widen_elem(__nv_bfloat16 x) { return __bfloat162float(x); }
+
 // A bf16 value is the upper half of a binary32 value.
 __device__ __forceinline__ void widen_bf16x2(uint32_t w, float &lo, float &hi) {
   lo = __uint_as_float(w << 16);

@@ -23,11 +23,22 @@ struct SplitPlan {
   int smem;      // dynamic shared memory per CTA
   int min_chunk; // smallest automatic chunk (keys)
   int cluster;   // 0: persistent kernel; else CTAs per cluster of the cluster kernel (grid = groups x cluster)
+  bool q8;       // int8 cache (codes + per-row scales): the quantised-cache kernel
   size_t off_part, bytes;  // workspace layout: counters, then partial blocks
 };
 
 // Fills *plan for the current device; TD_OK, or an error for unsupported shapes.
-td_status plan_split(td_dtype dtype, int B, int Hq, int Hkv, int T, int Smax, int D, int split, SplitPlan *plan);
+// q8: the caches hold int8 codes with per-row scales (q and out are bf16; dtype must be TD_BF16).
+td_status plan_split(td_dtype dtype, int B, int Hq, int Hkv, int T, int Smax, int D, int split, SplitPlan *plan,
+                     bool q8 = false);
+
+// Per-row int8 quantisation (codes + fp32 scales) of `rows` rows of D elements.
+cudaError_t launch_quantize_q8(size_t elem_bytes, const void *x, long long rows, int D, int8_t *codes, float *scales,
+                               cudaStream_t stream);
+// Quantises new rows [B, Hkv, T, D] into an int8 cache at seq_lens (td_kv_append's rules).
+cudaError_t launch_append_q8(size_t elem_bytes, const void *k_new, const void *v_new, int8_t *k_codes,
+                             float *k_scales, int8_t *v_codes, float *v_scales, int32_t *seq_lens, int B, int Hkv,
+                             int T, int Smax, int D, int advance, uint32_t *dev_status, cudaStream_t stream);
 
 cudaError_t launch_split(td_dtype dtype, int D, const SplitPlan &plan, const SplitParams &p, cudaStream_t stream);
 

@@ -5,13 +5,14 @@
 #include "td_split_attn.cuh"
 #include "td_split_cluster.cuh"
 #include "td_split_mma.cuh"
+#include "td_split_q8.cuh"
 
 namespace td {
 
 namespace {
 
 constexpr int kMaxDevices = 64;
-constexpr int kKernelSlots = 2 * 2 * 4 + 2 * 2;  // CUDA-core: dtype x D x row padding; mma: D x m tiles
+constexpr int kKernelSlots = 2 * 2 * 4 + 2 * 2 + 2;  // CUDA-core: dtype x D x row padding; mma: D x m tiles; q8: D
 
 struct KernelRef {
   const void *fn;
@@ -107,6 +108,47 @@ KernelRef pick_mma(int D, int MT) {
   if (D == 64) return mma_ref_of<64>();
   if (D == 128) return mma_ref_of<128>();
   return KernelRef{nullptr, 0, nullptr};
+}
+
+// 8-bit caches: 3-D maps over the codes [B*Hkv][Smax][D] (boxes of 64 whole rows, no
+// swizzle) and 2-D maps over the scales [B*Hkv][Smax] (boxes of 64), zero fill outside.
+bool encode_q8_maps(Q8Args *a, const SplitParams &p, int D) {
+  const PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (enc == nullptr) return false;
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const cuuint64_t cdims[3] = {(cuuint64_t)D, (cuuint64_t)p.Smax, (cuuint64_t)p.B * p.Hkv};
+  const cuuint64_t cstrides[2] = {(cuuint64_t)D, (cuuint64_t)p.Smax * D};
+  const cuuint32_t cbox[3] = {(cuuint32_t)D, 64, 1};
+  const cuuint64_t sdims[2] = {(cuuint64_t)p.Smax, (cuuint64_t)p.B * p.Hkv};
+  const cuuint64_t sstrides[1] = {(cuuint64_t)p.Smax * 4};
+  const cuuint32_t sbox[2] = {Q8Cfg<128, 1>::SCALE_BOX, 1};  // 68: a stage's 64 plus the alignment slack
+  const auto code_map = [&](CUtensorMap *m, const void *base) {
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(base), cdims, cstrides, cbox, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  };
+  const auto scale_map = [&](CUtensorMap *m, const float *base) {
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(base), sdims, sstrides, sbox, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  };
+  return code_map(&a->kmap, p.k) && code_map(&a->vmap, p.v) && scale_map(&a->ksmap, p.k_scales) &&
+         scale_map(&a->vsmap, p.v_scales);
+}
+
+template <int D>
+cudaError_t launch_q8(const SplitParams &p, int grid, int smem, cudaStream_t stream) {
+  Q8Args a;
+  if (!encode_q8_maps(&a, p, D)) return cudaErrorInvalidValue;
+  a.p = p;
+  return launch_pdl(split_attn_q8_kernel<D>, dim3(grid), dim3(kThreads), smem, stream, a);
+}
+
+template <int D>
+KernelRef q8_ref_of() {
+  constexpr int smem = Q8Cfg<D, kQ8Stages<D>>::SMEM_BYTES;
+  static_assert(smem + 8704 <= 227 * 1024, "q8 kernel shared memory");
+  return KernelRef{reinterpret_cast<const void *>(&split_attn_q8_kernel<D>), smem, &launch_q8<D>};
 }
 
 template <int D>
@@ -215,7 +257,8 @@ int device_sm_count(int device) {
   return n;
 }
 
-td_status plan_split(td_dtype dtype, int B, int Hq, int Hkv, int T, int Smax, int D, int split, SplitPlan *plan) {
+td_status plan_split(td_dtype dtype, int B, int Hq, int Hkv, int T, int Smax, int D, int split, SplitPlan *plan,
+                     bool q8) {
   if (dtype != TD_F32 && dtype != TD_BF16) return TD_ERR_UNSUPPORTED;
   if (D != 64 && D != 128) return TD_ERR_UNSUPPORTED;
   if (B < 1 || Hq < 1 || Hkv < 1 || T < 1 || Smax < 1 || split < 0 || Hq % Hkv != 0) return TD_ERR_INVALID_ARG;
@@ -241,12 +284,13 @@ td_status plan_split(td_dtype dtype, int B, int Hq, int Hkv, int T, int Smax, in
   }
   const long long RB = (GT + R - 1) / R;
   const long long U = (long long)Hkv * RB;
-  const KernelRef k = pick(dtype, D, mma, variant);
+  if (q8 && !mma) return TD_ERR_UNSUPPORTED;
+  const KernelRef k = q8 ? (D == 64 ? q8_ref_of<64>() : q8_ref_of<128>()) : pick(dtype, D, mma, variant);
   if (k.fn == nullptr) return TD_ERR_UNSUPPORTED;
   int device = 0;
   if (cudaGetDevice(&device) != cudaSuccess) return TD_ERR_CUDA;
   const int sms = device_sm_count(device);
-  const int per_sm = blocks_per_sm(device, slot_of(dtype, D, mma, variant), k);
+  const int per_sm = blocks_per_sm(device, q8 ? 20 + (D == 64 ? 0 : 1) : slot_of(dtype, D, mma, variant), k);
   if (sms <= 0 || per_sm <= 0) return TD_ERR_CUDA;
   // CTAs the automatic split aims to fill. When a kv head's rows fit one row block and the
   // groups are few, leave one slot per group free: the previous call's merging CTAs (one per
@@ -255,7 +299,7 @@ td_status plan_split(td_dtype dtype, int B, int Hq, int Hkv, int T, int Smax, in
   // B = 1: 32k 26.3 -> 25.7 us, 16k 17.75 -> 17.4 us; the two-row-block verify is slower
   // this way, 27.5 -> 28.3 us, and keeps the full grid).
   const long long slots = (long long)sms * per_sm;
-  const bool spare = mma && RB == 1 && (long long)B * U * 4 <= slots;
+  const bool spare = mma && !q8 && RB == 1 && (long long)B * U * 4 <= slots;
   const long long p_target = slots - (spare ? (long long)B * U : 0);
   long long ns;
   if (split > 0) {
@@ -269,6 +313,7 @@ td_status plan_split(td_dtype dtype, int B, int Hq, int Hkv, int T, int Smax, in
   const long long items_max = (long long)B * U * ns;
   if (items_max >= (1LL << 31)) return TD_ERR_UNSUPPORTED;
   plan->mma = mma;
+  plan->q8 = q8;
   plan->RP = variant;
   plan->R = R;
   plan->RB = (int)RB;
@@ -283,7 +328,7 @@ td_status plan_split(td_dtype dtype, int B, int Hq, int Hkv, int T, int Smax, in
   // of clusters of at least two CTAs, about two CTAs per SM: one cluster per group, the
   // largest that fits (its CTAs share the group's keys evenly and merge on chip)
   plan->cluster = 0;
-  if (mma && split == 0) {
+  if (mma && !q8 && split == 0) {
     const long long groups = (long long)B * U;
     for (int cs = kMaxCluster; cs >= 2; cs /= 2) {
       if (groups * cs * 5 < (long long)sms * 8) break;
@@ -304,7 +349,9 @@ td_status plan_split(td_dtype dtype, int B, int Hq, int Hkv, int T, int Smax, in
 
 cudaError_t launch_split(td_dtype dtype, int D, const SplitPlan &plan, const SplitParams &p, cudaStream_t stream) {
   cudaError_t e;
-  if (plan.cluster > 0) {
+  if (plan.q8) {
+    e = D == 64 ? launch_q8<64>(p, plan.grid, plan.smem, stream) : launch_q8<128>(p, plan.grid, plan.smem, stream);
+  } else if (plan.cluster > 0) {
     e = D == 64 ? launch_cluster<64>(p, plan.grid, plan.cluster, stream)
                 : launch_cluster<128>(p, plan.grid, plan.cluster, stream);
   } else {

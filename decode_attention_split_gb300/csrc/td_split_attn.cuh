@@ -63,6 +63,9 @@ struct SplitParams {
   const float *rope_sin;
   int32_t *advance_lens;   // the seq_lens array, to advance by T once every CTA has read it; or null
   int *done;               // grid-wide count of CTAs that have read the lengths (workspace, zero)
+  // 8-bit caches: k and v hold int8 codes, these the fp32 scale of every row [B, Hkv, Smax]
+  const float *k_scales;
+  const float *v_scales;
 };
 
 // Attended length of a sequence whose stored length is `raw`, with the status bits its

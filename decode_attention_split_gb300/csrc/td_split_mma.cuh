@@ -152,6 +152,113 @@ __device__ void place_new_rows(const SplitParams &p, unsigned char *stage, int b
   fence_proxy_async_smem();
 }
 
+// One warp's step over 16 keys of a landed stage (keys key0 .. key0+15, rows kr .. kr+15 of
+// the stage's tiles): S = Q K^T over two 8-key n tiles, masking by the rows' visible-key
+// limits `lim`, the online softmax in base 2, then O += P V. kt / vt address bf16 K / V tiles
+// in the TMA-swizzled layout. For quantised caches, kscale / vscale hold the stage's per-row
+// scales: the key scale multiplies the scores and the value scale multiplies P (the tiles
+// then hold the integer codes); both null for bf16 caches. F16: the tiles and the query
+// fragments hold fp16 instead of bf16 (P is then rounded to fp16).
+template <int D, bool F16 = false>
+__device__ __forceinline__ void warp_keys16(const uint32_t (&qa)[D / 16][4], uint32_t kt, uint32_t vt, int kr,
+                                            int key0, const int (&lim)[2], float qscale, const float *kscale,
+                                            const float *vscale, float (&o)[D / 8][4], float (&m_run)[2],
+                                            float (&l_run)[2]) {
+  constexpr int TK = 64, KSD = D / 16, NTD = D / 8;
+  const int lane = threadIdx.x & 31, tig = lane & 3;
+  float sc[2][4];
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt) {
+    sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+#pragma unroll
+    for (int i = 0; i < KSD / 2; ++i) {
+      uint32_t bk[4];
+      ldmatrix_x4(bk, kt + tma_swz<TK>(kr + nt * 8 + (lane & 7), 4 * i + (lane >> 3)));
+      if (F16) {
+        mma_f16_16816(sc[nt], qa[2 * i], bk[0], bk[1]);
+        mma_f16_16816(sc[nt], qa[2 * i + 1], bk[2], bk[3]);
+      } else {
+        mma_bf16_16816(sc[nt], qa[2 * i], bk[0], bk[1]);
+        mma_bf16_16816(sc[nt], qa[2 * i + 1], bk[2], bk[3]);
+      }
+    }
+  }
+  float ks[2][2], vs[2][2];  // scales of this thread's four keys
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int r = kr + nt * 8 + 2 * tig + e;
+      ks[nt][e] = kscale != nullptr ? kscale[r] * qscale : qscale;
+      vs[nt][e] = vscale != nullptr ? vscale[r] : 1.f;
+    }
+  // scale to base-2 units, mask, online softmax; row half h holds sc[nt][2h], sc[nt][2h+1]
+  float alpha[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    float mx = -INFINITY;
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int key = key0 + nt * 8 + 2 * tig + e;
+        const float v = key < lim[h] ? sc[nt][2 * h + e] * ks[nt][e] : -INFINITY;
+        sc[nt][2 * h + e] = v;
+        mx = fmaxf(mx, v);
+      }
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    const float m_new = fmaxf(m_run[h], mx);
+    const float base = m_new == -INFINITY ? 0.f : m_new;
+    alpha[h] = exp2f(m_run[h] - base);
+    m_run[h] = m_new;
+    float ps = 0.f;
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const float pv = exp2f(sc[nt][2 * h + e] - base);
+        sc[nt][2 * h + e] = pv * vs[nt][e];
+        ps += pv;
+      }
+    l_run[h] = l_run[h] * alpha[h] + ps;
+  }
+  if (__any_sync(0xffffffffu, alpha[0] != 1.f || alpha[1] != 1.f)) {
+#pragma unroll
+    for (int nt = 0; nt < NTD; ++nt) {
+      o[nt][0] *= alpha[0];
+      o[nt][1] *= alpha[0];
+      o[nt][2] *= alpha[1];
+      o[nt][3] *= alpha[1];
+    }
+  }
+  uint32_t pa[4];
+  if (F16) {
+    pa[0] = pack_f16x2(sc[0][0], sc[0][1]);
+    pa[1] = pack_f16x2(sc[0][2], sc[0][3]);
+    pa[2] = pack_f16x2(sc[1][0], sc[1][1]);
+    pa[3] = pack_f16x2(sc[1][2], sc[1][3]);
+  } else {
+    pa[0] = pack_bf16x2(sc[0][0], sc[0][1]);
+    pa[1] = pack_bf16x2(sc[0][2], sc[0][3]);
+    pa[2] = pack_bf16x2(sc[1][0], sc[1][1]);
+    pa[3] = pack_bf16x2(sc[1][2], sc[1][3]);
+  }
+  // O += P V over these 16 keys, two 8-wide output tiles per ldmatrix
+#pragma unroll
+  for (int i = 0; i < NTD / 2; ++i) {
+    uint32_t bv[4];
+    ldmatrix_x4_trans(bv, vt + tma_swz<TK>(kr + (lane & 7) + ((lane >> 3) & 1) * 8, 2 * i + (lane >> 4)));
+    if (F16) {
+      mma_f16_16816(o[2 * i], pa, bv[0], bv[1]);
+      mma_f16_16816(o[2 * i + 1], pa, bv[2], bv[3]);
+    } else {
+      mma_bf16_16816(o[2 * i], pa, bv[0], bv[1]);
+      mma_bf16_16816(o[2 * i + 1], pa, bv[2], bv[3]);
+    }
+  }
+}
+
 // Streams keys [c0, c1) of kv head kvh of sequence b (attended length L) for the query rows
 // of row block rb through the ring at `smem` (1024-byte aligned; NST stages with barriers
 // s_bars; `seq` counts the stages this CTA has consumed, for the barrier parities) and leaves
@@ -279,71 +386,7 @@ __device__ bool stream_chunk(const MmaArgs &a, unsigned char *smem, uint64_t *s_
     if (tid == 0 && st + NST - 1 < nstages) issue(st + NST - 1);
     const int kr = warp * C::TKW;  // first key row (within the stage) of this warp's step
     const int key0 = j0 + kr;
-    if (key0 < c1) {
-      // S = Q K^T over 16 keys: two 8-key n tiles
-      float sc[2][4];
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
-        sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
-#pragma unroll
-        for (int i = 0; i < C::KSD / 2; ++i) {
-          uint32_t bk[4];
-          ldmatrix_x4(bk, kt + tma_swz<C::TK>(kr + nt * 8 + (lane & 7), 4 * i + (lane >> 3)));
-          mma_bf16_16816(sc[nt], qa[2 * i], bk[0], bk[1]);
-          mma_bf16_16816(sc[nt], qa[2 * i + 1], bk[2], bk[3]);
-        }
-      }
-      // scale to base-2 units, mask, online softmax; row half h holds sc[nt][2h], sc[nt][2h+1]
-      float alpha[2];
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        float mx = -INFINITY;
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int key = key0 + nt * 8 + 2 * tig + e;
-            const float v = key < lim[h] ? sc[nt][2 * h + e] * p.qscale : -INFINITY;
-            sc[nt][2 * h + e] = v;
-            mx = fmaxf(mx, v);
-          }
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-        const float m_new = fmaxf(m_run[h], mx);
-        const float base = m_new == -INFINITY ? 0.f : m_new;
-        alpha[h] = exp2f(m_run[h] - base);
-        m_run[h] = m_new;
-        float ps = 0.f;
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const float pv = exp2f(sc[nt][2 * h + e] - base);
-            sc[nt][2 * h + e] = pv;
-            ps += pv;
-          }
-        l_run[h] = l_run[h] * alpha[h] + ps;
-      }
-      if (__any_sync(0xffffffffu, alpha[0] != 1.f || alpha[1] != 1.f)) {
-#pragma unroll
-        for (int nt = 0; nt < C::NTD; ++nt) {
-          o[nt][0] *= alpha[0];
-          o[nt][1] *= alpha[0];
-          o[nt][2] *= alpha[1];
-          o[nt][3] *= alpha[1];
-        }
-      }
-      const uint32_t pa[4] = {pack_bf16x2(sc[0][0], sc[0][1]), pack_bf16x2(sc[0][2], sc[0][3]),
-                              pack_bf16x2(sc[1][0], sc[1][1]), pack_bf16x2(sc[1][2], sc[1][3])};
-      // O += P V over these 16 keys, two 8-wide output tiles per ldmatrix
-#pragma unroll
-      for (int i = 0; i < C::NTD / 2; ++i) {
-        uint32_t bv[4];
-        ldmatrix_x4_trans(bv, vt + tma_swz<C::TK>(kr + (lane & 7) + ((lane >> 3) & 1) * 8, 2 * i + (lane >> 4)));
-        mma_bf16_16816(o[2 * i], pa, bv[0], bv[1]);
-        mma_bf16_16816(o[2 * i + 1], pa, bv[2], bv[3]);
-      }
-    }
+    if (key0 < c1) warp_keys16<D>(qa, kt, vt, kr, key0, lim, p.qscale, nullptr, nullptr, o, m_run, l_run);
     consumed = st + 1;
   }
   if (!ok) {

@@ -26,6 +26,8 @@
  *                  rotation, cache write and split attention.
  *   td_spec_accept the accept/reject step after a verify pass ("tinydecode", "speculative
  *                  decoding"; "FlashSpec", "How it works": Leviathan et al. Algorithm 1).
+ *   td_*_q8        an 8-bit KV cache: int8 codes with one fp32 scale per row (the per-row
+ *                  INT8 scheme "llm-decode-cuda" applies to its weights, for the K/V bytes).
  *
  * Layouts (row-major, contiguous, element type given by td_dtype):
  *   q, out         [B, Hq, D] for decode; [B, Hq, T, D] for verify
@@ -233,6 +235,35 @@ td_status td_spec_accept(const float *target_logits, const float *draft_logits, 
                          const float *uniforms, int B, int G, int V, float temperature, int32_t *n_accepted,
                          int32_t *next_token, void *workspace, size_t workspace_bytes, uint32_t *dev_status,
                          void *stream);
+
+/*
+ * 8-bit KV cache. A row x of D elements is stored as int8 codes and one fp32 scale:
+ *   scale = max_i |x_i| / 127,  code_i = clamp(rint(x_i / scale), -127, 127) (0 when scale == 0),
+ * computed in fp32 with IEEE division and ties to even, and reads back as code_i * scale.
+ * Caches: k_codes, v_codes int8 [B, Hkv, Smax, D]; k_scales, v_scales fp32 [B, Hkv, Smax].
+ */
+
+/* Quantises `rows` rows of D elements of x (TD_F32 or TD_BF16) into codes [rows, D] and scales [rows]. */
+td_status td_quantize_q8(td_dtype dtype, const void *x, long long rows, int D, int8_t *codes, float *scales,
+                         void *stream);
+
+/* td_kv_append for an 8-bit cache: the new rows (dtype TD_F32 or TD_BF16) are quantised into
+ * rows L_b .. L_b+T-1; the same overflow rule, advance and status bit. */
+td_status td_kv_append_q8(td_dtype dtype, const void *k_new, const void *v_new, int8_t *k_codes, float *k_scales,
+                          int8_t *v_codes, float *v_scales, int32_t *seq_lens, int B, int Hkv, int T, int Smax, int D,
+                          int advance, uint32_t *dev_status, void *stream);
+
+/* td_decode_attn / td_verify_attn over an 8-bit cache: the same results as over the cache
+ * the codes stand for (code * scale), q and out bf16, D 64 or 128, Smax a multiple of 4,
+ * scales 16-byte aligned. The workspace is td_decode_workspace_bytes' (which covers it). */
+td_status td_decode_attn_q8(const void *q, const int8_t *k_codes, const float *k_scales, const int8_t *v_codes,
+                            const float *v_scales, const int32_t *seq_lens, int B, int Hq, int Hkv, int Smax, int D,
+                            float scale, int split, void *out, float *lse, void *workspace, size_t workspace_bytes,
+                            uint32_t *dev_status, void *stream);
+td_status td_verify_attn_q8(const void *q, const int8_t *k_codes, const float *k_scales, const int8_t *v_codes,
+                            const float *v_scales, const int32_t *seq_lens, int B, int Hq, int Hkv, int T, int Smax,
+                            int D, float scale, int split, void *out, float *lse, void *workspace,
+                            size_t workspace_bytes, uint32_t *dev_status, void *stream);
 
 /*
  * Decode attention without a workspace argument: the same computation and arguments as
