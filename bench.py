@@ -43,6 +43,7 @@ from decode_attention_split_gb300.workloads import WORKLOADS, kv_read_bytes, mak
 
 METRIC = "decode-attn achieved KV-read GB/s (% of HBM peak) and µs/call, B=1 at 4k–32k ctx"
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
 
 
 def parse():
@@ -330,6 +331,33 @@ def q8_point(td, name, L, dev, l2_bytes, peak, budget_calls=200):
             "bf16_equivalent_gbs": round(bf16_bytes / (us * 1e-6) / 1e9, 1)}
 
 
+def prefill_point(td, dev, T=4096, B=1, Hq=24, Hkv=8, D=128, reps=20):
+    """Causal prefill of a T-token prompt on the tensor cores (a NEXT row): a graph of `reps`
+    launches; FLOPs = 4 * D * Hq * B * T(T+1)/2 (Q K^T and P V over the visible keys)."""
+    g = torch.Generator().manual_seed(3)
+    q = torch.randn(B, Hq, T, D, generator=g).to(torch.bfloat16).to(dev)
+    k = torch.randn(B, Hkv, T, D, generator=g).to(torch.bfloat16).to(dev)
+    v = torch.randn(B, Hkv, T, D, generator=g).to(torch.bfloat16).to(dev)
+    sl = torch.full((B,), T, dtype=torch.int32, device=dev)
+    out = torch.empty_like(q)
+    s = torch.cuda.Stream(dev)
+    with torch.cuda.stream(s):
+        td.td_prefill_attn(q, k, v, sl, out=out, stream=s)
+    s.synchronize()
+    gr = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gr, stream=s):
+        for _ in range(reps):
+            td.td_prefill_attn(q, k, v, sl, out=out, stream=s)
+    ms = min(time_graph(gr, s, 2) for _ in range(3)) / (2 * reps)
+    flops = 4 * D * Hq * B * T * (T + 1) / 2
+    tf = flops / (ms * 1e-3) / 1e12
+    peaks, kind = measured_peaks()
+    peak = float(peaks.get("bf16_tflops", FALLBACK_BF16_TFLOPS))
+    return {"row": "tiled causal prefill (td_prefill_attn, tcgen05)", "B": B, "T": T, "Hq": Hq, "Hkv": Hkv, "D": D,
+            "us_per_call": round(ms * 1e3, 2), "tflops": round(tf, 1), "peak_bf16_tflops": peak,
+            "frac_of_peak": round(tf / peak, 4), "peak_kind": f"bf16_tflops of {kind}"}
+
+
 def sweep_point(td, name, L, dev, l2_bytes, peak, budget_calls=200):
     """Attention kernel alone on one workload point: graph of R launches over rotating caches."""
     w = WORKLOADS[name]
@@ -513,6 +541,7 @@ def run_td(args, world, rank, local):
         sweep.append(sweep_point(td, "verify6", 16390, dev, l2, peak))
         next_rows = [spec_point(td, dev, l2, peak), spec_point(td, dev, l2, peak, B=8)]
         next_rows += [q8_point(td, "llama3b", Ls, dev, l2, peak) for Ls in (4096, 16384, 32768)]
+        next_rows += [prefill_point(td, dev, T=4096), prefill_point(td, dev, T=8192)]
     traffic = recorded_traffic("split_attn_kernel", f"{w.name}:{L}")
     line = {
         "metric": METRIC,

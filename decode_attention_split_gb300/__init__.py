@@ -21,6 +21,7 @@ from .api import (  # noqa: F401
     td_kv_append,
     td_kv_append_q8,
     td_lse_merge,
+    td_prefill_attn,
     td_rope_append_attn,
     td_rope_kv_append,
     td_quantize_q8,

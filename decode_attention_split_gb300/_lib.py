@@ -22,6 +22,7 @@ SYMBOLS = (
     "td_kv_append_q8",
     "td_decode_attn_q8",
     "td_verify_attn_q8",
+    "td_prefill_attn",
     "td_kv_append",
     "td_decode_attn",
     "td_verify_attn",
@@ -70,6 +71,8 @@ def _declare(lib):
     lib.td_decode_attn_q8.restype = i
     lib.td_verify_attn_q8.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp, vp, vp, sz, vp, vp]
     lib.td_verify_attn_q8.restype = i
+    lib.td_prefill_attn.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, f, vp, vp, vp, vp]
+    lib.td_prefill_attn.restype = i
     lib.td_spec_accept.restype = i
     lib.td_kv_append.argtypes = [i, vp, vp, vp, vp, vp, i, i, i, i, i, i, vp, vp]
     lib.td_kv_append.restype = i

@@ -411,3 +411,31 @@ def td_decode_attn_q8(q, k_codes, k_scales, v_codes, v_scales, seq_lens, scale: 
         raise ValueError("q must be [B, Hq, D]")
     return td_verify_attn_q8(q, k_codes, k_scales, v_codes, v_scales, seq_lens, scale, split, out, lse, workspace,
                              dev_status, stream, return_lse)
+
+
+def td_prefill_attn(q, k_cache, v_cache, seq_lens, scale: float | None = None, out=None, lse=None, dev_status=None,
+                    stream=None, return_lse: bool = False):
+    """Causal prefill over the cache: q [B,Hq,T,D] bf16 (seq_lens count the T tokens, whose K/V
+    rows are already written) -> out [B,Hq,T,D] (+ lse [B,Hq,T]); tensor-core tiles."""
+    if q.dim() != 4:
+        raise ValueError("q must be [B, Hq, T, D]")
+    dev = _cuda(q, k_cache, v_cache, seq_lens, out, lse, dev_status)
+    B, Hq, T, D = q.shape
+    _, Hkv, Smax, Dk = k_cache.shape
+    if k_cache.shape[0] != B or Dk != D or v_cache.shape != k_cache.shape:
+        raise ValueError("q and cache shapes disagree")
+    if not (q.dtype == k_cache.dtype == v_cache.dtype == torch.bfloat16):
+        raise TypeError("prefill takes bfloat16 q and caches")
+    if seq_lens.dtype != torch.int32 or seq_lens.shape != (B,):
+        raise TypeError("seq_lens must be int32 [B]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty(B, Hq, T, dtype=torch.float32, device=q.device)
+    with torch.cuda.device(dev):
+        st = lib().td_prefill_attn(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(seq_lens), B, Hq, Hkv, T, Smax, D,
+                                   float(scale), _ptr(out), _ptr(lse), _ptr(dev_status), _stream(stream, dev))
+    check("td_prefill_attn", st)
+    return (out, lse) if (return_lse or lse is not None) else out

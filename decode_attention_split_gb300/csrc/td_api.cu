@@ -306,3 +306,19 @@ td_status td_decode_attn_q8(const void *q, const int8_t *k_codes, const float *k
 }
 
 }  // extern "C"
+
+extern "C" td_status td_prefill_attn(const void *q, const void *k_cache, const void *v_cache, const int32_t *seq_lens,
+                                     int B, int Hq, int Hkv, int T, int Smax, int D, float scale, void *out, float *lse,
+                                     uint32_t *dev_status, void *stream) {
+  if (q == nullptr || k_cache == nullptr || v_cache == nullptr || seq_lens == nullptr || out == nullptr)
+    return TD_ERR_INVALID_ARG;
+  if (B < 1 || Hq < 1 || Hkv < 1 || T < 1 || Smax < 1 || Hq % Hkv != 0 || !isfinite(scale)) return TD_ERR_INVALID_ARG;
+  if ((D != 64 && D != 128) || T > Smax || B > 65535 || Hq > 65535) return TD_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) || !aligned4(seq_lens) ||
+      (lse != nullptr && !aligned4(lse)) || (dev_status != nullptr && !aligned4(dev_status)))
+    return TD_ERR_UNSUPPORTED;
+  const cudaError_t e = td::launch_prefill(q, k_cache, v_cache, seq_lens, B, Hq, Hkv, T, Smax, D, scale, out, lse,
+                                           dev_status, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) cudaGetLastError();
+  return e == cudaSuccess ? TD_OK : cuda_fail(e);
+}

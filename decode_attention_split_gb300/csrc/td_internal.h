@@ -63,6 +63,11 @@ cudaError_t launch_spec_accept(const float *target, const float *draft, const in
                                int B, int G, int V, float temperature, int32_t *n_out, int32_t *tok_out,
                                uint32_t *status, void *workspace, cudaStream_t stream);
 
+// Tiled causal prefill attention on the tensor cores (tcgen05); bf16, D 64 or 128.
+cudaError_t launch_prefill(const void *q, const void *k, const void *v, const int32_t *seq_lens, int B, int Hq, int Hkv,
+                           int T, int Smax, int D, float scale, void *out, float *lse, uint32_t *status,
+                           cudaStream_t stream);
+
 // SM count of the current device (cached per device).
 int device_sm_count(int device);
 

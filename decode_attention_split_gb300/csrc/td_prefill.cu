@@ -1,0 +1,426 @@
+// Tiled causal prefill attention on the fifth-generation tensor cores (tcgen05, TMEM, TMA).
+//
+// Method ("tinydecode": prefill is the causal attention path over the prompt; "llm-decode-cuda"
+// names "a tiled FlashAttention-style kernel" as its next step for prefill): for every query
+// row t of a chunk of T tokens on top of the cache (seq_lens[b] = L counting them), the exact
+// softmax attention over keys j < L - T + t + 1, the same result td_verify_attn defines,
+// computed tile by tile with an online softmax.
+//
+// GB300 design: one CTA (4 warps) per tile of 128 query rows of one query head. Q, K and V
+// tiles cross by TMA with the 128-byte swizzle (K/V double-buffered, 128 keys per tile);
+// one thread issues the tensor-core products, the accumulators live in TMEM:
+//   S[128 x 128] = Q K^T        (A = Q, B = K, both K-major)         -> TMEM columns [0, 128)
+//   O[128 x D]  += P V          (A = P from shared memory, B = V MN-major) -> columns [128, 128 + D)
+// Between the two products every thread owns one query row (its TMEM lane): it reads its S
+// row, masks it causally, and writes P = 2^(s - m) in bf16 into a K-major swizzled tile. The
+// reference maximum m moves only when a row's maximum rises more than 8 (base 2) above it,
+// and only then are that row's O and l rescaled (read, scaled and written back in TMEM);
+// otherwise P stays below 2^8 and O / l, kept against the same m, need no correction.
+// Every wait is bounded; a timeout sets TD_DEV_WAIT_TIMEOUT and the CTA frees its TMEM.
+#include <cudaTypedefs.h>
+#include <math.h>
+
+#include <mutex>
+
+#include "td_device.cuh"
+#include "td_internal.h"
+
+namespace td {
+
+namespace {
+
+constexpr int kPfThreads = 128;
+constexpr int kPfRows = 128;   // query rows per CTA
+constexpr int kPfKeys = 128;   // keys per tile
+constexpr int kRegion = 128 * 128;  // bytes of one swizzled [128 rows][64 bf16] region
+constexpr float kRescaleGap = 8.f;  // base-2 rise of a row maximum before m moves
+
+template <int D>
+struct PfCfg {
+  static constexpr int HALVES = D / 64;                 // 64-column regions per row tile
+  static constexpr int TILE = HALVES * kRegion;         // Q, K or V tile bytes
+  static constexpr int Q_OFF = 0;
+  static constexpr int K_OFF = TILE;                    // two K buffers
+  static constexpr int V_OFF = 3 * TILE;                // two V buffers
+  static constexpr int P_OFF = 5 * TILE;                // P: [128 rows][128 keys] = two regions
+  static constexpr int SMEM = P_OFF + 2 * kRegion + 1024;  // + alignment slack
+  static constexpr int TMEM_COLS = 256;                 // S (128) + O (D), a power of two
+  static_assert(SMEM <= 227 * 1024, "prefill shared memory");
+};
+
+struct PfArgs {
+  CUtensorMap qmap;  // q [B*Hq][T][D]
+  CUtensorMap kmap;  // caches [B*Hkv][Smax][D], boxes of 128 rows
+  CUtensorMap vmap;
+  const int32_t *seq_lens;
+  void *out;         // [B, Hq, T, D] bf16
+  float *lse;        // [B, Hq, T] or null
+  uint32_t *status;
+  int B, Hq, Hkv, T, Smax;
+  float qscale;      // scale * log2(e)
+};
+
+__device__ __forceinline__ void tma3(uint32_t dst, const CUtensorMap *m, int x, int y, int z, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(
+          dst),
+      "l"(m), "r"(x), "r"(y), "r"(z), "r"(bar)
+      : "memory");
+}
+
+// Shared-memory matrix descriptor, 128-byte swizzle: start address, leading and stride byte
+// offsets (K-major: the stride between 8-row groups; MN-major: leading = the stride between
+// 64-column regions, stride = between 8-row groups), descriptor version 1.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((addr & 0x3FFFF) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFF) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFF) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+// kind::f16 instruction descriptor: fp32 accumulator, bf16 A and B, A K-major, B K- or
+// MN-major, M x N.
+__host__ __device__ constexpr uint32_t mma_idesc(int M, int N, bool b_mn_major) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) |
+         ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, bool accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(
+          d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"((uint32_t)accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// 32 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,"
+      "%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
+      "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])), "r"(__float_as_uint(v[3])),
+      "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])), "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])),
+      "r"(__float_as_uint(v[8])), "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+      "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])),
+      "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])),
+      "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
+      "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
+      "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
+      "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+      : "memory");
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// Byte offset of 16-byte chunk c (of 16) of row r in a [128 rows][128 cols] bf16 tile kept
+// as two 128-byte-swizzled regions of 64 columns (the layout TMA writes and the tensor core
+// reads as K-major).
+__device__ __forceinline__ uint32_t tile_chunk(int r, int c) {
+  return (uint32_t)((c >> 3) * kRegion + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+}
+
+template <int D>
+__global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_constant__ PfArgs a) {
+  using C = PfCfg<D>;
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  __shared__ __align__(8) uint64_t bar_q, bar_kv[2], bar_s, bar_o;
+  __shared__ uint32_t s_taddr;
+  __shared__ int s_fail;
+  const int tid = threadIdx.x, warp = tid >> 5;
+  unsigned char *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  const uint32_t sb = smem_u32(smem);
+  const int qt = blockIdx.x, hq = blockIdx.y, b = blockIdx.z;
+  const int G = a.Hq / a.Hkv, kvh = hq / G;
+  const int t0 = qt * kPfRows;
+
+  if (tid == 0) {
+    mbar_init(smem_u32(&bar_q), 1);
+    mbar_init(smem_u32(&bar_kv[0]), 1);
+    mbar_init(smem_u32(&bar_kv[1]), 1);
+    mbar_init(smem_u32(&bar_s), 1);
+    mbar_init(smem_u32(&bar_o), 1);
+    fence_mbar_init();
+    s_fail = 0;
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&s_taddr)),
+                 "n"(C::TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_taddr;
+  const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+  const uint32_t tS = tmem, tO = tmem + kPfKeys;
+
+  griddep_wait();
+  griddep_launch_dependents();
+  const int32_t raw = a.seq_lens[b];
+  const int L = raw < 0 ? 0 : (raw > a.Smax ? a.Smax : raw);
+  // row r (query t = t0 + r) sees keys j < L - T + t + 1
+  const int row = tid;
+  const int t = t0 + row;
+  const bool row_valid = t < a.T;
+  const int lim = row_valid ? max(0, min(L, L - a.T + t + 1)) : 0;
+  const int last_t = min(t0 + kPfRows, a.T) - 1;
+  const int kend = max(0, min(L, L - a.T + last_t + 1));  // keys any row of the tile sees
+  const int nkt = (kend + kPfKeys - 1) / kPfKeys;
+  if (tid == 0 && qt == 0 && hq == 0) {
+    uint32_t bits = 0;
+    if (raw < 0) bits |= TD_DEV_NEGATIVE_SEQLEN;
+    if (raw > a.Smax) bits |= TD_DEV_SEQLEN_CLAMPED;
+    if (a.T > 1 && L < a.T) bits |= TD_DEV_VERIFY_SHORT;
+    report(a.status, bits);
+  }
+
+  const int zq = b * a.Hq + hq, zk = b * a.Hkv + kvh;
+  auto load_kv = [&](int kt) {  // thread 0: key tile kt into buffer kt % 2
+    const int buf = kt & 1;
+    const uint32_t bar = smem_u32(&bar_kv[buf]);
+    mbar_arrive_expect_tx(bar, 2 * C::TILE);
+#pragma unroll
+    for (int h = 0; h < C::HALVES; ++h) {
+      tma3(sb + C::K_OFF + buf * C::TILE + h * kRegion, &a.kmap, 64 * h, kt * kPfKeys, zk, bar);
+      tma3(sb + C::V_OFF + buf * C::TILE + h * kRegion, &a.vmap, 64 * h, kt * kPfKeys, zk, bar);
+    }
+  };
+  if (tid == 0 && nkt > 0) {
+    const uint32_t bar = smem_u32(&bar_q);
+    mbar_arrive_expect_tx(bar, C::TILE);
+#pragma unroll
+    for (int h = 0; h < C::HALVES; ++h) tma3(sb + C::Q_OFF + h * kRegion, &a.qmap, 64 * h, t0, zq, bar);
+    load_kv(0);
+    if (nkt > 1) load_kv(1);
+  }
+
+  constexpr uint32_t kIdS = mma_idesc(kPfRows, kPfKeys, false);
+  constexpr uint32_t kIdO = mma_idesc(kPfRows, D, true);
+  float m_ref = -INFINITY, l = 0.f;
+  bool ok = true;
+  for (int kt = 0; kt < nkt && ok; ++kt) {
+    const int buf = kt & 1;
+    // every thread: this tile's K/V have landed (its V rows past the sequence are zeroed below)
+    bool landed = mbar_wait_bounded(smem_u32(&bar_kv[buf]), (uint32_t)(kt >> 1) & 1u);
+    if (kt == 0) landed = landed && mbar_wait_bounded(smem_u32(&bar_q), 0);
+    if (!__syncthreads_and(landed)) {
+      ok = false;
+      break;
+    }
+    if (tid == 0) {
+      tc_fence_after();
+      // S = Q K^T over D in steps of 16 (32 bytes along a swizzled row; the next 64 columns
+      // are the next region)
+#pragma unroll
+      for (int k = 0; k < D / 16; ++k) {
+        const uint32_t off = (k >> 2) * kRegion + (k & 3) * 32;
+        tc_mma(tS, smem_desc(sb + C::Q_OFF + off, 16, 1024), smem_desc(sb + C::K_OFF + buf * C::TILE + off, 16, 1024),
+               kIdS, k > 0);
+      }
+      tc_commit(smem_u32(&bar_s));
+    }
+    // V rows at or past the sequence's length: zeroed (a masked p of 0 must not meet a stale value)
+    const int vrows = min(kPfKeys, L - kt * kPfKeys);
+    if (vrows < kPfKeys) {
+      unsigned char *vt = smem + C::V_OFF + buf * C::TILE;
+      for (int idx = tid; idx < (kPfKeys - vrows) * (D / 8); idx += kPfThreads) {
+        const int r = vrows + idx / (D / 8), c = idx % (D / 8);
+        *reinterpret_cast<uint4 *>(vt + tile_chunk(r, c)) = make_uint4(0u, 0u, 0u, 0u);
+      }
+      fence_proxy_async_smem();
+    }
+    // the previous P V product must be done before P and O are touched
+    bool done = mbar_wait_bounded(smem_u32(&bar_s), (uint32_t)kt & 1u);
+    if (kt > 0) done = done && mbar_wait_bounded(smem_u32(&bar_o), (uint32_t)(kt - 1) & 1u);
+    if (!__syncthreads_and(done)) {
+      ok = false;
+      break;
+    }
+    tc_fence_after();
+    if (tid == 0 && kt + 1 < nkt && kt >= 1) load_kv(kt + 1);  // buffer (kt+1)&1 is free: P V of kt-1 finished
+    // this row's scores: scaled to base 2, masked causally
+    const int j0 = kt * kPfKeys;
+    float mx = -INFINITY;
+#pragma unroll
+    for (int c = 0; c < kPfKeys; c += 32) {
+      float s[32];
+      tmem_ld32(tS + lane_base + c, s);
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        if (j0 + c + i < lim) mx = fmaxf(mx, s[i] * a.qscale);
+    }
+    const bool move = mx > m_ref + kRescaleGap || (m_ref == -INFINITY && mx > -INFINITY);
+    const float alpha = (move && m_ref != -INFINITY) ? exp2f(m_ref - mx) : 1.f;
+    if (move) {
+      l *= alpha;
+      m_ref = mx;
+    }
+    // TMEM loads and stores are warp-wide: a warp rescales when any of its rows must
+    if (kt > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+      for (int c = 0; c < D; c += 32) {
+        float o[32];
+        tmem_ld32(tO + lane_base + c, o);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) o[i] *= alpha;
+        tmem_st32(tO + lane_base + c, o);
+      }
+    }
+    // P = 2^(s - m) in bf16 into the K-major swizzled P tile (row = this thread's query)
+    const float base = m_ref == -INFINITY ? 0.f : m_ref;
+#pragma unroll
+    for (int c = 0; c < kPfKeys; c += 32) {
+      float s[32];
+      tmem_ld32(tS + lane_base + c, s);
+      uint32_t pk[16];
+#pragma unroll
+      for (int i = 0; i < 32; i += 2) {
+        const float p0 = (j0 + c + i < lim) ? exp2f(s[i] * a.qscale - base) : 0.f;
+        const float p1 = (j0 + c + i + 1 < lim) ? exp2f(s[i + 1] * a.qscale - base) : 0.f;
+        l += p0 + p1;
+        const __nv_bfloat162 v2 = __floats2bfloat162_rn(p0, p1);
+        pk[i / 2] = *reinterpret_cast<const uint32_t *>(&v2);
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        *reinterpret_cast<uint4 *>(smem + C::P_OFF + tile_chunk(row, c / 8 + q)) =
+            make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+    }
+    fence_proxy_async_smem();  // P is read by the tensor core (asynchronous proxy)
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0) {
+      tc_fence_after();
+      // O += P V over the tile's 128 keys in steps of 16: A = P (K-major), B = V (MN-major:
+      // 16 keys = 16 rows of 128 bytes; the next 64 columns are the next region)
+#pragma unroll
+      for (int k = 0; k < kPfKeys / 16; ++k) {
+        tc_mma(tO, smem_desc(sb + C::P_OFF + (k >> 2) * kRegion + (k & 3) * 32, 16, 1024),
+               smem_desc(sb + C::V_OFF + buf * C::TILE + k * 16 * 128, kRegion, 1024), kIdO, kt > 0 || k > 0);
+      }
+      tc_commit(smem_u32(&bar_o));
+    }
+  }
+  if (nkt > 0) {
+    bool done = ok && mbar_wait_bounded(smem_u32(&bar_o), (uint32_t)(nkt - 1) & 1u);
+    if (!__syncthreads_and(done)) ok = false;
+  }
+  if (!ok && tid == 0) report(a.status, TD_DEV_WAIT_TIMEOUT);
+  tc_fence_after();
+  // epilogue: O / l for this row, lse = m + log2(l) (natural-log units); the TMEM loads are
+  // warp-wide, so every thread takes part and only the stores depend on the row
+  const float inv = (ok && l > 0.f) ? 1.f / l : 0.f;
+  __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(a.out) + (((size_t)b * a.Hq + hq) * a.T + (row_valid ? t : 0)) * D;
+#pragma unroll
+  for (int c = 0; c < D; c += 32) {
+    float o[32];
+    if (nkt > 0) {
+      tmem_ld32(tO + lane_base + c, o);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) o[i] = 0.f;
+    }
+    if (row_valid) {
+      uint32_t pk[16];
+#pragma unroll
+      for (int i = 0; i < 32; i += 2) {
+        const __nv_bfloat162 v2 = __floats2bfloat162_rn(o[i] * inv, o[i + 1] * inv);
+        pk[i / 2] = *reinterpret_cast<const uint32_t *>(&v2);
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        reinterpret_cast<uint4 *>(orow + c)[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+    }
+  }
+  if (row_valid && a.lse != nullptr)
+    a.lse[((size_t)b * a.Hq + hq) * a.T + t] = (ok && l > 0.f) ? (m_ref + log2f(l)) * kLn2 : -INFINITY;
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(C::TMEM_COLS) : "memory");
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 pf_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+// 3-D map over [planes][rows][D] bf16, boxes of 64 columns x 128 rows, 128-byte swizzle.
+bool pf_map(CUtensorMap *m, const void *base, long long planes, int rows, int D) {
+  const PFN_cuTensorMapEncodeTiled_v12000 enc = pf_encoder();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)rows, (cuuint64_t)planes};
+  const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)rows * D * 2};
+  const cuuint32_t box[3] = {64, 128, 1};
+  const cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D>
+cudaError_t launch_prefill_d(PfArgs &a, const void *q, const void *k, const void *v, cudaStream_t stream) {
+  if (!pf_map(&a.qmap, q, (long long)a.B * a.Hq, a.T, D) || !pf_map(&a.kmap, k, (long long)a.B * a.Hkv, a.Smax, D) ||
+      !pf_map(&a.vmap, v, (long long)a.B * a.Hkv, a.Smax, D))
+    return cudaErrorInvalidValue;
+  static std::once_flag once;
+  static cudaError_t attr = cudaSuccess;
+  std::call_once(once, [] {
+    attr = cudaFuncSetAttribute(reinterpret_cast<const void *>(&prefill_kernel<D>),
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, PfCfg<D>::SMEM);
+  });
+  if (attr != cudaSuccess) return attr;
+  const dim3 grid((unsigned)((a.T + kPfRows - 1) / kPfRows), (unsigned)a.Hq, (unsigned)a.B);
+  return launch_pdl(prefill_kernel<D>, grid, dim3(kPfThreads), PfCfg<D>::SMEM, stream, a);
+}
+
+}  // namespace
+
+cudaError_t launch_prefill(const void *q, const void *k, const void *v, const int32_t *seq_lens, int B, int Hq, int Hkv,
+                           int T, int Smax, int D, float scale, void *out, float *lse, uint32_t *status,
+                           cudaStream_t stream) {
+  PfArgs a;
+  a.seq_lens = seq_lens;
+  a.out = out;
+  a.lse = lse;
+  a.status = status;
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.T = T;
+  a.Smax = Smax;
+  a.qscale = scale * kLog2e;
+  return D == 64 ? launch_prefill_d<64>(a, q, k, v, stream) : launch_prefill_d<128>(a, q, k, v, stream);
+}
+
+}  // namespace td

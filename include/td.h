@@ -26,6 +26,10 @@
  *                  rotation, cache write and split attention.
  *   td_spec_accept the accept/reject step after a verify pass ("tinydecode", "speculative
  *                  decoding"; "FlashSpec", "How it works": Leviathan et al. Algorithm 1).
+ *   td_prefill_attn  causal attention of a long chunk of T new tokens (a prompt) over the
+ *                  cache: td_verify_attn's result, tiled for the tensor cores (tcgen05)
+ *                  ("llm-decode-cuda" names a tiled FlashAttention-style prefill kernel as
+ *                  its next step; "tinydecode"'s prefill path is causal over the prompt).
  *   td_*_q8        an 8-bit KV cache: int8 codes with one fp32 scale per row (the per-row
  *                  INT8 scheme "llm-decode-cuda" applies to its weights, for the K/V bytes).
  *
@@ -264,6 +268,18 @@ td_status td_verify_attn_q8(const void *q, const int8_t *k_codes, const float *k
                             const float *v_scales, const int32_t *seq_lens, int B, int Hq, int Hkv, int T, int Smax,
                             int D, float scale, int split, void *out, float *lse, void *workspace,
                             size_t workspace_bytes, uint32_t *dev_status, void *stream);
+
+/*
+ * Prefill: query row (hq, t), t < T, attends keys j < L_b - T + t + 1, L_b = seq_lens[b]
+ * clamped to [0, Smax] and counting the T new tokens (whose K/V rows must already be in the
+ * cache): td_verify_attn's definition, for long chunks. bf16 only; D 64 or 128. One CTA per
+ * 128 query rows of one query head; no workspace. q, out [B, Hq, T, D]; lse [B, Hq, T]
+ * (nullable). Status bits as td_verify_attn; a bounded wait that gives up sets
+ * TD_DEV_WAIT_TIMEOUT.
+ */
+td_status td_prefill_attn(const void *q, const void *k_cache, const void *v_cache, const int32_t *seq_lens, int B,
+                          int Hq, int Hkv, int T, int Smax, int D, float scale, void *out, float *lse,
+                          uint32_t *dev_status, void *stream);
 
 /*
  * Decode attention without a workspace argument: the same computation and arguments as
