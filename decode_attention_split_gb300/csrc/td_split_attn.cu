@@ -110,22 +110,23 @@ KernelRef pick_mma(int D, int MT) {
   return KernelRef{nullptr, 0, nullptr};
 }
 
-// 8-bit caches: 3-D maps over the codes [B*Hkv][Smax][D] (boxes of 64 whole rows, no
-// swizzle) and 2-D maps over the scales [B*Hkv][Smax] (boxes of 64), zero fill outside.
+// 8-bit caches: 3-D maps over the codes [B*Hkv][Smax][D] (boxes of 128 whole rows, swizzled
+// over 128-byte rows for D = 128 and 64-byte rows for D = 64) and 2-D maps over the scales
+// [B*Hkv][Smax] (boxes of 132), zero fill outside.
 bool encode_q8_maps(Q8Args *a, const SplitParams &p, int D) {
   const PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
   if (enc == nullptr) return false;
   const cuuint32_t estr[3] = {1, 1, 1};
   const cuuint64_t cdims[3] = {(cuuint64_t)D, (cuuint64_t)p.Smax, (cuuint64_t)p.B * p.Hkv};
   const cuuint64_t cstrides[2] = {(cuuint64_t)D, (cuuint64_t)p.Smax * D};
-  const cuuint32_t cbox[3] = {(cuuint32_t)D, 64, 1};
+  const cuuint32_t cbox[3] = {(cuuint32_t)D, (cuuint32_t)Q8Cfg<128, kQ8Stages<128>>::TK, 1};
   const cuuint64_t sdims[2] = {(cuuint64_t)p.Smax, (cuuint64_t)p.B * p.Hkv};
   const cuuint64_t sstrides[1] = {(cuuint64_t)p.Smax * 4};
-  const cuuint32_t sbox[2] = {Q8Cfg<128, 1>::SCALE_BOX, 1};  // 68: a stage's 64 plus the alignment slack
+  const cuuint32_t sbox[2] = {Q8Cfg<128, kQ8Stages<128>>::SCALE_BOX, 1};  // a stage's rows plus the alignment slack
   const auto code_map = [&](CUtensorMap *m, const void *base) {
     return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(base), cdims, cstrides, cbox, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+               CU_TENSOR_MAP_INTERLEAVE_NONE, D == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
   };
   const auto scale_map = [&](CUtensorMap *m, const float *base) {
     return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(base), sdims, sstrides, sbox, estr,

@@ -427,10 +427,11 @@ __device__ bool stream_chunk(const MmaArgs &a, unsigned char *smem, uint64_t *s_
   return ok;
 }
 
-// Warms L2 with the first `n` stages of K and V of keys [c0, c1) of (b, kvh).
-template <int D>
+// Warms L2 with the first `n` stages (of 64 rows) of K and V of keys [c0, c1) of (b, kvh):
+// bf16 rows, or for 8-bit caches (Q8) the code rows and their scales.
+template <int D, bool Q8 = false>
 __device__ void prefetch_chunk_l2(const SplitParams &p, int b, int kvh, int c0, int c1, int n) {
-  constexpr int ROWB = D * 2, TK = 64;
+  constexpr int ROWB = Q8 ? D : D * 2, TK = 64;
   const size_t row0 = ((size_t)b * p.Hkv + kvh) * p.Smax + c0;
   const unsigned char *k = static_cast<const unsigned char *>(p.k) + row0 * ROWB;
   const unsigned char *v = static_cast<const unsigned char *>(p.v) + row0 * ROWB;
@@ -441,6 +442,17 @@ __device__ void prefetch_chunk_l2(const SplitParams &p, int b, int kvh, int c0, 
     prefetch_l2_bulk(k + (size_t)r * ROWB, bytes);
     prefetch_l2_bulk(v + (size_t)r * ROWB, bytes);
   }
+  if constexpr (Q8) {
+    // the whole 16-byte units holding the rows' scales (a sequence's Smax scales are a whole
+    // number of 16-byte units, so these stay inside its own)
+    const float *sc[2] = {p.k_scales + row0, p.v_scales + row0};
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const uintptr_t a0 = reinterpret_cast<uintptr_t>(sc[i]) & ~(uintptr_t)15;
+      const uintptr_t a1 = (reinterpret_cast<uintptr_t>(sc[i] + rows) + 15) & ~(uintptr_t)15;
+      prefetch_l2_bulk(reinterpret_cast<const void *>(a0), (uint32_t)(a1 - a0));
+    }
+  }
 }
 
 // Run by one thread before the wait for the previous kernel in the stream, whose writes
@@ -449,7 +461,7 @@ __device__ void prefetch_chunk_l2(const SplitParams &p, int b, int kvh, int c0, 
 // check, and an L2 prefetch of that chunk's first `n` stages, so the HBM latency of the
 // first stages overlaps the previous kernel's tail. A hint only: a wrong guess wastes a
 // prefetch, and the real plan is made after the wait. Batches of up to 8 sequences.
-template <int D>
+template <int D, bool Q8 = false>
 __device__ void prefetch_first_item(const SplitParams &p, int n) {
   if (p.B > 8) return;
   long long all = 0;
@@ -471,7 +483,7 @@ __device__ void prefetch_first_item(const SplitParams &p, int n) {
     if (item < NC * U) {
       const int c = item % NC, kvh = item / NC / p.RB;
       const int c0 = c * S;
-      prefetch_chunk_l2<D>(p, b, kvh, c0, min(c0 + S, L), n);
+      prefetch_chunk_l2<D, Q8>(p, b, kvh, c0, min(c0 + S, L), n);
       return;
     }
     item -= NC * U;

@@ -6,15 +6,24 @@
 // scheme "llm-decode-cuda" applies to its weights, read here for the K/V bytes that bound
 // the decode step): a row reads back as code * scale.
 //
-// GB300 design: the bytes streamed from HBM halve. Stages of 64 rows cross by TMA as int8
-// tiles plus their 64 + 64 scales (tensor maps with zero fill past Smax). Each stage is
-// widened once, in shared memory, into the 16-bit tile layout the tensor-core step reads. The
-// step runs in fp16 here: an int8 code becomes an fp16 value exactly with one byte permute
-// and half a packed subtraction per value (bf16's 8 significant bits leave no such trick),
-// and the query is rounded to fp16 once per item. The scales are not applied to the tiles:
-// the key scale multiplies each score and the value scale multiplies each probability
-// before the P V product (warp_keys16). Everything else (planning, chunking, the fused
-// merge) is the persistent kernel's.
+// GB300 design: the bytes streamed from HBM halve. Stages of 128 rows cross by TMA as int8
+// tiles (with the 128-byte swizzle for 128-byte rows, the 64-byte one for 64-byte rows) plus
+// their scales (tensor maps with zero fill past Smax); each of the 4 warps takes 32 keys of a
+// stage. The tensor-core step runs in fp16 and takes its B operands straight from the int8
+// tiles: ldmatrix moves 16-bit words (two codes), and in registers one byte permute places a
+// code c (sign bit flipped: c + 128) under the exponent byte 0x64, which reads as the exact
+// fp16 value 1152 + c. The constant 1152 is not subtracted per value: it adds 1152 * sum(q)
+// to every score of a query row and 1152 * sum(p) to every output of a row, and both are
+// taken off afterwards from products of the same operands with a tile of 1152s (an fp32
+// cancellation of about 2^-24 * 1279 * sum|q| per score, far below the query's own rounding
+// to fp16). bf16's 8 significant bits leave no such trick. For the scores the order of the
+// head dimensions is free: each thread's four dims are whichever four consecutive codes its
+// word holds, and the query fragments (fp16, exact for bf16 queries) take the same order.
+// For P V the transposed load gives each thread two adjacent output dims of two keys: the
+// even dims form one 8-wide output tile and the odd dims another, put back in order when the
+// partial results are written. The scales are not applied to the codes: the key scale
+// multiplies each score and the value scale each probability before the P V product.
+// Everything else (planning, chunking, the fused merge) is the persistent kernel's.
 #pragma once
 
 #include "td_split_mma.cuh"
@@ -24,24 +33,38 @@ namespace td {
 template <int D, int NST_>
 struct Q8Cfg {
   static constexpr int NST = NST_;
-  static constexpr int TK = 64;
+  static constexpr int TK = 128;                               // keys per stage, 32 per warp
   static constexpr int CODE_BYTES = TK * D;                    // one int8 tile
+  static constexpr int CODES_STAGE = 2 * CODE_BYTES;           // K then V codes
   // the scales of a stage's rows are fetched from the 16-byte boundary at or below its first
-  // row (a TMA load's inner coordinate must be 16-byte aligned): 68 values, the stage's 64
+  // row (a TMA load's inner coordinate must be 16-byte aligned): TK + 4 values, the stage's
   // starting at index (first row & 3)
   static constexpr int SCALE_BOX = TK + 4;
-  static constexpr int SCALE_SLOT = 384;                       // bytes kept per scale box (128-aligned)
-  static constexpr int STAGE_BYTES = 2 * CODE_BYTES + 2 * SCALE_SLOT;  // K, V codes, then K, V scales
-  static constexpr int RING_BYTES = NST * STAGE_BYTES;
-  static constexpr int WORK_BYTES = 2 * TK * D * 2;            // the widened bf16 K and V tiles
-  static constexpr int WORK_OFF = (RING_BYTES + 1023) / 1024 * 1024;
-  static constexpr int SMEM_BYTES = WORK_OFF + WORK_BYTES + 1024;  // + alignment slack
-  static_assert(CODE_BYTES % 128 == 0, "tiles keep 128-byte alignment");
-  static_assert(kWarps * kMmaRows * (D + 2) * 4 <= WORK_OFF + WORK_BYTES, "combine area fits");
+  static constexpr int SCALE_SLOT = 640;                       // bytes kept per scale box (128-aligned)
+  static constexpr int SCALE_OFF = NST * CODES_STAGE;          // K, V scale slots of every stage
+  static constexpr int RING_BYTES = SCALE_OFF + NST * 2 * SCALE_SLOT;
+  static constexpr int SMEM_BYTES = RING_BYTES + 1024;         // + alignment slack
+  static_assert(CODE_BYTES % 1024 == 0, "code tiles keep the swizzle's 1024-byte alignment");
+  static_assert(SCALE_BOX * 4 <= SCALE_SLOT && (SCALE_BOX * 4) % 16 == 0, "scale box");
+  static_assert(kWarps * kMmaRows * (D + 2) * 4 <= RING_BYTES, "combine area fits");
 };
 
+// Ring depth: two CTAs per SM, NST - 1 stages in flight while one is read.
 template <int D>
-constexpr int kQ8Stages = 4;
+constexpr int kQ8Stages = D == 128 ? 3 : 6;
+
+// Byte offset of 16-byte chunk `ch` of row `row` in an int8 tile of D-byte rows as the TMA
+// unit writes it: 128-byte swizzle for D = 128 (chunk c ^ (row & 7)), 64-byte swizzle for
+// D = 64 (chunk c ^ ((row >> 1) & 3)); either way the 8 rows one ldmatrix reads fall in 8
+// different bank groups.
+template <int D>
+__device__ __forceinline__ uint32_t q8_swz(int row, int ch) {
+  if constexpr (D == 128) {
+    return (uint32_t)(row * 128 + ((ch ^ (row & 7)) << 4));
+  } else {
+    return (uint32_t)(row * 64 + ((ch ^ ((row >> 1) & 3)) << 4));
+  }
+}
 
 struct Q8Args {
   CUtensorMap kmap, vmap;    // int8 codes [B*Hkv][Smax][D]
@@ -58,52 +81,139 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
       : "memory");
 }
 
-// Sixteen int8 codes -> sixteen fp16 values, exactly: with the sign bit flipped a code c is
-// the byte c + 128; placed under the exponent byte 0x64 it forms the fp16 value 1024 + c + 128,
-// and one packed subtraction of 1152 leaves c (two values per instruction).
-__device__ __forceinline__ void widen_codes16(const uint4 v, uint4 &lo, uint4 &hi) {
-  const uint32_t w[4] = {v.x ^ 0x80808080u, v.y ^ 0x80808080u, v.z ^ 0x80808080u, v.w ^ 0x80808080u};
-  const __half2 bias = __halves2half2(__ushort_as_half((unsigned short)0x6480), __ushort_as_half((unsigned short)0x6480));
-  uint32_t out[8];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const uint32_t a = __byte_perm(w[i], 0x64646464u, 0x4140);  // bytes 0, 1 under 0x64
-    const uint32_t b = __byte_perm(w[i], 0x64646464u, 0x4342);  // bytes 2, 3
-    const __half2 ha = __hsub2(*reinterpret_cast<const __half2 *>(&a), bias);
-    const __half2 hb = __hsub2(*reinterpret_cast<const __half2 *>(&b), bias);
-    out[2 * i] = *reinterpret_cast<const uint32_t *>(&ha);
-    out[2 * i + 1] = *reinterpret_cast<const uint32_t *>(&hb);
-  }
-  lo = make_uint4(out[0], out[1], out[2], out[3]);
-  hi = make_uint4(out[4], out[5], out[6], out[7]);
+// Two int8 codes of a word (sign bits already flipped) -> the fp16 values 1152 + code: `sel`
+// places the chosen bytes under the exponent byte 0x64.
+__device__ __forceinline__ uint32_t codes_f16x2(uint32_t flipped, uint32_t sel) {
+  return __byte_perm(flipped, 0x64646464u, sel);
 }
+constexpr uint32_t kFlip = 0x80808080u;
+constexpr uint32_t kF16x2_1152 = 0x64806480u;           // two fp16 1152s
+constexpr uint32_t kSelB01 = 0x4140, kSelB23 = 0x4342;  // bytes 0, 1 / bytes 2, 3
+constexpr uint32_t kSelB02 = 0x4240, kSelB13 = 0x4341;  // bytes 0, 2 / bytes 1, 3
 
-// Eight bf16 values -> eight fp16 values (rounded to nearest even; exact for queries whose
-// magnitudes lie in fp16's normal range).
-__device__ __forceinline__ uint4 bf16x8_to_f16x8(const uint4 v) {
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-  uint32_t out[4];
+// One warp's step over 32 keys (rows kr .. kr+31 of the stage's code tiles kt / vt; keys
+// key0 ..): S = Q K^T with the key scales, online softmax in base 2, then
+// O += (P * value scale) V, where O and `ob` (the rows' 1152 * sum(p) terms) both carry the
+// code bias. qb: the rows' score bias 1152 * sum(q), the scores' starting value negated;
+// qscale = scale * log2(e) multiplies each key scale. ks / vs point at the
+// stage's scales (index = row in the stage). MASK: some key of the step lies at or past a
+// row's limit `lim` or the sequence's end `kend` (otherwise no key is masked: rows that do
+// not exist compute finite values nobody reads). Fragment orders (mma m16n8k16, g = lane / 4, c = lane % 4):
+//  - scores: ldmatrix gives thread (g, c) codes 4c .. 4c+3 of a 16-dim block of key g; the
+//    k slots 2c, 2c+1, 2c+8, 2c+9 hold those four dims, and so do the query fragments;
+//  - P V: the transposed ldmatrix gives thread (g, c) dims 2g, 2g+1 of keys 2c, 2c+1; o[2j]
+//    takes the even dims of 16-dim block j and o[2j+1] the odd ones, so thread (g, c) holds
+//    dims 16j + 4c .. 16j + 4c + 3 of its rows as o[2j][0], o[2j+1][0], o[2j][1], o[2j+1][1].
+template <int D, bool MASK>
+__device__ __forceinline__ void warp_keys32_q8(const uint32_t (&qa)[D / 16][4], const float (&qb)[2], uint32_t kt,
+                                               uint32_t vt, int kr, int key0, int kend, const int (&lim)[2],
+                                               float qscale, const float *ks, const float *vs, float (&o)[D / 8][4],
+                                               float (&ob)[4], float (&m_run)[2], float (&l_run)[2]) {
+  constexpr int NX = D / 32;  // ldmatrix.x4 per 16 keys: 16 keys x 32 dims
+  const int lane = threadIdx.x & 31, tig = lane & 3;
+  const int lrow = kr + (lane & 7) + ((lane >> 3) & 1) * 8, lch = lane >> 4;
+  float sc[4][4];  // n tiles of 8 keys, starting from minus the rows' score bias
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w[i]));
-    out[i] = pack_f16x2(f.x, f.y);
+  for (int nt = 0; nt < 4; ++nt) {
+    sc[nt][0] = sc[nt][1] = -qb[0];
+    sc[nt][2] = sc[nt][3] = -qb[1];
   }
-  return make_uint4(out[0], out[1], out[2], out[3]);
+#pragma unroll
+  for (int hf = 0; hf < 2; ++hf)
+#pragma unroll
+    for (int i = 0; i < NX; ++i) {
+      uint32_t r[4];  // keys 0-7 / 8-15 of dims 32i .. 32i+15, then of dims 32i+16 .. 32i+31
+      ldmatrix_x4(r, kt + q8_swz<D>(lrow + 16 * hf, 2 * i + lch));
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const uint32_t f = r[e] ^ kFlip;
+        mma_f16_16816(sc[2 * hf + (e & 1)], qa[2 * i + (e >> 1)], codes_f16x2(f, kSelB01), codes_f16x2(f, kSelB23));
+      }
+    }
+  float kss[4][2], vss[4][2];  // scales of this thread's eight keys
+#pragma unroll
+  for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int r = kr + nt * 8 + 2 * tig + e;
+      kss[nt][e] = ks[r] * qscale;
+      // keys past the sequence: a stale scale must not meet a zero probability
+      vss[nt][e] = !MASK || key0 + nt * 8 + 2 * tig + e < kend ? vs[r] : 0.f;
+    }
+  float alpha[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    float mx = -INFINITY;
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int key = key0 + nt * 8 + 2 * tig + e;
+        const float v = !MASK || key < lim[h] ? sc[nt][2 * h + e] * kss[nt][e] : -INFINITY;
+        sc[nt][2 * h + e] = v;
+        mx = fmaxf(mx, v);
+      }
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    const float m_new = fmaxf(m_run[h], mx);
+    const float base = m_new == -INFINITY ? 0.f : m_new;
+    alpha[h] = exp2_approx(m_run[h] - base);
+    m_run[h] = m_new;
+    float ps = 0.f;
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const float pv = exp2_approx(sc[nt][2 * h + e] - base);
+        sc[nt][2 * h + e] = pv * vss[nt][e];
+        ps += pv;
+      }
+    l_run[h] = l_run[h] * alpha[h] + ps;
+  }
+  if (__any_sync(0xffffffffu, alpha[0] != 1.f || alpha[1] != 1.f)) {
+#pragma unroll
+    for (int nt = 0; nt < D / 8; ++nt) {
+      o[nt][0] *= alpha[0];
+      o[nt][1] *= alpha[0];
+      o[nt][2] *= alpha[1];
+      o[nt][3] *= alpha[1];
+    }
+    ob[0] *= alpha[0];
+    ob[1] *= alpha[0];
+    ob[2] *= alpha[1];
+    ob[3] *= alpha[1];
+  }
+#pragma unroll
+  for (int hf = 0; hf < 2; ++hf) {
+    const uint32_t pa[4] = {pack_f16x2(sc[2 * hf][0], sc[2 * hf][1]), pack_f16x2(sc[2 * hf][2], sc[2 * hf][3]),
+                            pack_f16x2(sc[2 * hf + 1][0], sc[2 * hf + 1][1]),
+                            pack_f16x2(sc[2 * hf + 1][2], sc[2 * hf + 1][3])};
+    mma_f16_16816(ob, pa, kF16x2_1152, kF16x2_1152);
+#pragma unroll
+    for (int i = 0; i < NX; ++i) {
+      uint32_t r[4];  // transposed: keys 0-7 / 8-15 of dims 32i .. 32i+15, then of 32i+16 ..
+      ldmatrix_x4_trans(r, vt + q8_swz<D>(lrow + 16 * hf, 2 * i + lch));
+#pragma unroll
+      for (int d2 = 0; d2 < 2; ++d2) {
+        const uint32_t lo = r[2 * d2] ^ kFlip, hi = r[2 * d2 + 1] ^ kFlip;
+        const int j = 2 * i + d2;  // 16-dim block
+        mma_f16_16816(o[2 * j], pa, codes_f16x2(lo, kSelB02), codes_f16x2(hi, kSelB02));
+        mma_f16_16816(o[2 * j + 1], pa, codes_f16x2(lo, kSelB13), codes_f16x2(hi, kSelB13));
+      }
+    }
+  }
 }
 
 // Streams keys [c0, c1) of (b, kvh) for row block rb, as stream_chunk does for bf16 caches,
 // leaving the same combine area (at the start of `smem`).
 template <int D, int NST>
-__device__ bool stream_chunk_q8(const Q8Args &a, unsigned char *smem, uint64_t *s_bars, float *s_ks, float *s_vs,
-                                uint32_t &seq, int b, int kvh, int rb, int L, int c0, int c1) {
+__device__ bool stream_chunk_q8(const Q8Args &a, unsigned char *smem, uint64_t *s_bars, uint32_t &seq, int b, int kvh,
+                                int rb, int L, int c0, int c1) {
   using C = Q8Cfg<D, NST>;
-  constexpr int NCH = D * 2 / 16;  // 16-byte chunks per bf16 row
   const SplitParams &p = a.p;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int gid = lane >> 2;
+  const int gid = lane >> 2, tig = lane & 3;
   const uint32_t sbase = smem_u32(smem);
-  unsigned char *work = smem + C::WORK_OFF;
-  const uint32_t kt = sbase + C::WORK_OFF, vt = kt + C::TK * D * 2;
   const int GT = p.G * p.T;
   const int nstages = (c1 - c0 + C::TK - 1) / C::TK;
   const int zc = b * p.Hkv + kvh;
@@ -112,30 +222,24 @@ __device__ bool stream_chunk_q8(const Q8Args &a, unsigned char *smem, uint64_t *
   auto issue = [&](int sidx) {
     const int buf = (seq + sidx) % NST;
     const uint32_t bar = smem_u32(&s_bars[buf]);
-    const uint32_t dst = sbase + buf * C::STAGE_BYTES;
+    const uint32_t dst = sbase + buf * C::CODES_STAGE;
+    const uint32_t sdst = sbase + C::SCALE_OFF + buf * 2 * C::SCALE_SLOT;
     const int y = c0 + sidx * C::TK;
     fence_proxy_async_smem();
-    mbar_arrive_expect_tx(bar, 2 * C::CODE_BYTES + 2 * C::SCALE_BOX * 4);
+    mbar_arrive_expect_tx(bar, C::CODES_STAGE + 2 * C::SCALE_BOX * 4);
     tma_load_3d(dst, &a.kmap, 0, y, zc, bar, policy);
     tma_load_3d(dst + C::CODE_BYTES, &a.vmap, 0, y, zc, bar, policy);
-    tma_load_2d(dst + 2 * C::CODE_BYTES, &a.ksmap, y & ~3, zc, bar, policy);
-    tma_load_2d(dst + 2 * C::CODE_BYTES + C::SCALE_SLOT, &a.vsmap, y & ~3, zc, bar, policy);
+    tma_load_2d(sdst, &a.ksmap, y & ~3, zc, bar, policy);
+    tma_load_2d(sdst + C::SCALE_SLOT, &a.vsmap, y & ~3, zc, bar, policy);
   };
-  // the query rows, as fp16, go to the work K tile, read into registers before the first
-  // widening
-  for (int idx = tid; idx < kMmaRows * NCH; idx += kThreads) {
-    const int r = idx / NCH, ch = idx % NCH;
-    const int gr = rb * p.R + r;
-    uint4 v = make_uint4(0u, 0u, 0u, 0u);
-    if (r < p.R && gr < GT) {
-      const int hq = kvh * p.G + gr / p.T, t = gr % p.T;
-      v = bf16x8_to_f16x8(static_cast<const uint4 *>(p.q)[(((size_t)b * p.Hq + hq) * p.T + t) * NCH + ch]);
-    }
-    *reinterpret_cast<uint4 *>(work + swz<D * 2>(r, ch)) = v;
-  }
   if (tid == 0) {
-    for (int s2 = 0; s2 < min(NST, nstages); ++s2) issue(s2);
+    for (int s2 = 0; s2 < min(NST - 1, nstages); ++s2) issue(s2);
   }
+  // query rows gid and gid + 8 of this row block as fp16 A fragments (exact: a bf16 value in
+  // fp16's range is an fp16 value; the scale stays out of them, its product would round),
+  // dims in the order the key fragments take (slots 2c, 2c+1 <- dims 4c, 4c+1; slots 2c+8,
+  // 2c+9 <- dims 4c+2, 4c+3)
+  uint32_t qa[D / 16][4];
   int lim[2];
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
@@ -143,9 +247,31 @@ __device__ bool stream_chunk_q8(const Q8Args &a, unsigned char *smem, uint64_t *
     const int gr = rb * p.R + r;
     const bool valid = r < p.R && gr < GT;
     lim[h] = valid ? min(max(L - p.T + gr % p.T + 1, 0), c1) : 0;
+    const int hq = kvh * p.G + (valid ? gr / p.T : 0), t = valid ? gr % p.T : 0;
+    const uint2 *qrow = reinterpret_cast<const uint2 *>(static_cast<const __nv_bfloat16 *>(p.q) +
+                                                        (((size_t)b * p.Hq + hq) * p.T + t) * D);
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+      uint2 w = valid ? qrow[ks * 4 + tig] : make_uint2(0u, 0u);
+      const float2 lo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w.x));
+      const float2 hi = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w.y));
+      qa[ks][h] = pack_f16x2(lo.x, lo.y);
+      qa[ks][2 + h] = pack_f16x2(hi.x, hi.y);
+    }
   }
-  uint32_t qa[D / 16][4];
-  float o[D / 8][4];
+  // the rows' score bias 1152 * sum(q), from the same fragments
+  float qb[2];
+  {
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) mma_f16_16816(acc, qa[ks], kF16x2_1152, kF16x2_1152);
+    qb[0] = acc[0];
+    qb[1] = acc[2];
+  }
+  // keys every existing row of the block sees (a warp-uniform bound for the unmasked step)
+  int lim_all = c1;
+  for (int r = 0; r < min(p.R, GT - rb * p.R); ++r) lim_all = min(lim_all, max(L - p.T + (rb * p.R + r) % p.T + 1, 0));
+  float o[D / 8][4], ob[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
   for (int nt = 0; nt < D / 8; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
   float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
@@ -155,50 +281,30 @@ __device__ bool stream_chunk_q8(const Q8Args &a, unsigned char *smem, uint64_t *
   for (int st = 0; st < nstages; ++st) {
     const int buf = (seq + st) % NST;
     const bool landed = mbar_wait_bounded(smem_u32(&s_bars[buf]), ((seq + st) / NST) & 1u);
-    // every warp has finished the previous stage with the work tiles; one decision for all
+    // every warp has finished the previous stage, whose buffer is refilled next; one decision
+    // for the whole CTA
     if (!__syncthreads_and(landed)) {
       ok = false;
       break;
     }
-    if (st == 0) {
-#pragma unroll
-      for (int j = 0; j < D / 16; ++j)
-        ldmatrix_x4(qa[j], kt + swz<D * 2>(((lane >> 3) & 1) * 8 + (lane & 7), 2 * j + (lane >> 4)));
-      __syncthreads();  // the query tile is read before the work tiles are overwritten
-    }
+    if (tid == 0 && st + NST - 1 < nstages) issue(st + NST - 1);
     const int j0 = c0 + st * C::TK;
-    const int valid = min(C::TK, c1 - j0);
-    // widen this stage's codes into the work tiles (value rows past the chunk: zero)
-    const unsigned char *k8 = smem + buf * C::STAGE_BYTES;
-    const unsigned char *v8 = k8 + C::CODE_BYTES;
-    for (int idx = tid; idx < 2 * C::TK * (D / 16); idx += kThreads) {
-      const bool isv = idx >= C::TK * (D / 16);
-      const int i = isv ? idx - C::TK * (D / 16) : idx;
-      const int r = i / (D / 16), c = i % (D / 16);
-      uint4 lo, hi;
-      if (isv && r >= valid) {
-        lo = hi = make_uint4(0u, 0u, 0u, 0u);
-      } else {
-        widen_codes16(*reinterpret_cast<const uint4 *>((isv ? v8 : k8) + r * D + c * 16), lo, hi);
-      }
-      unsigned char *tile = work + (isv ? C::TK * D * 2 : 0);
-      *reinterpret_cast<uint4 *>(tile + tma_swz<C::TK>(r, 2 * c)) = lo;
-      *reinterpret_cast<uint4 *>(tile + tma_swz<C::TK>(r, 2 * c + 1)) = hi;
-    }
-    if (tid < 2 * C::TK) {
-      const bool isv = tid >= C::TK;
-      const float *sc = reinterpret_cast<const float *>(k8 + 2 * C::CODE_BYTES + (isv ? C::SCALE_SLOT : 0));
-      (isv ? s_vs : s_ks)[tid % C::TK] = sc[(j0 & 3) + tid % C::TK];
-    }
-    __syncthreads();  // work tiles and scales ready; this ring buffer is free
-    if (tid == 0 && st + NST < nstages) issue(st + NST);
-    const int kr = warp * 16;
+    const int kr = warp * 32;
     const int key0 = j0 + kr;
-    if (key0 < c1) warp_keys16<D, true>(qa, kt, vt, kr, key0, lim, p.qscale, s_ks, s_vs, o, m_run, l_run);
+    if (key0 < c1) {
+      const uint32_t kt = sbase + buf * C::CODES_STAGE;
+      const float *scl = reinterpret_cast<const float *>(smem + C::SCALE_OFF + buf * 2 * C::SCALE_SLOT) + (j0 & 3);
+      if (key0 + 32 <= lim_all)
+        warp_keys32_q8<D, false>(qa, qb, kt, kt + C::CODE_BYTES, kr, key0, L, lim, p.qscale, scl,
+                                 scl + C::SCALE_SLOT / 4, o, ob, m_run, l_run);
+      else
+        warp_keys32_q8<D, true>(qa, qb, kt, kt + C::CODE_BYTES, kr, key0, L, lim, p.qscale, scl,
+                                scl + C::SCALE_SLOT / 4, o, ob, m_run, l_run);
+    }
     consumed = st + 1;
   }
   if (!ok) {
-    const int issued = min(nstages, consumed + NST);
+    const int issued = min(nstages, consumed + NST - 1);
     for (int st = consumed; st < issued; ++st)
       mbar_wait_bounded(smem_u32(&s_bars[(seq + st) % NST]), ((seq + st) / NST) & 1u);
     if (tid == 0) report(p.status, TD_DEV_WAIT_TIMEOUT);
@@ -211,12 +317,11 @@ __device__ bool stream_chunk_q8(const Q8Args &a, unsigned char *smem, uint64_t *
     l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 1);
     l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 2);
   }
-  __syncthreads();  // ring and work tiles idle: reuse them as the combine area
+  __syncthreads();  // ring idle: reuse it as the combine area
   float *combine = reinterpret_cast<float *>(smem);
   float *cm = combine;
   float *cl = combine + kWarps * kMmaRows;
   float *ca = combine + 2 * kWarps * kMmaRows;
-  const int tig = lane & 3;
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     const int r = gid + 8 * h;
@@ -224,10 +329,12 @@ __device__ bool stream_chunk_q8(const Q8Args &a, unsigned char *smem, uint64_t *
       cm[warp * kMmaRows + r] = m_run[h];
       cl[warp * kMmaRows + r] = l_run[h];
     }
+    const float bias = ob[2 * h];  // 1152 * sum(p) of row r: the code bias in every output
 #pragma unroll
-    for (int nt = 0; nt < D / 8; ++nt)
-      *reinterpret_cast<float2 *>(&ca[(warp * kMmaRows + r) * D + nt * 8 + 2 * tig]) =
-          make_float2(o[nt][2 * h], o[nt][2 * h + 1]);
+    for (int j = 0; j < D / 16; ++j)
+      *reinterpret_cast<float4 *>(&ca[(warp * kMmaRows + r) * D + 16 * j + 4 * tig]) =
+          make_float4(o[2 * j][2 * h] - bias, o[2 * j + 1][2 * h] - bias, o[2 * j][2 * h + 1] - bias,
+                      o[2 * j + 1][2 * h + 1] - bias);
   }
   __syncthreads();
   return ok;
@@ -240,7 +347,7 @@ __global__ void __launch_bounds__(kThreads, 2) split_attn_q8_kernel(const __grid
   constexpr int NST = kQ8Stages<D>;
   using C = Q8Cfg<D, NST>;
   using E = __nv_bfloat16;
-  static_assert((merge_fixed_floats<D, kMmaRows>() + part_block_floats(kMmaRows, D)) * 4 <= C::WORK_OFF + C::WORK_BYTES,
+  static_assert((merge_fixed_floats<D, kMmaRows>() + part_block_floats(kMmaRows, D)) * 4 <= C::RING_BYTES,
                 "merge stages at least one chunk");
   const SplitParams &p = a.p;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -250,7 +357,6 @@ __global__ void __launch_bounds__(kThreads, 2) split_attn_q8_kernel(const __grid
   __shared__ int s_chunk, s_last;
   __shared__ __align__(8) uint64_t s_merge_bar;
   __shared__ __align__(8) uint64_t s_bars[NST];
-  __shared__ float s_ks[64], s_vs[64];
 
   const int tid = threadIdx.x;
   unsigned char *smem = align1024(smem_raw);
@@ -263,7 +369,8 @@ __global__ void __launch_bounds__(kThreads, 2) split_attn_q8_kernel(const __grid
   }
   uint32_t merge_phase = 0;
   uint32_t seq = 0;
-  griddep_wait();
+  if (tid == 0) prefetch_first_item<D, true>(p, prefetch_stages(p));
+  griddep_wait();  // inputs may come from the previous kernel in the stream
   griddep_launch_dependents();
   plan_items(p, s_len, s_prefix, &s_chunk, s_red);
   const int S = s_chunk;
@@ -291,8 +398,8 @@ __global__ void __launch_bounds__(kThreads, 2) split_attn_q8_kernel(const __grid
     const int rb = rest % p.RB;
     const int kvh = rest / p.RB;
     const int c0 = c * S;
-    const bool ok = stream_chunk_q8<D, NST>(a, smem, s_bars, s_ks, s_vs, seq, b, kvh, rb, L, c0, min(c0 + S, L));
-    finish_item<E, D, kMmaRows, kWarps>(p, combine, (C::WORK_OFF + C::WORK_BYTES) / 4, &s_merge_bar, merge_phase, b,
+    const bool ok = stream_chunk_q8<D, NST>(a, smem, s_bars, seq, b, kvh, rb, L, c0, min(c0 + S, L));
+    finish_item<E, D, kMmaRows, kWarps>(p, combine, C::RING_BYTES / 4, &s_merge_bar, merge_phase, b,
                                         kvh, rb, c, NC, &s_last);
     fence_proxy_async_smem();
     __syncthreads();

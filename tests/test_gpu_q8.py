@@ -138,3 +138,20 @@ def test_q8_rejects_unaligned_smax(td):
     with pytest.raises(TDError) as e:
         td.td_decode_attn_q8(q, codes, scales, codes, scales, torch.tensor([30], dtype=torch.int32, device="cuda"))
     assert e.value.status == 2
+
+
+@pytest.mark.parametrize("T,split", [(1, 0), (1, 100), (5, 0)])
+def test_q8_stale_rows_past_the_length_are_never_used(td, T, split):
+    """Codes and scales past a sequence's length (stale rows) leave the result unchanged, even
+    non-finite scales: a masked key's zero probability never meets its value scale."""
+    case = small_case(dtype="bf16", B=2, Hq=24, Hkv=8, D=128, Smax=1024, T=T, seq_lens=[700, 333], seed=11 + T)
+    kc, ks, vc, vs = _q8_case(case)
+    ref = _run_q8(td, case, kc, ks, vc, vs, split)
+    ks2, vs2, vc2 = ks.copy(), vs.copy(), vc.copy()
+    for b, L in enumerate(case.seq_lens.tolist()):
+        ks2[b, :, L:] = np.nan
+        vs2[b, :, L:] = np.inf
+        vc2[b, :, L:] = 127
+    out, lse, st = _run_q8(td, case, kc, ks2, vc2, vs2, split)
+    assert st == ref[2]
+    assert torch.equal(out, ref[0]) and torch.equal(lse, ref[1])
