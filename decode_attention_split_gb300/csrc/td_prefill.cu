@@ -6,17 +6,22 @@
 // softmax attention over keys j < L - T + t + 1, the same result td_verify_attn defines,
 // computed tile by tile with an online softmax.
 //
-// GB300 design: one CTA (4 warps) per tile of 128 query rows of one query head. Q, K and V
-// tiles cross by TMA with the 128-byte swizzle (K/V double-buffered, 128 keys per tile);
-// one thread issues the tensor-core products, the accumulators live in TMEM:
-//   S[128 x 128] = Q K^T        (A = Q, B = K, both K-major)         -> TMEM columns [0, 128)
-//   O[128 x D]  += P V          (A = P from shared memory, B = V MN-major) -> columns [128, 128 + D)
+// GB300 design: one CTA (4 warps) per tile of 128 query rows of one query head, two CTAs per
+// SM so that one's tensor-core products run while the other computes its softmax. Q, K and
+// V tiles cross by TMA with the 128-byte swizzle (K/V double-buffered, 64 keys per tile); one
+// thread issues the tensor-core products, the accumulators live in TMEM:
+//   S[128 x 64] = Q K^T         (A = Q, B = K, both K-major)         -> TMEM columns [0, 64)
+//   O[128 x D] += P V           (A = P from shared memory, B = V MN-major) -> columns [64, 64 + D)
 // Between the two products every thread owns one query row (its TMEM lane): it reads its S
-// row, masks it causally, and writes P = 2^(s - m) in bf16 into a K-major swizzled tile. The
-// reference maximum m moves only when a row's maximum rises more than 8 (base 2) above it,
-// and only then are that row's O and l rescaled (read, scaled and written back in TMEM);
-// otherwise P stays below 2^8 and O / l, kept against the same m, need no correction.
-// Every wait is bounded; a timeout sets TD_DEV_WAIT_TIMEOUT and the CTA frees its TMEM.
+// row into registers once, masks it causally (only in tiles that reach the diagonal or the
+// sequence's end), and writes P = 2^(s - m) in bf16 into a K-major swizzled tile that takes
+// the place of the K tile the product S has finished with (for D = 128 the two have the same
+// size; for D = 64 P has its own buffer). The reference maximum m moves only when a row's
+// maximum rises more than 8 (base 2) above it, and only then are that row's O and l rescaled
+// (read, scaled and written back in TMEM); otherwise P stays below 2^8 and O / l, kept
+// against the same m, need no correction. Query tiles are launched longest first (causal
+// rows late in the prompt see the most keys). Every wait is bounded; a timeout sets
+// TD_DEV_WAIT_TIMEOUT and the CTA frees its TMEM.
 #include <cudaTypedefs.h>
 #include <math.h>
 
@@ -24,6 +29,7 @@
 
 #include "td_device.cuh"
 #include "td_internal.h"
+#include "td_mma.cuh"
 
 namespace td {
 
@@ -31,26 +37,30 @@ namespace {
 
 constexpr int kPfThreads = 128;
 constexpr int kPfRows = 128;   // query rows per CTA
-constexpr int kPfKeys = 128;   // keys per tile
-constexpr int kRegion = 128 * 128;  // bytes of one swizzled [128 rows][64 bf16] region
-constexpr float kRescaleGap = 8.f;  // base-2 rise of a row maximum before m moves
+constexpr int kPfKeys = 64;    // keys per tile
+constexpr int kQRegion = kPfRows * 128;  // bytes of one swizzled [128 rows][64 bf16] region
+constexpr int kKRegion = kPfKeys * 128;  // bytes of one swizzled [64 rows][64 bf16] region
+constexpr float kRescaleGap = 8.f;       // base-2 rise of a row maximum before m moves
 
 template <int D>
 struct PfCfg {
   static constexpr int HALVES = D / 64;                 // 64-column regions per row tile
-  static constexpr int TILE = HALVES * kRegion;         // Q, K or V tile bytes
+  static constexpr int Q_TILE = HALVES * kQRegion;
+  static constexpr int KV_TILE = HALVES * kKRegion;     // one K or V tile
+  static constexpr int P_TILE = kQRegion;               // P: [128 rows][64 keys], one region
+  static constexpr bool P_IN_K = KV_TILE >= P_TILE;     // P takes the spent K tile's place
   static constexpr int Q_OFF = 0;
-  static constexpr int K_OFF = TILE;                    // two K buffers
-  static constexpr int V_OFF = 3 * TILE;                // two V buffers
-  static constexpr int P_OFF = 5 * TILE;                // P: [128 rows][128 keys] = two regions
-  static constexpr int SMEM = P_OFF + 2 * kRegion + 1024;  // + alignment slack
-  static constexpr int TMEM_COLS = 256;                 // S (128) + O (D), a power of two
-  static_assert(SMEM <= 227 * 1024, "prefill shared memory");
+  static constexpr int K_OFF = Q_TILE;                  // two K buffers
+  static constexpr int V_OFF = K_OFF + 2 * KV_TILE;     // two V buffers
+  static constexpr int P_OFF = V_OFF + 2 * KV_TILE;     // own P buffer when P_IN_K is false
+  static constexpr int SMEM = P_OFF + (P_IN_K ? 0 : P_TILE) + 1024;  // + alignment slack
+  static constexpr int TMEM_COLS = 256;                 // S (64) + O (D), a power of two
+  static_assert(2 * (SMEM + 1024 + 128) <= 228 * 1024, "two CTAs per SM");
 };
 
 struct PfArgs {
   CUtensorMap qmap;  // q [B*Hq][T][D]
-  CUtensorMap kmap;  // caches [B*Hkv][Smax][D], boxes of 128 rows
+  CUtensorMap kmap;  // caches [B*Hkv][Smax][D], boxes of 64 rows
   CUtensorMap vmap;
   const int32_t *seq_lens;
   void *out;         // [B, Hq, T, D] bf16
@@ -98,6 +108,21 @@ __device__ __forceinline__ void tc_commit(uint32_t bar) {
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
+// 64 consecutive fp32 columns of this thread's TMEM lane: two loads and their wait in one
+// statement, so no use of the registers can be placed before the wait.
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
+  uint32_t r[64];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%64];\n"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%65];\n"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+      : "r"(taddr), "r"(taddr + 32)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
+}
+
 // 32 consecutive fp32 columns of this thread's TMEM lane.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   uint32_t r[32];
@@ -132,24 +157,23 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) 
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
-// Byte offset of 16-byte chunk c (of 16) of row r in a [128 rows][128 cols] bf16 tile kept
-// as two 128-byte-swizzled regions of 64 columns (the layout TMA writes and the tensor core
-// reads as K-major).
-__device__ __forceinline__ uint32_t tile_chunk(int r, int c) {
-  return (uint32_t)((c >> 3) * kRegion + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+// Byte offset of 16-byte chunk c of row r in a tile of `rows` rows kept as 128-byte-swizzled
+// regions of 64 bf16 columns (the layout TMA writes and the tensor core reads as K-major).
+__device__ __forceinline__ uint32_t tile_chunk(int rows, int r, int c) {
+  return (uint32_t)((c >> 3) * rows * 128 + r * 128 + (((c & 7) ^ (r & 7)) << 4));
 }
 
 template <int D>
-__global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_constant__ PfArgs a) {
+__global__ void __launch_bounds__(kPfThreads, 2) prefill_kernel(const __grid_constant__ PfArgs a) {
   using C = PfCfg<D>;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   __shared__ __align__(8) uint64_t bar_q, bar_kv[2], bar_s, bar_o;
   __shared__ uint32_t s_taddr;
-  __shared__ int s_fail;
   const int tid = threadIdx.x, warp = tid >> 5;
   unsigned char *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sb = smem_u32(smem);
-  const int qt = blockIdx.x, hq = blockIdx.y, b = blockIdx.z;
+  const int qt = gridDim.x - 1 - blockIdx.x;  // the tiles late in the prompt (most keys) first
+  const int hq = blockIdx.y, b = blockIdx.z;
   const int G = a.Hq / a.Hkv, kvh = hq / G;
   const int t0 = qt * kPfRows;
 
@@ -160,7 +184,6 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
     mbar_init(smem_u32(&bar_s), 1);
     mbar_init(smem_u32(&bar_o), 1);
     fence_mbar_init();
-    s_fail = 0;
   }
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&s_taddr)),
@@ -173,7 +196,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
   tc_fence_after();
   const uint32_t tmem = s_taddr;
   const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-  const uint32_t tS = tmem, tO = tmem + kPfKeys;
+  const uint32_t tS = tmem, tO = tmem + 128;
 
   griddep_wait();
   griddep_launch_dependents();
@@ -185,7 +208,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
   const bool row_valid = t < a.T;
   const int lim = row_valid ? max(0, min(L, L - a.T + t + 1)) : 0;
   const int last_t = min(t0 + kPfRows, a.T) - 1;
-  const int kend = max(0, min(L, L - a.T + last_t + 1));  // keys any row of the tile sees
+  const int kend = max(0, min(L, L - a.T + last_t + 1));      // keys any row of the tile sees
+  const int kall = max(0, min(L, L - a.T + t0 + 1));          // keys every row of the tile sees
   const int nkt = (kend + kPfKeys - 1) / kPfKeys;
   if (tid == 0 && qt == 0 && hq == 0) {
     uint32_t bits = 0;
@@ -199,28 +223,32 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
   auto load_kv = [&](int kt) {  // thread 0: key tile kt into buffer kt % 2
     const int buf = kt & 1;
     const uint32_t bar = smem_u32(&bar_kv[buf]);
-    mbar_arrive_expect_tx(bar, 2 * C::TILE);
+    mbar_arrive_expect_tx(bar, 2 * C::KV_TILE);
 #pragma unroll
     for (int h = 0; h < C::HALVES; ++h) {
-      tma3(sb + C::K_OFF + buf * C::TILE + h * kRegion, &a.kmap, 64 * h, kt * kPfKeys, zk, bar);
-      tma3(sb + C::V_OFF + buf * C::TILE + h * kRegion, &a.vmap, 64 * h, kt * kPfKeys, zk, bar);
+      tma3(sb + C::K_OFF + buf * C::KV_TILE + h * kKRegion, &a.kmap, 64 * h, kt * kPfKeys, zk, bar);
+      tma3(sb + C::V_OFF + buf * C::KV_TILE + h * kKRegion, &a.vmap, 64 * h, kt * kPfKeys, zk, bar);
     }
   };
   if (tid == 0 && nkt > 0) {
     const uint32_t bar = smem_u32(&bar_q);
-    mbar_arrive_expect_tx(bar, C::TILE);
+    mbar_arrive_expect_tx(bar, C::Q_TILE);
 #pragma unroll
-    for (int h = 0; h < C::HALVES; ++h) tma3(sb + C::Q_OFF + h * kRegion, &a.qmap, 64 * h, t0, zq, bar);
+    for (int h = 0; h < C::HALVES; ++h) tma3(sb + C::Q_OFF + h * kQRegion, &a.qmap, 64 * h, t0, zq, bar);
     load_kv(0);
     if (nkt > 1) load_kv(1);
   }
 
   constexpr uint32_t kIdS = mma_idesc(kPfRows, kPfKeys, false);
   constexpr uint32_t kIdO = mma_idesc(kPfRows, D, true);
+  const float qscale = a.qscale;
   float m_ref = -INFINITY, l = 0.f;
   bool ok = true;
   for (int kt = 0; kt < nkt && ok; ++kt) {
     const int buf = kt & 1;
+    const uint32_t kbuf = sb + C::K_OFF + buf * C::KV_TILE, vbuf = sb + C::V_OFF + buf * C::KV_TILE;
+    // P of this tile takes the place of its K tile once S is computed (D = 128)
+    const uint32_t pbuf = C::P_IN_K ? kbuf : sb + C::P_OFF;
     // every thread: this tile's K/V have landed (its V rows past the sequence are zeroed below)
     bool landed = mbar_wait_bounded(smem_u32(&bar_kv[buf]), (uint32_t)(kt >> 1) & 1u);
     if (kt == 0) landed = landed && mbar_wait_bounded(smem_u32(&bar_q), 0);
@@ -234,23 +262,24 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
       // are the next region)
 #pragma unroll
       for (int k = 0; k < D / 16; ++k) {
-        const uint32_t off = (k >> 2) * kRegion + (k & 3) * 32;
-        tc_mma(tS, smem_desc(sb + C::Q_OFF + off, 16, 1024), smem_desc(sb + C::K_OFF + buf * C::TILE + off, 16, 1024),
-               kIdS, k > 0);
+        const uint32_t col = (k & 3) * 32;
+        tc_mma(tS, smem_desc(sb + C::Q_OFF + (k >> 2) * kQRegion + col, 16, 1024),
+               smem_desc(kbuf + (k >> 2) * kKRegion + col, 16, 1024), kIdS, k > 0);
       }
       tc_commit(smem_u32(&bar_s));
     }
     // V rows at or past the sequence's length: zeroed (a masked p of 0 must not meet a stale value)
-    const int vrows = min(kPfKeys, L - kt * kPfKeys);
+    const int j0 = kt * kPfKeys;
+    const int vrows = min(kPfKeys, L - j0);
     if (vrows < kPfKeys) {
-      unsigned char *vt = smem + C::V_OFF + buf * C::TILE;
+      unsigned char *vt = smem + C::V_OFF + buf * C::KV_TILE;
       for (int idx = tid; idx < (kPfKeys - vrows) * (D / 8); idx += kPfThreads) {
         const int r = vrows + idx / (D / 8), c = idx % (D / 8);
-        *reinterpret_cast<uint4 *>(vt + tile_chunk(r, c)) = make_uint4(0u, 0u, 0u, 0u);
+        *reinterpret_cast<uint4 *>(vt + tile_chunk(kPfKeys, r, c)) = make_uint4(0u, 0u, 0u, 0u);
       }
       fence_proxy_async_smem();
     }
-    // the previous P V product must be done before P and O are touched
+    // S is complete, and so is the previous P V product (P and O are touched next)
     bool done = mbar_wait_bounded(smem_u32(&bar_s), (uint32_t)kt & 1u);
     if (kt > 0) done = done && mbar_wait_bounded(smem_u32(&bar_o), (uint32_t)(kt - 1) & 1u);
     if (!__syncthreads_and(done)) {
@@ -258,20 +287,28 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
       break;
     }
     tc_fence_after();
-    if (tid == 0 && kt + 1 < nkt && kt >= 1) load_kv(kt + 1);  // buffer (kt+1)&1 is free: P V of kt-1 finished
-    // this row's scores: scaled to base 2, masked causally
-    const int j0 = kt * kPfKeys;
-    float mx = -INFINITY;
+    // buffer (kt+1)&1 is free: the P V product of kt-1, which read its V and P, is done
+    if (tid == 0 && kt + 1 < nkt && kt >= 1) load_kv(kt + 1);
+    // this row's 64 scores, read once
+    float sv[kPfKeys];
+    tmem_ld64(tS + lane_base, sv);
+    // tiles short of every row's diagonal and of the sequence's end need no mask
+    const bool full = j0 + kPfKeys <= kall;
+    const int vis = full ? kPfKeys : min(kPfKeys, max(0, lim - j0));  // this row's visible keys
+    // the row maximum, scaled to base 2 (the scale's sign decides which extreme)
+    float ext = qscale >= 0.f ? -INFINITY : INFINITY;
+    if (qscale >= 0.f) {
 #pragma unroll
-    for (int c = 0; c < kPfKeys; c += 32) {
-      float s[32];
-      tmem_ld32(tS + lane_base + c, s);
+      for (int i = 0; i < kPfKeys; ++i)
+        if (full || i < vis) ext = fmaxf(ext, sv[i]);
+    } else {
 #pragma unroll
-      for (int i = 0; i < 32; ++i)
-        if (j0 + c + i < lim) mx = fmaxf(mx, s[i] * a.qscale);
+      for (int i = 0; i < kPfKeys; ++i)
+        if (full || i < vis) ext = fminf(ext, sv[i]);
     }
+    const float mx = vis > 0 ? ext * qscale : -INFINITY;
     const bool move = mx > m_ref + kRescaleGap || (m_ref == -INFINITY && mx > -INFINITY);
-    const float alpha = (move && m_ref != -INFINITY) ? exp2f(m_ref - mx) : 1.f;
+    const float alpha = (move && m_ref != -INFINITY) ? exp2_approx(m_ref - mx) : 1.f;
     if (move) {
       l *= alpha;
       m_ref = mx;
@@ -288,37 +325,32 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
       }
     }
     // P = 2^(s - m) in bf16 into the K-major swizzled P tile (row = this thread's query)
-    const float base = m_ref == -INFINITY ? 0.f : m_ref;
+    const float nbase = m_ref == -INFINITY ? 0.f : -m_ref;
+    uint32_t pk[kPfKeys / 2];
 #pragma unroll
-    for (int c = 0; c < kPfKeys; c += 32) {
-      float s[32];
-      tmem_ld32(tS + lane_base + c, s);
-      uint32_t pk[16];
-#pragma unroll
-      for (int i = 0; i < 32; i += 2) {
-        const float p0 = (j0 + c + i < lim) ? exp2f(s[i] * a.qscale - base) : 0.f;
-        const float p1 = (j0 + c + i + 1 < lim) ? exp2f(s[i + 1] * a.qscale - base) : 0.f;
-        l += p0 + p1;
-        const __nv_bfloat162 v2 = __floats2bfloat162_rn(p0, p1);
-        pk[i / 2] = *reinterpret_cast<const uint32_t *>(&v2);
-      }
-#pragma unroll
-      for (int q = 0; q < 4; ++q)
-        *reinterpret_cast<uint4 *>(smem + C::P_OFF + tile_chunk(row, c / 8 + q)) =
-            make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+    for (int i = 0; i < kPfKeys; i += 2) {
+      const float p0 = (full || i < vis) ? exp2_approx(fmaf(sv[i], qscale, nbase)) : 0.f;
+      const float p1 = (full || i + 1 < vis) ? exp2_approx(fmaf(sv[i + 1], qscale, nbase)) : 0.f;
+      l += p0 + p1;
+      pk[i / 2] = pack_bf16x2(p0, p1);
     }
+    unsigned char *prow = smem + (pbuf - sb);
+#pragma unroll
+    for (int c = 0; c < kPfKeys / 8; ++c)
+      *reinterpret_cast<uint4 *>(prow + tile_chunk(kPfRows, row, c)) =
+          make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
     fence_proxy_async_smem();  // P is read by the tensor core (asynchronous proxy)
     tc_fence_before();
     __syncthreads();
     if (tid == 0) {
       tc_fence_after();
-      // O += P V over the tile's 128 keys in steps of 16: A = P (K-major), B = V (MN-major:
-      // 16 keys = 16 rows of 128 bytes; the next 64 columns are the next region)
+      // O += P V over the tile's 64 keys in steps of 16: A = P (K-major, 32 bytes per step),
+      // B = V (MN-major: 16 keys = 16 rows of 128 bytes; the next 64 columns are the next
+      // region)
 #pragma unroll
-      for (int k = 0; k < kPfKeys / 16; ++k) {
-        tc_mma(tO, smem_desc(sb + C::P_OFF + (k >> 2) * kRegion + (k & 3) * 32, 16, 1024),
-               smem_desc(sb + C::V_OFF + buf * C::TILE + k * 16 * 128, kRegion, 1024), kIdO, kt > 0 || k > 0);
-      }
+      for (int k = 0; k < kPfKeys / 16; ++k)
+        tc_mma(tO, smem_desc(pbuf + k * 32, 16, 1024), smem_desc(vbuf + k * 16 * 128, kKRegion, 1024), kIdO,
+               kt > 0 || k > 0);
       tc_commit(smem_u32(&bar_o));
     }
   }
@@ -344,10 +376,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
     if (row_valid) {
       uint32_t pk[16];
 #pragma unroll
-      for (int i = 0; i < 32; i += 2) {
-        const __nv_bfloat162 v2 = __floats2bfloat162_rn(o[i] * inv, o[i + 1] * inv);
-        pk[i / 2] = *reinterpret_cast<const uint32_t *>(&v2);
-      }
+      for (int i = 0; i < 32; i += 2) pk[i / 2] = pack_bf16x2(o[i] * inv, o[i + 1] * inv);
 #pragma unroll
       for (int q = 0; q < 4; ++q)
         reinterpret_cast<uint4 *>(orow + c)[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
@@ -375,13 +404,13 @@ PFN_cuTensorMapEncodeTiled_v12000 pf_encoder() {
   return fn;
 }
 
-// 3-D map over [planes][rows][D] bf16, boxes of 64 columns x 128 rows, 128-byte swizzle.
-bool pf_map(CUtensorMap *m, const void *base, long long planes, int rows, int D) {
+// 3-D map over [planes][rows][D] bf16, boxes of 64 columns x box_rows rows, 128-byte swizzle.
+bool pf_map(CUtensorMap *m, const void *base, long long planes, int rows, int D, int box_rows) {
   const PFN_cuTensorMapEncodeTiled_v12000 enc = pf_encoder();
   if (enc == nullptr) return false;
   const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)rows, (cuuint64_t)planes};
   const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)rows * D * 2};
-  const cuuint32_t box[3] = {64, 128, 1};
+  const cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
   const cuuint32_t es[3] = {1, 1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, es,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -390,8 +419,9 @@ bool pf_map(CUtensorMap *m, const void *base, long long planes, int rows, int D)
 
 template <int D>
 cudaError_t launch_prefill_d(PfArgs &a, const void *q, const void *k, const void *v, cudaStream_t stream) {
-  if (!pf_map(&a.qmap, q, (long long)a.B * a.Hq, a.T, D) || !pf_map(&a.kmap, k, (long long)a.B * a.Hkv, a.Smax, D) ||
-      !pf_map(&a.vmap, v, (long long)a.B * a.Hkv, a.Smax, D))
+  if (!pf_map(&a.qmap, q, (long long)a.B * a.Hq, a.T, D, kPfRows) ||
+      !pf_map(&a.kmap, k, (long long)a.B * a.Hkv, a.Smax, D, kPfKeys) ||
+      !pf_map(&a.vmap, v, (long long)a.B * a.Hkv, a.Smax, D, kPfKeys))
     return cudaErrorInvalidValue;
   static std::once_flag once;
   static cudaError_t attr = cudaSuccess;

@@ -154,16 +154,12 @@ __device__ void place_new_rows(const SplitParams &p, unsigned char *stage, int b
 
 // One warp's step over 16 keys of a landed stage (keys key0 .. key0+15, rows kr .. kr+15 of
 // the stage's tiles): S = Q K^T over two 8-key n tiles, masking by the rows' visible-key
-// limits `lim`, the online softmax in base 2, then O += P V. kt / vt address bf16 K / V tiles
-// in the TMA-swizzled layout. For quantised caches, kscale / vscale hold the stage's per-row
-// scales: the key scale multiplies the scores and the value scale multiplies P (the tiles
-// then hold the integer codes); both null for bf16 caches. F16: the tiles and the query
-// fragments hold fp16 instead of bf16 (P is then rounded to fp16).
-template <int D, bool F16 = false>
+// limits `lim`, the online softmax in base 2, then O += P V. kt / vt address bf16 K / V
+// tiles in the TMA-swizzled layout.
+template <int D>
 __device__ __forceinline__ void warp_keys16(const uint32_t (&qa)[D / 16][4], uint32_t kt, uint32_t vt, int kr,
-                                            int key0, const int (&lim)[2], float qscale, const float *kscale,
-                                            const float *vscale, float (&o)[D / 8][4], float (&m_run)[2],
-                                            float (&l_run)[2]) {
+                                            int key0, const int (&lim)[2], float qscale, float (&o)[D / 8][4],
+                                            float (&m_run)[2], float (&l_run)[2]) {
   constexpr int TK = 64, KSD = D / 16, NTD = D / 8;
   const int lane = threadIdx.x & 31, tig = lane & 3;
   float sc[2][4];
@@ -174,24 +170,10 @@ __device__ __forceinline__ void warp_keys16(const uint32_t (&qa)[D / 16][4], uin
     for (int i = 0; i < KSD / 2; ++i) {
       uint32_t bk[4];
       ldmatrix_x4(bk, kt + tma_swz<TK>(kr + nt * 8 + (lane & 7), 4 * i + (lane >> 3)));
-      if (F16) {
-        mma_f16_16816(sc[nt], qa[2 * i], bk[0], bk[1]);
-        mma_f16_16816(sc[nt], qa[2 * i + 1], bk[2], bk[3]);
-      } else {
-        mma_bf16_16816(sc[nt], qa[2 * i], bk[0], bk[1]);
-        mma_bf16_16816(sc[nt], qa[2 * i + 1], bk[2], bk[3]);
-      }
+      mma_bf16_16816(sc[nt], qa[2 * i], bk[0], bk[1]);
+      mma_bf16_16816(sc[nt], qa[2 * i + 1], bk[2], bk[3]);
     }
   }
-  float ks[2][2], vs[2][2];  // scales of this thread's four keys
-#pragma unroll
-  for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      const int r = kr + nt * 8 + 2 * tig + e;
-      ks[nt][e] = kscale != nullptr ? kscale[r] * qscale : qscale;
-      vs[nt][e] = vscale != nullptr ? vscale[r] : 1.f;
-    }
   // scale to base-2 units, mask, online softmax; row half h holds sc[nt][2h], sc[nt][2h+1]
   float alpha[2];
 #pragma unroll
@@ -202,7 +184,7 @@ __device__ __forceinline__ void warp_keys16(const uint32_t (&qa)[D / 16][4], uin
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         const int key = key0 + nt * 8 + 2 * tig + e;
-        const float v = key < lim[h] ? sc[nt][2 * h + e] * ks[nt][e] : -INFINITY;
+        const float v = key < lim[h] ? sc[nt][2 * h + e] * qscale : -INFINITY;
         sc[nt][2 * h + e] = v;
         mx = fmaxf(mx, v);
       }
@@ -218,7 +200,7 @@ __device__ __forceinline__ void warp_keys16(const uint32_t (&qa)[D / 16][4], uin
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         const float pv = exp2f(sc[nt][2 * h + e] - base);
-        sc[nt][2 * h + e] = pv * vs[nt][e];
+        sc[nt][2 * h + e] = pv;
         ps += pv;
       }
     l_run[h] = l_run[h] * alpha[h] + ps;
@@ -232,30 +214,15 @@ __device__ __forceinline__ void warp_keys16(const uint32_t (&qa)[D / 16][4], uin
       o[nt][3] *= alpha[1];
     }
   }
-  uint32_t pa[4];
-  if (F16) {
-    pa[0] = pack_f16x2(sc[0][0], sc[0][1]);
-    pa[1] = pack_f16x2(sc[0][2], sc[0][3]);
-    pa[2] = pack_f16x2(sc[1][0], sc[1][1]);
-    pa[3] = pack_f16x2(sc[1][2], sc[1][3]);
-  } else {
-    pa[0] = pack_bf16x2(sc[0][0], sc[0][1]);
-    pa[1] = pack_bf16x2(sc[0][2], sc[0][3]);
-    pa[2] = pack_bf16x2(sc[1][0], sc[1][1]);
-    pa[3] = pack_bf16x2(sc[1][2], sc[1][3]);
-  }
+  const uint32_t pa[4] = {pack_bf16x2(sc[0][0], sc[0][1]), pack_bf16x2(sc[0][2], sc[0][3]),
+                          pack_bf16x2(sc[1][0], sc[1][1]), pack_bf16x2(sc[1][2], sc[1][3])};
   // O += P V over these 16 keys, two 8-wide output tiles per ldmatrix
 #pragma unroll
   for (int i = 0; i < NTD / 2; ++i) {
     uint32_t bv[4];
     ldmatrix_x4_trans(bv, vt + tma_swz<TK>(kr + (lane & 7) + ((lane >> 3) & 1) * 8, 2 * i + (lane >> 4)));
-    if (F16) {
-      mma_f16_16816(o[2 * i], pa, bv[0], bv[1]);
-      mma_f16_16816(o[2 * i + 1], pa, bv[2], bv[3]);
-    } else {
-      mma_bf16_16816(o[2 * i], pa, bv[0], bv[1]);
-      mma_bf16_16816(o[2 * i + 1], pa, bv[2], bv[3]);
-    }
+    mma_bf16_16816(o[2 * i], pa, bv[0], bv[1]);
+    mma_bf16_16816(o[2 * i + 1], pa, bv[2], bv[3]);
   }
 }
 
@@ -386,7 +353,7 @@ __device__ bool stream_chunk(const MmaArgs &a, unsigned char *smem, uint64_t *s_
     if (tid == 0 && st + NST - 1 < nstages) issue(st + NST - 1);
     const int kr = warp * C::TKW;  // first key row (within the stage) of this warp's step
     const int key0 = j0 + kr;
-    if (key0 < c1) warp_keys16<D>(qa, kt, vt, kr, key0, lim, p.qscale, nullptr, nullptr, o, m_run, l_run);
+    if (key0 < c1) warp_keys16<D>(qa, kt, vt, kr, key0, lim, p.qscale, o, m_run, l_run);
     consumed = st + 1;
   }
   if (!ok) {
