@@ -313,7 +313,8 @@ extern "C" td_status td_prefill_attn(const void *q, const void *k_cache, const v
   if (q == nullptr || k_cache == nullptr || v_cache == nullptr || seq_lens == nullptr || out == nullptr)
     return TD_ERR_INVALID_ARG;
   if (B < 1 || Hq < 1 || Hkv < 1 || T < 1 || Smax < 1 || Hq % Hkv != 0 || !isfinite(scale)) return TD_ERR_INVALID_ARG;
-  if ((D != 64 && D != 128) || T > Smax || B > 65535 || Hq > 65535) return TD_ERR_UNSUPPORTED;
+  if ((D != 64 && D != 128) || T > Smax || B > 65535 || Hq > 65535 || (T + 127) / 128 > 65535)
+    return TD_ERR_UNSUPPORTED;
   if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) || !aligned4(seq_lens) ||
       (lse != nullptr && !aligned4(lse)) || (dev_status != nullptr && !aligned4(dev_status)))
     return TD_ERR_UNSUPPORTED;

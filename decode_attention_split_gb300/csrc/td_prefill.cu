@@ -6,22 +6,25 @@
 // softmax attention over keys j < L - T + t + 1, the same result td_verify_attn defines,
 // computed tile by tile with an online softmax.
 //
-// GB300 design: one CTA (4 warps) per tile of 128 query rows of one query head, two CTAs per
-// SM so that one's tensor-core products run while the other computes its softmax. Q, K and
-// V tiles cross by TMA with the 128-byte swizzle (K/V double-buffered, 64 keys per tile); one
-// thread issues the tensor-core products, the accumulators live in TMEM:
-//   S[128 x 64] = Q K^T         (A = Q, B = K, both K-major)         -> TMEM columns [0, 64)
-//   O[128 x D] += P V           (A = P from shared memory, B = V MN-major) -> columns [64, 64 + D)
-// Between the two products every thread owns one query row (its TMEM lane): it reads its S
-// row into registers once, masks it causally (only in tiles that reach the diagonal or the
-// sequence's end), and writes P = 2^(s - m) in bf16 into a K-major swizzled tile that takes
-// the place of the K tile the product S has finished with (for D = 128 the two have the same
-// size; for D = 64 P has its own buffer). The reference maximum m moves only when a row's
-// maximum rises more than 8 (base 2) above it, and only then are that row's O and l rescaled
-// (read, scaled and written back in TMEM); otherwise P stays below 2^8 and O / l, kept
-// against the same m, need no correction. Query tiles are launched longest first (causal
-// rows late in the prompt see the most keys). Every wait is bounded; a timeout sets
-// TD_DEV_WAIT_TIMEOUT and the CTA frees its TMEM.
+// GB300 design: one CTA per tile of 128 query rows of one query head, two CTAs per SM. Q, K
+// and V tiles cross by TMA with the 128-byte swizzle (K and V double-buffered with their own
+// barriers, 64 keys per tile). A fifth warp issues the copies and the tensor-core products;
+// the accumulators live in TMEM:
+//   S[128 x 64] = Q K^T     (A = Q, B = K, both K-major in shared memory)  -> S buffer kt % 2
+//   O[128 x D] += P V       (A = P in TMEM, B = V MN-major in shared memory) -> O
+// S is double-buffered (TMEM columns [0, 64) and [64, 128), O from column 128), so the
+// product S of tile kt+1 runs while the four softmax warps work on tile kt. Each softmax
+// thread owns one query row (its TMEM lane): it reads its 64 scores once, masks them
+// causally (only in tiles that reach the diagonal or the sequence's end), and writes
+// P = 2^(s - m) as bf16 pairs over the first 32 columns of the same S buffer, which the P V
+// product reads as its A operand (lane = row, one column per pair of keys). A softmax warp
+// hands its rows over through an mbarrier (one arrival per warp), so the warps do not wait
+// for one another within a tile. The reference maximum m moves only when a row's maximum
+// rises more than 8 (base 2) above it, and only then are that row's O and l rescaled (after
+// the previous P V product is complete); otherwise P stays below 2^8 and O / l, kept against
+// the same m, need no correction. Query tiles are launched longest first (causal rows late in
+// the prompt see the most keys). Every wait is bounded; a timeout sets TD_DEV_WAIT_TIMEOUT,
+// and the CTA waits (bounded) for its copies and products in flight before it frees TMEM.
 #include <cudaTypedefs.h>
 #include <math.h>
 
@@ -35,7 +38,8 @@ namespace td {
 
 namespace {
 
-constexpr int kPfThreads = 128;
+constexpr int kPfSoftmaxWarps = 4;             // one query row per thread
+constexpr int kPfThreads = 32 * (kPfSoftmaxWarps + 1);  // + the copy / tensor-core warp
 constexpr int kPfRows = 128;   // query rows per CTA
 constexpr int kPfKeys = 64;    // keys per tile
 constexpr int kQRegion = kPfRows * 128;  // bytes of one swizzled [128 rows][64 bf16] region
@@ -47,14 +51,11 @@ struct PfCfg {
   static constexpr int HALVES = D / 64;                 // 64-column regions per row tile
   static constexpr int Q_TILE = HALVES * kQRegion;
   static constexpr int KV_TILE = HALVES * kKRegion;     // one K or V tile
-  static constexpr int P_TILE = kQRegion;               // P: [128 rows][64 keys], one region
-  static constexpr bool P_IN_K = KV_TILE >= P_TILE;     // P takes the spent K tile's place
   static constexpr int Q_OFF = 0;
   static constexpr int K_OFF = Q_TILE;                  // two K buffers
   static constexpr int V_OFF = K_OFF + 2 * KV_TILE;     // two V buffers
-  static constexpr int P_OFF = V_OFF + 2 * KV_TILE;     // own P buffer when P_IN_K is false
-  static constexpr int SMEM = P_OFF + (P_IN_K ? 0 : P_TILE) + 1024;  // + alignment slack
-  static constexpr int TMEM_COLS = 256;                 // S (64) + O (D), a power of two
+  static constexpr int SMEM = V_OFF + 2 * KV_TILE + 1024;  // + alignment slack
+  static constexpr int TMEM_COLS = 256;                 // two S buffers (64 each) + O (D), a power of two
   static_assert(2 * (SMEM + 1024 + 128) <= 228 * 1024, "two CTAs per SM");
 };
 
@@ -101,6 +102,16 @@ __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a, uint64_t b, 
       : "memory");
 }
 
+// The same with A in TMEM (`a_tmem`: lane = row, one 32-bit column per pair of K elements).
+__device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                          bool accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(
+          d_tmem),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"((uint32_t)accumulate)
+      : "memory");
+}
+
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
 }
@@ -139,22 +150,40 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
-      "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
-      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])), "r"(__float_as_uint(v[3])),
-      "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])), "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])),
-      "r"(__float_as_uint(v[8])), "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
-      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
-      "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])),
-      "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])),
-      "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
-      "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
-      "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
-      "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
-      : "memory");
+// 32 consecutive 32-bit columns of this thread's TMEM lane, waited for.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&w)[32]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr), "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7]), "r"(w[8]), "r"(w[9]), "r"(w[10]), "r"(w[11]), "r"(w[12]), "r"(w[13]), "r"(w[14]), "r"(w[15]), "r"(w[16]), "r"(w[17]), "r"(w[18]), "r"(w[19]), "r"(w[20]), "r"(w[21]), "r"(w[22]), "r"(w[23]), "r"(w[24]), "r"(w[25]), "r"(w[26]), "r"(w[27]), "r"(w[28]), "r"(w[29]), "r"(w[30]), "r"(w[31]) : "memory");
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
+  uint32_t w[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(v[i]);
+  tmem_st32(taddr, w);
+}
+
+// One row's probabilities 2^(s * qscale + nbase) for the 64 scores sv, packed in bf16 pairs
+// into pk; MASK: keys from `vis` on get 0. Returns their fp32 sum (in packed pairs, two
+// partial sums, so the additions do not form one chain).
+template <bool MASK>
+__device__ __forceinline__ float p_row(const float (&sv)[kPfKeys], float qscale, float nbase, int vis,
+                                       uint32_t (&pk)[kPfKeys / 2]) {
+  float2 l2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+  const float2 sc2 = make_float2(qscale, qscale), nb2 = make_float2(nbase, nbase);
+#pragma unroll
+  for (int i = 0; i < kPfKeys; i += 2) {
+    const float2 x = ffma2(make_float2(sv[i], sv[i + 1]), sc2, nb2);
+    float2 pr = make_float2(exp2_approx(x.x), exp2_approx(x.y));
+    if (MASK) {
+      pr.x = i < vis ? pr.x : 0.f;
+      pr.y = i + 1 < vis ? pr.y : 0.f;
+    }
+    l2[(i >> 1) & 1] = fadd2(l2[(i >> 1) & 1], pr);
+    pk[i / 2] = pack_bf16x2(pr.x, pr.y);
+  }
+  const float2 t = fadd2(l2[0], l2[1]);
+  return t.x + t.y;
 }
 
 // Byte offset of 16-byte chunk c of row r in a tile of `rows` rows kept as 128-byte-swizzled
@@ -167,22 +196,29 @@ template <int D>
 __global__ void __launch_bounds__(kPfThreads, 2) prefill_kernel(const __grid_constant__ PfArgs a) {
   using C = PfCfg<D>;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
-  __shared__ __align__(8) uint64_t bar_q, bar_kv[2], bar_s, bar_o;
+  __shared__ __align__(8) uint64_t bar_q, bar_k[2], bar_v[2], bar_s[2], bar_p[2], bar_o, bar_fin;
   __shared__ uint32_t s_taddr;
-  const int tid = threadIdx.x, warp = tid >> 5;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   unsigned char *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sb = smem_u32(smem);
-  const int qt = gridDim.x - 1 - blockIdx.x;  // the tiles late in the prompt (most keys) first
-  const int hq = blockIdx.y, b = blockIdx.z;
+  // blocks start in index order, x fastest: every head's tile late in the prompt (most keys)
+  // comes before any shorter one
+  const int qt = gridDim.y - 1 - blockIdx.y;
+  const int hq = blockIdx.x % a.Hq, b = blockIdx.x / a.Hq;
   const int G = a.Hq / a.Hkv, kvh = hq / G;
   const int t0 = qt * kPfRows;
 
   if (tid == 0) {
     mbar_init(smem_u32(&bar_q), 1);
-    mbar_init(smem_u32(&bar_kv[0]), 1);
-    mbar_init(smem_u32(&bar_kv[1]), 1);
-    mbar_init(smem_u32(&bar_s), 1);
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&bar_k[i]), 1);
+      mbar_init(smem_u32(&bar_v[i]), 1);
+      mbar_init(smem_u32(&bar_s[i]), 1);
+      mbar_init(smem_u32(&bar_p[i]), kPfSoftmaxWarps);
+    }
     mbar_init(smem_u32(&bar_o), 1);
+    mbar_init(smem_u32(&bar_fin), 1);
     fence_mbar_init();
   }
   if (warp == 0) {
@@ -195,21 +231,15 @@ __global__ void __launch_bounds__(kPfThreads, 2) prefill_kernel(const __grid_con
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = s_taddr;
-  const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-  const uint32_t tS = tmem, tO = tmem + 128;
+  const uint32_t tS = tmem, tO = tmem + 128;  // S buffer i at tS + 64 i
 
   griddep_wait();
   griddep_launch_dependents();
   const int32_t raw = a.seq_lens[b];
   const int L = raw < 0 ? 0 : (raw > a.Smax ? a.Smax : raw);
-  // row r (query t = t0 + r) sees keys j < L - T + t + 1
-  const int row = tid;
-  const int t = t0 + row;
-  const bool row_valid = t < a.T;
-  const int lim = row_valid ? max(0, min(L, L - a.T + t + 1)) : 0;
   const int last_t = min(t0 + kPfRows, a.T) - 1;
-  const int kend = max(0, min(L, L - a.T + last_t + 1));      // keys any row of the tile sees
-  const int kall = max(0, min(L, L - a.T + t0 + 1));          // keys every row of the tile sees
+  const int kend = max(0, min(L, L - a.T + last_t + 1));  // keys any row of the tile sees
+  const int kall = max(0, min(L, L - a.T + t0 + 1));      // keys every row of the tile sees
   const int nkt = (kend + kPfKeys - 1) / kPfKeys;
   if (tid == 0 && qt == 0 && hq == 0) {
     uint32_t bits = 0;
@@ -218,172 +248,236 @@ __global__ void __launch_bounds__(kPfThreads, 2) prefill_kernel(const __grid_con
     if (a.T > 1 && L < a.T) bits |= TD_DEV_VERIFY_SHORT;
     report(a.status, bits);
   }
-
-  const int zq = b * a.Hq + hq, zk = b * a.Hkv + kvh;
-  auto load_kv = [&](int kt) {  // thread 0: key tile kt into buffer kt % 2
-    const int buf = kt & 1;
-    const uint32_t bar = smem_u32(&bar_kv[buf]);
-    mbar_arrive_expect_tx(bar, 2 * C::KV_TILE);
-#pragma unroll
-    for (int h = 0; h < C::HALVES; ++h) {
-      tma3(sb + C::K_OFF + buf * C::KV_TILE + h * kKRegion, &a.kmap, 64 * h, kt * kPfKeys, zk, bar);
-      tma3(sb + C::V_OFF + buf * C::KV_TILE + h * kKRegion, &a.vmap, 64 * h, kt * kPfKeys, zk, bar);
-    }
-  };
-  if (tid == 0 && nkt > 0) {
-    const uint32_t bar = smem_u32(&bar_q);
-    mbar_arrive_expect_tx(bar, C::Q_TILE);
-#pragma unroll
-    for (int h = 0; h < C::HALVES; ++h) tma3(sb + C::Q_OFF + h * kQRegion, &a.qmap, 64 * h, t0, zq, bar);
-    load_kv(0);
-    if (nkt > 1) load_kv(1);
-  }
-
-  constexpr uint32_t kIdS = mma_idesc(kPfRows, kPfKeys, false);
-  constexpr uint32_t kIdO = mma_idesc(kPfRows, D, true);
   const float qscale = a.qscale;
-  float m_ref = -INFINITY, l = 0.f;
   bool ok = true;
-  for (int kt = 0; kt < nkt && ok; ++kt) {
-    const int buf = kt & 1;
-    const uint32_t kbuf = sb + C::K_OFF + buf * C::KV_TILE, vbuf = sb + C::V_OFF + buf * C::KV_TILE;
-    // P of this tile takes the place of its K tile once S is computed (D = 128)
-    const uint32_t pbuf = C::P_IN_K ? kbuf : sb + C::P_OFF;
-    // every thread: this tile's K/V have landed (its V rows past the sequence are zeroed below)
-    bool landed = mbar_wait_bounded(smem_u32(&bar_kv[buf]), (uint32_t)(kt >> 1) & 1u);
-    if (kt == 0) landed = landed && mbar_wait_bounded(smem_u32(&bar_q), 0);
-    if (!__syncthreads_and(landed)) {
-      ok = false;
-      break;
+  // copy / tensor-core thread: tiles of K and V issued and seen landed (for the wind-down)
+  int kq = 0, kw = 0, vq = 0, vw = 0;
+  bool q_seen = false;
+  float m_ref = -INFINITY, l = 0.f;  // softmax threads: this row's reference maximum and sum
+
+  if (warp == kPfSoftmaxWarps) {
+    if (lane == 0 && nkt > 0) {
+      const int zq = b * a.Hq + hq, zk = b * a.Hkv + kvh;
+      constexpr uint32_t kIdS = mma_idesc(kPfRows, kPfKeys, false);
+      constexpr uint32_t kIdO = mma_idesc(kPfRows, D, true);
+      auto load = [&](bool v, int kt) {  // K or V tile kt into buffer kt % 2
+        const int buf = kt & 1;
+        const uint32_t bar = smem_u32(v ? &bar_v[buf] : &bar_k[buf]);
+        const uint32_t dst = sb + (v ? C::V_OFF : C::K_OFF) + buf * C::KV_TILE;
+        mbar_arrive_expect_tx(bar, C::KV_TILE);
+#pragma unroll
+        for (int h = 0; h < C::HALVES; ++h) tma3(dst + h * kKRegion, v ? &a.vmap : &a.kmap, 64 * h, kt * kPfKeys, zk, bar);
+      };
+      // S of tile kt into S buffer kt % 2 (K tile kt has landed): over D in steps of 16 (32
+      // bytes along a swizzled row; the next 64 columns are the next region)
+      auto issue_s = [&](int kt) {
+        const uint32_t kbuf = sb + C::K_OFF + (kt & 1) * C::KV_TILE;
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t col = (k & 3) * 32;
+          tc_mma(tS + (kt & 1) * kPfKeys, smem_desc(sb + C::Q_OFF + (k >> 2) * kQRegion + col, 16, 1024),
+                 smem_desc(kbuf + (k >> 2) * kKRegion + col, 16, 1024), kIdS, k > 0);
+        }
+        tc_commit(smem_u32(&bar_s[kt & 1]));
+      };
+      {
+        const uint32_t bar = smem_u32(&bar_q);
+        mbar_arrive_expect_tx(bar, C::Q_TILE);
+#pragma unroll
+        for (int h = 0; h < C::HALVES; ++h) tma3(sb + C::Q_OFF + h * kQRegion, &a.qmap, 64 * h, t0, zq, bar);
+      }
+      for (; kq < min(nkt, 2); ++kq) {
+        load(false, kq);
+        load(true, kq);
+      }
+      vq = kq;
+      q_seen = mbar_wait_bounded(smem_u32(&bar_q), 0);
+      ok = q_seen && mbar_wait_bounded(smem_u32(&bar_k[0]), 0);
+      if (ok) {
+        kw = 1;
+        issue_s(0);
+      }
+      for (int kt = 0; ok && kt < nkt; ++kt) {
+        const int b0 = kt & 1, b1 = b0 ^ 1;
+        if (kt + 1 < nkt) {
+          // S buffer b1 and V buffer b1 are free once the P V product of kt-1 is done
+          if (kt >= 1) ok = mbar_wait_bounded(smem_u32(&bar_o), (uint32_t)(kt - 1) & 1u);
+          ok = ok && mbar_wait_bounded(smem_u32(&bar_k[b1]), (uint32_t)((kt + 1) >> 1) & 1u);
+          if (!ok) break;
+          kw = kt + 2;
+          issue_s(kt + 1);
+          if (kt >= 1) load(true, vq++);  // V tile kt+1
+        }
+        if (kt + 2 < nkt) {
+          // K buffer b0 is free once S of kt is done
+          ok = mbar_wait_bounded(smem_u32(&bar_s[b0]), (uint32_t)(kt >> 1) & 1u);
+          if (!ok) break;
+          load(false, kq++);  // K tile kt+2
+        }
+        // P of kt is in TMEM (all four softmax warps) and V of kt has landed: O += P V over
+        // 64 keys in steps of 16 (A: 8 TMEM columns per step; B: MN-major, 16 rows of 128
+        // bytes per step, the next 64 columns in the next region)
+        ok = mbar_wait_bounded(smem_u32(&bar_p[b0]), (uint32_t)(kt >> 1) & 1u) &&
+             mbar_wait_bounded(smem_u32(&bar_v[b0]), (uint32_t)(kt >> 1) & 1u);
+        if (!ok) break;
+        vw = kt + 1;
+        tc_fence_after();
+        const uint32_t vbuf = sb + C::V_OFF + b0 * C::KV_TILE;
+#pragma unroll
+        for (int k = 0; k < kPfKeys / 16; ++k)
+          tc_mma_ts(tO, tS + b0 * kPfKeys + 8 * k, smem_desc(vbuf + k * 16 * 128, kKRegion, 1024), kIdO,
+                    kt > 0 || k > 0);
+        tc_commit(smem_u32(&bar_o));
+      }
     }
-    if (tid == 0) {
+    __syncwarp();
+  } else if (nkt > 0) {
+    // softmax warps: thread `row` owns query t = t0 + row, which sees keys j < L - T + t + 1
+    const int row = tid;
+    const int t = t0 + row;
+    const int lim = t < a.T ? max(0, min(L, L - a.T + t + 1)) : 0;
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    for (int kt = 0; kt < nkt; ++kt) {
+      const int b0 = kt & 1;
+      const uint32_t ph = (uint32_t)(kt >> 1) & 1u;
+      const uint32_t tSk = tS + b0 * kPfKeys + lane_base;
+      // S of kt is complete (the TMEM accesses below are warp-wide: one decision per warp)
+      if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&bar_s[b0]), ph))) {
+        ok = false;
+        break;
+      }
       tc_fence_after();
-      // S = Q K^T over D in steps of 16 (32 bytes along a swizzled row; the next 64 columns
-      // are the next region)
-#pragma unroll
-      for (int k = 0; k < D / 16; ++k) {
-        const uint32_t col = (k & 3) * 32;
-        tc_mma(tS, smem_desc(sb + C::Q_OFF + (k >> 2) * kQRegion + col, 16, 1024),
-               smem_desc(kbuf + (k >> 2) * kKRegion + col, 16, 1024), kIdS, k > 0);
+      const int j0 = kt * kPfKeys;
+      const int vrows = min(kPfKeys, L - j0);
+      if (vrows < kPfKeys) {
+        // V rows at or past the sequence's length, once landed: zeroed (a masked p of 0 must
+        // not meet a stale value)
+        if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&bar_v[b0]), ph))) {
+          ok = false;
+          break;
+        }
+        unsigned char *vt = smem + C::V_OFF + b0 * C::KV_TILE;
+        for (int idx = tid; idx < (kPfKeys - vrows) * (D / 8); idx += 32 * kPfSoftmaxWarps) {
+          const int r = vrows + idx / (D / 8), c = idx % (D / 8);
+          *reinterpret_cast<uint4 *>(vt + tile_chunk(kPfKeys, r, c)) = make_uint4(0u, 0u, 0u, 0u);
+        }
+        fence_proxy_async_smem();  // read next by the tensor core (asynchronous proxy)
       }
-      tc_commit(smem_u32(&bar_s));
-    }
-    // V rows at or past the sequence's length: zeroed (a masked p of 0 must not meet a stale value)
-    const int j0 = kt * kPfKeys;
-    const int vrows = min(kPfKeys, L - j0);
-    if (vrows < kPfKeys) {
-      unsigned char *vt = smem + C::V_OFF + buf * C::KV_TILE;
-      for (int idx = tid; idx < (kPfKeys - vrows) * (D / 8); idx += kPfThreads) {
-        const int r = vrows + idx / (D / 8), c = idx % (D / 8);
-        *reinterpret_cast<uint4 *>(vt + tile_chunk(kPfKeys, r, c)) = make_uint4(0u, 0u, 0u, 0u);
+      // this row's 64 scores, read once
+      float sv[kPfKeys];
+      tmem_ld64(tSk, sv);
+      // tiles short of every row's diagonal and of the sequence's end need no mask; in the
+      // others, keys from `vis` on are masked (this row's visible keys of the tile)
+      const bool full = j0 + kPfKeys <= kall;
+      const int vis = full ? kPfKeys : min(kPfKeys, max(0, lim - j0));
+      if (!full) {
+#pragma unroll
+        for (int i = 0; i < kPfKeys; ++i)
+          if (i >= vis) sv[i] = qscale >= 0.f ? -INFINITY : INFINITY;
       }
-      fence_proxy_async_smem();
-    }
-    // S is complete, and so is the previous P V product (P and O are touched next)
-    bool done = mbar_wait_bounded(smem_u32(&bar_s), (uint32_t)kt & 1u);
-    if (kt > 0) done = done && mbar_wait_bounded(smem_u32(&bar_o), (uint32_t)(kt - 1) & 1u);
-    if (!__syncthreads_and(done)) {
-      ok = false;
-      break;
-    }
-    tc_fence_after();
-    // buffer (kt+1)&1 is free: the P V product of kt-1, which read its V and P, is done
-    if (tid == 0 && kt + 1 < nkt && kt >= 1) load_kv(kt + 1);
-    // this row's 64 scores, read once
-    float sv[kPfKeys];
-    tmem_ld64(tS + lane_base, sv);
-    // tiles short of every row's diagonal and of the sequence's end need no mask
-    const bool full = j0 + kPfKeys <= kall;
-    const int vis = full ? kPfKeys : min(kPfKeys, max(0, lim - j0));  // this row's visible keys
-    // the row maximum, scaled to base 2 (the scale's sign decides which extreme)
-    float ext = qscale >= 0.f ? -INFINITY : INFINITY;
-    if (qscale >= 0.f) {
+      // the row maximum, scaled to base 2 (the scale's sign decides which extreme), in four
+      // independent chains
+      float e4[4];
+      if (qscale >= 0.f) {
 #pragma unroll
-      for (int i = 0; i < kPfKeys; ++i)
-        if (full || i < vis) ext = fmaxf(ext, sv[i]);
-    } else {
+        for (int j = 0; j < 4; ++j) e4[j] = fmaxf(sv[j], sv[j + 4]);
 #pragma unroll
-      for (int i = 0; i < kPfKeys; ++i)
-        if (full || i < vis) ext = fminf(ext, sv[i]);
-    }
-    const float mx = vis > 0 ? ext * qscale : -INFINITY;
-    const bool move = mx > m_ref + kRescaleGap || (m_ref == -INFINITY && mx > -INFINITY);
-    const float alpha = (move && m_ref != -INFINITY) ? exp2_approx(m_ref - mx) : 1.f;
-    if (move) {
-      l *= alpha;
-      m_ref = mx;
-    }
-    // TMEM loads and stores are warp-wide: a warp rescales when any of its rows must
-    if (kt > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+        for (int i = 8; i < kPfKeys; i += 4)
 #pragma unroll
-      for (int c = 0; c < D; c += 32) {
-        float o[32];
-        tmem_ld32(tO + lane_base + c, o);
+          for (int j = 0; j < 4; ++j) e4[j] = fmaxf(e4[j], sv[i + j]);
+      } else {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) o[i] *= alpha;
-        tmem_st32(tO + lane_base + c, o);
+        for (int j = 0; j < 4; ++j) e4[j] = fminf(sv[j], sv[j + 4]);
+#pragma unroll
+        for (int i = 8; i < kPfKeys; i += 4)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) e4[j] = fminf(e4[j], sv[i + j]);
       }
-    }
-    // P = 2^(s - m) in bf16 into the K-major swizzled P tile (row = this thread's query)
-    const float nbase = m_ref == -INFINITY ? 0.f : -m_ref;
-    uint32_t pk[kPfKeys / 2];
+      const float ext = qscale >= 0.f ? fmaxf(fmaxf(e4[0], e4[1]), fmaxf(e4[2], e4[3]))
+                                      : fminf(fminf(e4[0], e4[1]), fminf(e4[2], e4[3]));
+      const float mx = vis > 0 ? ext * qscale : -INFINITY;
+      const bool move = mx > m_ref + kRescaleGap || (m_ref == -INFINITY && mx > -INFINITY);
+      const float alpha = (move && m_ref != -INFINITY) ? exp2_approx(m_ref - mx) : 1.f;
+      if (move) {
+        l *= alpha;
+        m_ref = mx;
+      }
+      // a warp rescales its rows of O when any of them must, once the previous P V product
+      // is complete (TMEM loads and stores are warp-wide)
+      if (kt > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+        if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&bar_o), (uint32_t)(kt - 1) & 1u))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
 #pragma unroll
-    for (int i = 0; i < kPfKeys; i += 2) {
-      const float p0 = (full || i < vis) ? exp2_approx(fmaf(sv[i], qscale, nbase)) : 0.f;
-      const float p1 = (full || i + 1 < vis) ? exp2_approx(fmaf(sv[i + 1], qscale, nbase)) : 0.f;
-      l += p0 + p1;
-      pk[i / 2] = pack_bf16x2(p0, p1);
-    }
-    unsigned char *prow = smem + (pbuf - sb);
+        for (int c = 0; c < D; c += 32) {
+          float o[32];
+          tmem_ld32(tO + lane_base + c, o);
 #pragma unroll
-    for (int c = 0; c < kPfKeys / 8; ++c)
-      *reinterpret_cast<uint4 *>(prow + tile_chunk(kPfRows, row, c)) =
-          make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-    fence_proxy_async_smem();  // P is read by the tensor core (asynchronous proxy)
-    tc_fence_before();
-    __syncthreads();
-    if (tid == 0) {
-      tc_fence_after();
-      // O += P V over the tile's 64 keys in steps of 16: A = P (K-major, 32 bytes per step),
-      // B = V (MN-major: 16 keys = 16 rows of 128 bytes; the next 64 columns are the next
-      // region)
-#pragma unroll
-      for (int k = 0; k < kPfKeys / 16; ++k)
-        tc_mma(tO, smem_desc(pbuf + k * 32, 16, 1024), smem_desc(vbuf + k * 16 * 128, kKRegion, 1024), kIdO,
-               kt > 0 || k > 0);
-      tc_commit(smem_u32(&bar_o));
+          for (int i = 0; i < 32; ++i) o[i] *= alpha;
+          tmem_st32(tO + lane_base + c, o);
+        }
+      }
+      // P = 2^(s - m) as bf16 pairs over the S buffer's first 32 columns
+      const float nbase = m_ref == -INFINITY ? 0.f : -m_ref;
+      uint32_t pk[kPfKeys / 2];
+      if (full)
+        l += p_row<false>(sv, qscale, nbase, vis, pk);
+      else
+        l += p_row<true>(sv, qscale, nbase, vis, pk);
+      tmem_st32(tSk, pk);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&bar_p[b0]));
     }
+    // the last P V product is complete before O is read
+    if (ok && !__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&bar_o), (uint32_t)(nkt - 1) & 1u))) ok = false;
   }
-  if (nkt > 0) {
-    bool done = ok && mbar_wait_bounded(smem_u32(&bar_o), (uint32_t)(nkt - 1) & 1u);
-    if (!__syncthreads_and(done)) ok = false;
+  ok = __syncthreads_and(ok) != 0;
+  if (!ok && tid == kPfSoftmaxWarps * 32) {
+    // before shared memory and TMEM are released: the tensor-core products (one commit
+    // tracks them all) and the copies issued but never seen landed
+    tc_commit(smem_u32(&bar_fin));
+    mbar_wait_bounded(smem_u32(&bar_fin), 0);
+    if (nkt > 0 && !q_seen) mbar_wait_bounded(smem_u32(&bar_q), 0);
+    for (int kt = kw; kt < kq; ++kt) mbar_wait_bounded(smem_u32(&bar_k[kt & 1]), (uint32_t)(kt >> 1) & 1u);
+    for (int kt = vw; kt < vq; ++kt) mbar_wait_bounded(smem_u32(&bar_v[kt & 1]), (uint32_t)(kt >> 1) & 1u);
+    report(a.status, TD_DEV_WAIT_TIMEOUT);
   }
-  if (!ok && tid == 0) report(a.status, TD_DEV_WAIT_TIMEOUT);
+  __syncthreads();
   tc_fence_after();
-  // epilogue: O / l for this row, lse = m + log2(l) (natural-log units); the TMEM loads are
-  // warp-wide, so every thread takes part and only the stores depend on the row
-  const float inv = (ok && l > 0.f) ? 1.f / l : 0.f;
-  __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(a.out) + (((size_t)b * a.Hq + hq) * a.T + (row_valid ? t : 0)) * D;
+  if (warp < kPfSoftmaxWarps) {
+    // epilogue: O / l for this row, lse = m + log2(l) (natural-log units); the TMEM loads are
+    // warp-wide, so every thread takes part and only the stores depend on the row
+    const int row = tid, t = t0 + row;
+    const bool row_valid = t < a.T;
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const float inv = (ok && l > 0.f) ? 1.f / l : 0.f;
+    __nv_bfloat16 *orow =
+        static_cast<__nv_bfloat16 *>(a.out) + (((size_t)b * a.Hq + hq) * a.T + (row_valid ? t : 0)) * D;
 #pragma unroll
-  for (int c = 0; c < D; c += 32) {
-    float o[32];
-    if (nkt > 0) {
-      tmem_ld32(tO + lane_base + c, o);
-    } else {
+    for (int c = 0; c < D; c += 32) {
+      float o[32];
+      if (nkt > 0) {
+        tmem_ld32(tO + lane_base + c, o);
+      } else {
 #pragma unroll
-      for (int i = 0; i < 32; ++i) o[i] = 0.f;
+        for (int i = 0; i < 32; ++i) o[i] = 0.f;
+      }
+      if (row_valid) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) pk[i / 2] = pack_bf16x2(o[i] * inv, o[i + 1] * inv);
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          reinterpret_cast<uint4 *>(orow + c)[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+      }
     }
-    if (row_valid) {
-      uint32_t pk[16];
-#pragma unroll
-      for (int i = 0; i < 32; i += 2) pk[i / 2] = pack_bf16x2(o[i] * inv, o[i + 1] * inv);
-#pragma unroll
-      for (int q = 0; q < 4; ++q)
-        reinterpret_cast<uint4 *>(orow + c)[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
-    }
+    if (row_valid && a.lse != nullptr)
+      a.lse[((size_t)b * a.Hq + hq) * a.T + t] = (ok && l > 0.f) ? (m_ref + log2f(l)) * kLn2 : -INFINITY;
   }
-  if (row_valid && a.lse != nullptr)
-    a.lse[((size_t)b * a.Hq + hq) * a.T + t] = (ok && l > 0.f) ? (m_ref + log2f(l)) * kLn2 : -INFINITY;
   tc_fence_before();
   __syncthreads();
   if (warp == 0)
@@ -430,7 +524,7 @@ cudaError_t launch_prefill_d(PfArgs &a, const void *q, const void *k, const void
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, PfCfg<D>::SMEM);
   });
   if (attr != cudaSuccess) return attr;
-  const dim3 grid((unsigned)((a.T + kPfRows - 1) / kPfRows), (unsigned)a.Hq, (unsigned)a.B);
+  const dim3 grid((unsigned)(a.B * a.Hq), (unsigned)((a.T + kPfRows - 1) / kPfRows));
   return launch_pdl(prefill_kernel<D>, grid, dim3(kPfThreads), PfCfg<D>::SMEM, stream, a);
 }
 

@@ -272,10 +272,10 @@ td_status td_verify_attn_q8(const void *q, const int8_t *k_codes, const float *k
 /*
  * Prefill: query row (hq, t), t < T, attends keys j < L_b - T + t + 1, L_b = seq_lens[b]
  * clamped to [0, Smax] and counting the T new tokens (whose K/V rows must already be in the
- * cache): td_verify_attn's definition, for long chunks. bf16 only; D 64 or 128. One CTA per
- * 128 query rows of one query head; no workspace. q, out [B, Hq, T, D]; lse [B, Hq, T]
- * (nullable). Status bits as td_verify_attn; a bounded wait that gives up sets
- * TD_DEV_WAIT_TIMEOUT.
+ * cache): td_verify_attn's definition, for long chunks. bf16 only; D 64 or 128; T at most
+ * 65535 * 128 (TD_ERR_UNSUPPORTED beyond). One CTA per 128 query rows of one query head;
+ * no workspace. q, out [B, Hq, T, D]; lse [B, Hq, T] (nullable). Status bits as
+ * td_verify_attn; a bounded wait that gives up sets TD_DEV_WAIT_TIMEOUT.
  */
 td_status td_prefill_attn(const void *q, const void *k_cache, const void *v_cache, const int32_t *seq_lens, int B,
                           int Hq, int Hkv, int T, int Smax, int D, float scale, void *out, float *lse,

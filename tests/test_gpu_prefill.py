@@ -106,3 +106,18 @@ def test_prefill_4k_prompt_sampled_rows(td):
                                         case.scale)
         assert_out_close(out[:, hq:hq + 1, t], ref, "bf16", what=f"row ({hq}, {t})")
         assert_lse_close(lse[:, hq:hq + 1, t], ref_lse)
+
+
+@pytest.mark.parametrize("scale", [0.0, -0.05])
+def test_prefill_zero_and_negative_scale(td, scale):
+    """scale 0: each row is the mean of its visible values; a negative scale turns the row
+    minimum into the softmax's reference (both through masked and unmasked tiles)."""
+    case = small_case(dtype="bf16", B=1, Hq=4, Hkv=2, D=128, Smax=400, T=300, seq_lens=[390], seed=8)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out, lse = td.td_prefill_attn(case.q.cuda(), case.k_cache.cuda(), case.v_cache.cuda(), case.seq_lens.cuda(),
+                                  scale, dev_status=st, return_lse=True)
+    torch.cuda.synchronize()
+    ref, ref_lse, _ = oracle.load().attention(to_numpy(case.q), to_numpy(case.k_cache), to_numpy(case.v_cache),
+                                              case.seq_lens.numpy(), scale)
+    assert_out_close(out.cpu(), ref, "bf16")
+    assert_lse_close(lse.cpu(), ref_lse)
