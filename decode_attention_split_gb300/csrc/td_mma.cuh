@@ -65,6 +65,19 @@ __device__ __forceinline__ float exp2_approx(float x) {
   return y;
 }
 
+// Three-input maximum / minimum (one instruction each).
+__device__ __forceinline__ float fmax3f(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+__device__ __forceinline__ float fmin3f(float a, float b, float c) {
+  float d;
+  asm("min.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 // Packed fp32 pairs (fma.rn.f32x2 / add.rn.f32x2: two lanes per instruction, each rounded
 // as its scalar form).
 __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {

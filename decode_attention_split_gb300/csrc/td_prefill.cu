@@ -186,6 +186,20 @@ __device__ __forceinline__ float p_row(const float (&sv)[kPfKeys], float qscale,
   return t.x + t.y;
 }
 
+// The largest (MIN: smallest) of a row's 64 scores.
+template <bool MIN>
+__device__ __forceinline__ float row_extreme(const float (&sv)[kPfKeys]) {
+  float e[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const float *v = sv + 8 * j;
+    e[j] = MIN ? fmin3f(fmin3f(v[0], v[1], v[2]), fmin3f(v[3], v[4], v[5]), fminf(v[6], v[7]))
+               : fmax3f(fmax3f(v[0], v[1], v[2]), fmax3f(v[3], v[4], v[5]), fmaxf(v[6], v[7]));
+  }
+  return MIN ? fmin3f(fmin3f(e[0], e[1], e[2]), fmin3f(e[3], e[4], e[5]), fminf(e[6], e[7]))
+             : fmax3f(fmax3f(e[0], e[1], e[2]), fmax3f(e[3], e[4], e[5]), fmaxf(e[6], e[7]));
+}
+
 // Byte offset of 16-byte chunk c of row r in a tile of `rows` rows kept as 128-byte-swizzled
 // regions of 64 bf16 columns (the layout TMA writes and the tensor core reads as K-major).
 __device__ __forceinline__ uint32_t tile_chunk(int rows, int r, int c) {
@@ -376,26 +390,9 @@ __global__ void __launch_bounds__(kPfThreads, 2) prefill_kernel(const __grid_con
         for (int i = 0; i < kPfKeys; ++i)
           if (i >= vis) sv[i] = qscale >= 0.f ? -INFINITY : INFINITY;
       }
-      // the row maximum, scaled to base 2 (the scale's sign decides which extreme), in four
-      // independent chains
-      float e4[4];
-      if (qscale >= 0.f) {
-#pragma unroll
-        for (int j = 0; j < 4; ++j) e4[j] = fmaxf(sv[j], sv[j + 4]);
-#pragma unroll
-        for (int i = 8; i < kPfKeys; i += 4)
-#pragma unroll
-          for (int j = 0; j < 4; ++j) e4[j] = fmaxf(e4[j], sv[i + j]);
-      } else {
-#pragma unroll
-        for (int j = 0; j < 4; ++j) e4[j] = fminf(sv[j], sv[j + 4]);
-#pragma unroll
-        for (int i = 8; i < kPfKeys; i += 4)
-#pragma unroll
-          for (int j = 0; j < 4; ++j) e4[j] = fminf(e4[j], sv[i + j]);
-      }
-      const float ext = qscale >= 0.f ? fmaxf(fmaxf(e4[0], e4[1]), fmaxf(e4[2], e4[3]))
-                                      : fminf(fminf(e4[0], e4[1]), fminf(e4[2], e4[3]));
+      // the row maximum, scaled to base 2 (the scale's sign decides which extreme): eight
+      // independent chains of three-input steps
+      const float ext = qscale >= 0.f ? row_extreme<false>(sv) : row_extreme<true>(sv);
       const float mx = vis > 0 ? ext * qscale : -INFINITY;
       const bool move = mx > m_ref + kRescaleGap || (m_ref == -INFINITY && mx > -INFINITY);
       const float alpha = (move && m_ref != -INFINITY) ? exp2_approx(m_ref - mx) : 1.f;
