@@ -61,6 +61,11 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--profile-launches", type=int, default=0,
                     help="profiling mode: W warm-up calls then this many plain launches, no graphs, no JSON extras")
+    ap.add_argument("--profile-row", default=None, choices=["q8", "prefill"],
+                    help="profiling mode for a NEXT row's kernel instead of the timed step's call: q8 = "
+                         "td_decode_attn_q8 on the 3B-style layer at --seq-len with --profile-batch sequences "
+                         "(cache quantised on the GPU); prefill = td_prefill_attn on a --seq-len-token prompt")
+    ap.add_argument("--profile-batch", type=int, default=4)
     return ap.parse_args()
 
 
@@ -400,6 +405,34 @@ def sweep_point(td, name, L, dev, l2_bytes, peak, budget_calls=200):
             "cache_copies": C}
 
 
+def profile_row(td, args, dev):
+    """Plain launches of one NEXT row's kernel (W warm-up, then --profile-launches), no timing."""
+    g = torch.Generator(device=dev).manual_seed(0)
+    w = WORKLOADS["llama3b"]
+    L, B = args.seq_len, args.profile_batch
+    if args.profile_row == "q8":
+        k = torch.randn(B, w.Hkv, L, w.D, device=dev, generator=g).to(torch.bfloat16)
+        v = torch.randn(B, w.Hkv, L, w.D, device=dev, generator=g).to(torch.bfloat16)
+        q = torch.randn(B, w.Hq, w.D, device=dev, generator=g).to(torch.bfloat16)
+        kc, ks = td.td_quantize_q8(k)
+        vc, vs = td.td_quantize_q8(v)
+        del k, v
+        seq = torch.full((B,), L, dtype=torch.int32, device=dev)
+        call = lambda: td.td_decode_attn_q8(q, kc, ks, vc, vs, seq, w.D ** -0.5)  # noqa: E731
+    else:
+        q = torch.randn(B, w.Hq, L, w.D, device=dev, generator=g).to(torch.bfloat16)
+        k = torch.randn(B, w.Hkv, L, w.D, device=dev, generator=g).to(torch.bfloat16)
+        v = torch.randn(B, w.Hkv, L, w.D, device=dev, generator=g).to(torch.bfloat16)
+        seq = torch.full((B,), L, dtype=torch.int32, device=dev)
+        out = torch.empty_like(q)
+        call = lambda: td.td_prefill_attn(q, k, v, seq, out=out)  # noqa: E731
+    for _ in range(args.warmup + args.profile_launches):
+        call()
+    torch.cuda.synchronize(dev)
+    print(json.dumps({"profile_row": args.profile_row, "seq_len": L, "batch": B,
+                      "launches": args.warmup + args.profile_launches, "ok": True}))
+
+
 def run_td(args, world, rank, local):
     from decode_attention_split_gb300 import build
     build.build()
@@ -407,6 +440,9 @@ def run_td(args, world, rank, local):
 
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
+    if args.profile_row:
+        profile_row(td, args, dev)
+        return
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
