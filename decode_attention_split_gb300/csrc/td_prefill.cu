@@ -8,8 +8,9 @@
 //
 // GB300 design: one CTA per tile of 128 query rows of one query head, two CTAs per SM. Q, K
 // and V tiles cross by TMA with the 128-byte swizzle (K and V double-buffered with their own
-// barriers, 64 keys per tile). A fifth warp issues the copies and the tensor-core products;
-// the accumulators live in TMEM:
+// barriers, 64 keys per tile). A fifth warp issues the tensor-core products and a sixth the
+// copies (a copy waits for its buffer's previous product, which must not hold up the next
+// product's issue); the accumulators live in TMEM:
 //   S[128 x 64] = Q K^T     (A = Q, B = K, both K-major in shared memory)  -> S buffer kt % 2
 //   O[128 x D] += P V       (A = P in TMEM, B = V MN-major in shared memory) -> O
 // S is double-buffered (TMEM columns [0, 64) and [64, 128), O from column 128), so the
@@ -38,8 +39,10 @@ namespace td {
 
 namespace {
 
-constexpr int kPfSoftmaxWarps = 4;             // one query row per thread
-constexpr int kPfThreads = 32 * (kPfSoftmaxWarps + 1);  // + the copy / tensor-core warp
+constexpr int kPfSoftmaxWarps = 4;                         // one query row per thread
+constexpr int kPfMmaWarp = kPfSoftmaxWarps;                  // issues the tensor-core products
+constexpr int kPfLoadWarp = kPfSoftmaxWarps + 1;             // issues the TMA copies
+constexpr int kPfThreads = 32 * (kPfSoftmaxWarps + 2);
 constexpr int kPfRows = 128;   // query rows per CTA
 constexpr int kPfKeys = 64;    // keys per tile
 constexpr int kQRegion = kPfRows * 128;  // bytes of one swizzled [128 rows][64 bf16] region
@@ -210,8 +213,9 @@ template <int D>
 __global__ void __launch_bounds__(kPfThreads, 2) prefill_kernel(const __grid_constant__ PfArgs a) {
   using C = PfCfg<D>;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
-  __shared__ __align__(8) uint64_t bar_q, bar_k[2], bar_v[2], bar_s[2], bar_p[2], bar_o, bar_fin;
+  __shared__ __align__(8) uint64_t bar_q, bar_k[2], bar_v[2], bar_s[2], bar_p[2], bar_vfree[2], bar_o, bar_fin;
   __shared__ uint32_t s_taddr;
+  __shared__ int s_issued[2], s_seen[3];  // wind-down: K / V tiles issued; K / V tiles, Q seen landed
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   unsigned char *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sb = smem_u32(smem);
@@ -230,7 +234,11 @@ __global__ void __launch_bounds__(kPfThreads, 2) prefill_kernel(const __grid_con
       mbar_init(smem_u32(&bar_v[i]), 1);
       mbar_init(smem_u32(&bar_s[i]), 1);
       mbar_init(smem_u32(&bar_p[i]), kPfSoftmaxWarps);
+      mbar_init(smem_u32(&bar_vfree[i]), 1);
     }
+    s_issued[0] = s_issued[1] = 0;
+    s_seen[0] = s_seen[1] = 0;
+    s_seen[2] = 1;
     mbar_init(smem_u32(&bar_o), 1);
     mbar_init(smem_u32(&bar_fin), 1);
     fence_mbar_init();
@@ -269,11 +277,67 @@ __global__ void __launch_bounds__(kPfThreads, 2) prefill_kernel(const __grid_con
   bool q_seen = false;
   float m_ref = -INFINITY, l = 0.f;  // softmax threads: this row's reference maximum and sum
 
-  if (warp == kPfSoftmaxWarps) {
+  if (warp == kPfMmaWarp) {
     if (lane == 0 && nkt > 0) {
-      const int zq = b * a.Hq + hq, zk = b * a.Hkv + kvh;
       constexpr uint32_t kIdS = mma_idesc(kPfRows, kPfKeys, false);
       constexpr uint32_t kIdO = mma_idesc(kPfRows, D, true);
+      // shared-memory descriptors of Q and of K / V buffer 0; any other tile, buffer or k
+      // step differs only in its start address (descriptor field in 16-byte units)
+      const uint64_t dq = smem_desc(sb + C::Q_OFF, 16, 1024);
+      const uint64_t dk = smem_desc(sb + C::K_OFF, 16, 1024);
+      const uint64_t dv = smem_desc(sb + C::V_OFF, kKRegion, 1024);
+      // S of tile kt into S buffer kt % 2 (K tile kt has landed): over D in steps of 16 (32
+      // bytes along a swizzled row; the next 64 columns are the next region)
+      auto issue_s = [&](int kt) {
+        const uint32_t kb = (uint32_t)(kt & 1) * C::KV_TILE;
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t off = (uint32_t)(k & 3) * 32;
+          tc_mma(tS + (kt & 1) * kPfKeys, dq + (((uint32_t)(k >> 2) * kQRegion + off) >> 4),
+                 dk + ((kb + (uint32_t)(k >> 2) * kKRegion + off) >> 4), kIdS, k > 0);
+        }
+        tc_commit(smem_u32(&bar_s[kt & 1]));
+      };
+      q_seen = mbar_wait_bounded(smem_u32(&bar_q), 0);
+      ok = q_seen && mbar_wait_bounded(smem_u32(&bar_k[0]), 0);
+      if (ok) {
+        kw = 1;
+        issue_s(0);
+      }
+      for (int kt = 0; ok && kt < nkt; ++kt) {
+        const int b0 = kt & 1, b1 = b0 ^ 1;
+        if (kt + 1 < nkt) {
+          // S buffer b1 (P of kt-1) is free once the P V product of kt-1 is done
+          if (kt >= 1) ok = mbar_wait_bounded(smem_u32(&bar_o), (uint32_t)(kt - 1) & 1u);
+          ok = ok && mbar_wait_bounded(smem_u32(&bar_k[b1]), (uint32_t)((kt + 1) >> 1) & 1u);
+          if (!ok) break;
+          kw = kt + 2;
+          issue_s(kt + 1);
+        }
+        // P of kt is in TMEM (all four softmax warps) and V of kt has landed: O += P V over
+        // 64 keys in steps of 16 (A: 8 TMEM columns per step; B: MN-major, 16 rows of 128
+        // bytes per step, the next 64 columns in the next region)
+        ok = mbar_wait_bounded(smem_u32(&bar_p[b0]), (uint32_t)(kt >> 1) & 1u) &&
+             mbar_wait_bounded(smem_u32(&bar_v[b0]), (uint32_t)(kt >> 1) & 1u);
+        if (!ok) break;
+        vw = kt + 1;
+        tc_fence_after();
+        const uint32_t vb = (uint32_t)b0 * C::KV_TILE;
+#pragma unroll
+        for (int k = 0; k < kPfKeys / 16; ++k)
+          tc_mma_ts(tO, tS + b0 * kPfKeys + 8 * k, dv + ((vb + (uint32_t)k * 16 * 128) >> 4), kIdO, kt > 0 || k > 0);
+        tc_commit(smem_u32(&bar_o));
+        tc_commit(smem_u32(&bar_vfree[b0]));  // V buffer b0 may be refilled
+      }
+      s_seen[0] = kw;
+      s_seen[1] = vw;
+      s_seen[2] = q_seen;
+    }
+    __syncwarp();
+  } else if (warp == kPfLoadWarp) {
+    if (lane == 0 && nkt > 0) {
+      const int zq = b * a.Hq + hq, zk = b * a.Hkv + kvh;
       auto load = [&](bool v, int kt) {  // K or V tile kt into buffer kt % 2
         const int buf = kt & 1;
         const uint32_t bar = smem_u32(v ? &bar_v[buf] : &bar_k[buf]);
@@ -281,19 +345,6 @@ __global__ void __launch_bounds__(kPfThreads, 2) prefill_kernel(const __grid_con
         mbar_arrive_expect_tx(bar, C::KV_TILE);
 #pragma unroll
         for (int h = 0; h < C::HALVES; ++h) tma3(dst + h * kKRegion, v ? &a.vmap : &a.kmap, 64 * h, kt * kPfKeys, zk, bar);
-      };
-      // S of tile kt into S buffer kt % 2 (K tile kt has landed): over D in steps of 16 (32
-      // bytes along a swizzled row; the next 64 columns are the next region)
-      auto issue_s = [&](int kt) {
-        const uint32_t kbuf = sb + C::K_OFF + (kt & 1) * C::KV_TILE;
-        tc_fence_after();
-#pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
-          const uint32_t col = (k & 3) * 32;
-          tc_mma(tS + (kt & 1) * kPfKeys, smem_desc(sb + C::Q_OFF + (k >> 2) * kQRegion + col, 16, 1024),
-                 smem_desc(kbuf + (k >> 2) * kKRegion + col, 16, 1024), kIdS, k > 0);
-        }
-        tc_commit(smem_u32(&bar_s[kt & 1]));
       };
       {
         const uint32_t bar = smem_u32(&bar_q);
@@ -306,44 +357,20 @@ __global__ void __launch_bounds__(kPfThreads, 2) prefill_kernel(const __grid_con
         load(true, kq);
       }
       vq = kq;
-      q_seen = mbar_wait_bounded(smem_u32(&bar_q), 0);
-      ok = q_seen && mbar_wait_bounded(smem_u32(&bar_k[0]), 0);
-      if (ok) {
-        kw = 1;
-        issue_s(0);
-      }
-      for (int kt = 0; ok && kt < nkt; ++kt) {
-        const int b0 = kt & 1, b1 = b0 ^ 1;
-        if (kt + 1 < nkt) {
-          // S buffer b1 and V buffer b1 are free once the P V product of kt-1 is done
-          if (kt >= 1) ok = mbar_wait_bounded(smem_u32(&bar_o), (uint32_t)(kt - 1) & 1u);
-          ok = ok && mbar_wait_bounded(smem_u32(&bar_k[b1]), (uint32_t)((kt + 1) >> 1) & 1u);
-          if (!ok) break;
-          kw = kt + 2;
-          issue_s(kt + 1);
-          if (kt >= 1) load(true, vq++);  // V tile kt+1
-        }
-        if (kt + 2 < nkt) {
-          // K buffer b0 is free once S of kt is done
-          ok = mbar_wait_bounded(smem_u32(&bar_s[b0]), (uint32_t)(kt >> 1) & 1u);
-          if (!ok) break;
-          load(false, kq++);  // K tile kt+2
-        }
-        // P of kt is in TMEM (all four softmax warps) and V of kt has landed: O += P V over
-        // 64 keys in steps of 16 (A: 8 TMEM columns per step; B: MN-major, 16 rows of 128
-        // bytes per step, the next 64 columns in the next region)
-        ok = mbar_wait_bounded(smem_u32(&bar_p[b0]), (uint32_t)(kt >> 1) & 1u) &&
-             mbar_wait_bounded(smem_u32(&bar_v[b0]), (uint32_t)(kt >> 1) & 1u);
+      // tile j (j >= 2) goes to buffer j % 2 once its previous user, tile j-2, is done with
+      // it: K after the product S of j-2, V after the P V product of j-2. Each buffer's next
+      // product needs the copy issued here, so its barrier cannot run a phase ahead.
+      for (int j = 2; ok && j < nkt; ++j) {
+        const uint32_t ph = (uint32_t)((j - 2) >> 1) & 1u;
+        ok = mbar_wait_bounded(smem_u32(&bar_s[j & 1]), ph);
         if (!ok) break;
-        vw = kt + 1;
-        tc_fence_after();
-        const uint32_t vbuf = sb + C::V_OFF + b0 * C::KV_TILE;
-#pragma unroll
-        for (int k = 0; k < kPfKeys / 16; ++k)
-          tc_mma_ts(tO, tS + b0 * kPfKeys + 8 * k, smem_desc(vbuf + k * 16 * 128, kKRegion, 1024), kIdO,
-                    kt > 0 || k > 0);
-        tc_commit(smem_u32(&bar_o));
+        load(false, kq++);
+        ok = mbar_wait_bounded(smem_u32(&bar_vfree[j & 1]), ph);
+        if (!ok) break;
+        load(true, vq++);
       }
+      s_issued[0] = kq;
+      s_issued[1] = vq;
     }
     __syncwarp();
   } else if (nkt > 0) {
@@ -433,15 +460,21 @@ __global__ void __launch_bounds__(kPfThreads, 2) prefill_kernel(const __grid_con
     if (ok && !__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&bar_o), (uint32_t)(nkt - 1) & 1u))) ok = false;
   }
   ok = __syncthreads_and(ok) != 0;
-  if (!ok && tid == kPfSoftmaxWarps * 32) {
+  if (!ok) {
     // before shared memory and TMEM are released: the tensor-core products (one commit
     // tracks them all) and the copies issued but never seen landed
-    tc_commit(smem_u32(&bar_fin));
-    mbar_wait_bounded(smem_u32(&bar_fin), 0);
-    if (nkt > 0 && !q_seen) mbar_wait_bounded(smem_u32(&bar_q), 0);
-    for (int kt = kw; kt < kq; ++kt) mbar_wait_bounded(smem_u32(&bar_k[kt & 1]), (uint32_t)(kt >> 1) & 1u);
-    for (int kt = vw; kt < vq; ++kt) mbar_wait_bounded(smem_u32(&bar_v[kt & 1]), (uint32_t)(kt >> 1) & 1u);
-    report(a.status, TD_DEV_WAIT_TIMEOUT);
+    if (tid == kPfMmaWarp * 32) {
+      tc_commit(smem_u32(&bar_fin));
+      mbar_wait_bounded(smem_u32(&bar_fin), 0);
+    }
+    if (tid == kPfLoadWarp * 32) {
+      if (nkt > 0 && !s_seen[2]) mbar_wait_bounded(smem_u32(&bar_q), 0);
+      for (int kt = s_seen[0]; kt < s_issued[0]; ++kt)
+        mbar_wait_bounded(smem_u32(&bar_k[kt & 1]), (uint32_t)(kt >> 1) & 1u);
+      for (int kt = s_seen[1]; kt < s_issued[1]; ++kt)
+        mbar_wait_bounded(smem_u32(&bar_v[kt & 1]), (uint32_t)(kt >> 1) & 1u);
+      report(a.status, TD_DEV_WAIT_TIMEOUT);
+    }
   }
   __syncthreads();
   tc_fence_after();
