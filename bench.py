@@ -29,6 +29,7 @@ import hashlib
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -88,9 +89,20 @@ def measured_peaks():
 
 
 def kernel_source_hash() -> str:
-    h = hashlib.sha256()
+    """Hash of the sources the timed decode kernel is built from: the translation units that
+    define and launch it (td_split_attn.cu, td_api.cu) with every header they include,
+    transitively, and td.h."""
     src = os.path.join(ROOT, "decode_attention_split_gb300", "csrc")
-    for name in sorted(os.listdir(src)):
+    seen, todo = set(), ["td_split_attn.cu", "td_api.cu"]
+    while todo:
+        name = todo.pop()
+        if name in seen or not os.path.exists(os.path.join(src, name)):
+            continue
+        seen.add(name)
+        with open(os.path.join(src, name)) as f:
+            todo += re.findall(r'^#include "([^"]+)"', f.read(), flags=re.M)
+    h = hashlib.sha256()
+    for name in sorted(seen):
         with open(os.path.join(src, name), "rb") as f:
             h.update(name.encode() + f.read())
     with open(os.path.join(ROOT, "include", "td.h"), "rb") as f:
