@@ -92,7 +92,25 @@ cudaError_t launch_mma(const SplitParams &p, int grid, int smem, cudaStream_t st
   if (!encode_cache_map(&a.kmap, p.k, p.B, p.Hkv, p.Smax, D) || !encode_cache_map(&a.vmap, p.v, p.B, p.Hkv, p.Smax, D))
     return cudaErrorInvalidValue;
   a.p = p;
-  return launch_pdl(split_attn_mma_kernel<D>, dim3(grid), dim3(kThreads), smem, stream, a);
+  if (p.RB == 1) {
+    // the decode instantiation: its shared-memory opt-in, once per device (the plan's
+    // occupancy query set the other's)
+    static std::mutex mu;
+    static bool done[kMaxDevices] = {};
+    int device = 0;
+    if (cudaGetDevice(&device) != cudaSuccess || device < 0 || device >= kMaxDevices) return cudaErrorInvalidDevice;
+    {
+      std::lock_guard<std::mutex> lock(mu);
+      if (!done[device]) {
+        const cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void *>(&split_attn_mma_kernel<D, true>),
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        done[device] = true;
+      }
+    }
+    return launch_pdl(split_attn_mma_kernel<D, true>, dim3(grid), dim3(kThreads), smem, stream, a);
+  }
+  return launch_pdl(split_attn_mma_kernel<D, false>, dim3(grid), dim3(kThreads), smem, stream, a);
 }
 
 template <int D>
@@ -100,7 +118,7 @@ KernelRef mma_ref_of() {
   // the ring plus 1024 bytes of slack for its alignment
   constexpr int smem = MmaCfg<D, kPersistentStages<D>>::RING_BYTES + 1024;
   static_assert(smem + 8448 <= 227 * 1024, "mma kernel shared memory");
-  return KernelRef{reinterpret_cast<const void *>(&split_attn_mma_kernel<D>), smem, &launch_mma<D>};
+  return KernelRef{reinterpret_cast<const void *>(&split_attn_mma_kernel<D, false>), smem, &launch_mma<D>};
 }
 
 KernelRef pick_mma(int D, int MT) {

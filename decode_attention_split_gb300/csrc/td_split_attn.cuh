@@ -136,7 +136,8 @@ __device__ __forceinline__ int first_chunk_size(const SplitParams &p, long long 
 // Exclusive prefix over the per-sequence item counts, computed by the whole CTA.
 // s_len[b] receives the clamped length; returns the chunk size through *s_chunk and the
 // item total in s_prefix[B]. s_red holds 2 * kWarps values.
-static __device__ void plan_items(const SplitParams &p, int *s_len, int *s_prefix, int *s_chunk, long long *s_red) {
+static __device__ void plan_items(const SplitParams &p, int *s_len, int *s_prefix, int *s_chunk, long long *s_red,
+                                  bool report_bits = true) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int U = p.Hkv * p.RB;
   constexpr int kSeg = (TD_MAX_BATCH + kThreads - 1) / kThreads;
@@ -148,13 +149,15 @@ static __device__ void plan_items(const SplitParams &p, int *s_len, int *s_prefi
   for (int i = 0; i < kSeg; ++i) {
     const int b = b0 + i;
     if (b < p.B) {
-      const int L = attended_len(p, p.seq_lens[b], bits);
+      // before the wait for the previous kernel the lengths may be written meanwhile: read
+      // them where that kernel's writes land, not through L1
+      const int L = attended_len(p, report_bits ? p.seq_lens[b] : ld_relaxed(p.seq_lens + b), bits);
       s_len[b] = L;
       tot += L;
       lmax = max(lmax, L);
     }
   }
-  if (blockIdx.x == 0) report(p.status, bits);
+  if (report_bits && blockIdx.x == 0) report(p.status, bits);
   // total keys over the batch
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
@@ -222,6 +225,27 @@ static __device__ void plan_items(const SplitParams &p, int *s_len, int *s_prefi
     break;
   }
   __syncthreads();
+}
+
+// The plan made before the wait for the previous kernel (from lengths that kernel may still
+// have been writing) is kept after the wait if every attended length reads the same now: the
+// plan is a function of those lengths alone. Otherwise it is made again. Either way the
+// status bits come from the lengths as read after the wait. Ends with a __syncthreads.
+static __device__ void confirm_plan(const SplitParams &p, int *s_len, int *s_prefix, int *s_chunk, long long *s_red) {
+  constexpr int kSeg = (TD_MAX_BATCH + kThreads - 1) / kThreads;
+  const int b0 = threadIdx.x * kSeg;
+  uint32_t bits = 0;
+  bool same = true;
+#pragma unroll
+  for (int i = 0; i < kSeg; ++i) {
+    const int b = b0 + i;
+    if (b < p.B) same = attended_len(p, ld_relaxed(p.seq_lens + b), bits) == s_len[b] && same;
+  }
+  if (__syncthreads_and(same)) {
+    if (blockIdx.x == 0) report(p.status, bits);
+    return;
+  }
+  plan_items(p, s_len, s_prefix, s_chunk, s_red);  // ends with __syncthreads
 }
 
 // Fused step with advance: the last CTA of the grid to have read the lengths moves every
@@ -467,9 +491,11 @@ __global__ void __launch_bounds__(kThreads, 2) split_attn_kernel(const SplitPara
     fence_mbar_init();
   }
   uint32_t merge_phase = 0;
+  // a plan on the lengths as they read now, kept after the wait if they read the same then
+  plan_items(p, s_len, s_prefix, &s_chunk, s_red, false);
   griddep_wait();  // inputs may come from the previous kernel in the stream
   griddep_launch_dependents();
-  plan_items(p, s_len, s_prefix, &s_chunk, s_red);  // ends with __syncthreads
+  confirm_plan(p, s_len, s_prefix, &s_chunk, s_red);  // ends with __syncthreads
 
   const int S = s_chunk;
   const int W = s_prefix[p.B];

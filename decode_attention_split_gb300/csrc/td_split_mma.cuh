@@ -465,7 +465,11 @@ __device__ __forceinline__ unsigned char *align1024(unsigned char *p) {
 
 // Persistent kernel: CTAs walk the work items of plan_items; chunk partials meet in the
 // workspace and the CTA that completes a group's last chunk merges them (finish_item).
-template <int D>
+// EARLY_PLAN (launched when one row block covers a kv head, i.e. decode): the plan is made
+// on the lengths as they read before the wait for the previous kernel and kept after it if
+// they read the same then (measured on the 3B-style layer: 4k 11.4 -> 10.5 us, 32k 25.7 ->
+// 25.5 us). The other instantiation plans after the wait.
+template <int D, bool EARLY_PLAN>
 __global__ void __launch_bounds__(kThreads, 2) split_attn_mma_kernel(const __grid_constant__ MmaArgs a) {
   constexpr int NST = kPersistentStages<D>;
   using C = MmaCfg<D, NST>;
@@ -493,9 +497,13 @@ __global__ void __launch_bounds__(kThreads, 2) split_attn_mma_kernel(const __gri
   uint32_t merge_phase = 0;
   uint32_t seq = 0;
   if (tid == 0) prefetch_first_item<D>(p, prefetch_stages(p));
+  if constexpr (EARLY_PLAN) plan_items(p, s_len, s_prefix, &s_chunk, s_red, false);
   griddep_wait();  // inputs may come from the previous kernel in the stream
   griddep_launch_dependents();
-  plan_items(p, s_len, s_prefix, &s_chunk, s_red);  // ends with __syncthreads
+  if constexpr (EARLY_PLAN)
+    confirm_plan(p, s_len, s_prefix, &s_chunk, s_red);  // ends with __syncthreads
+  else
+    plan_items(p, s_len, s_prefix, &s_chunk, s_red);  // ends with __syncthreads
   advance_after_reads(p, &s_last);  // fused step: the lengths move on once every CTA has read them
   const int S = s_chunk;
   const int W = s_prefix[p.B];
