@@ -89,17 +89,17 @@ def test_prefill_matches_verify_kernel(td):
     assert_out_close(out, ver.cpu().double().numpy(), "bf16", what="prefill vs verify kernel")
 
 
-def test_prefill_4k_prompt_sampled_rows(td):
-    """A 4096-token prompt of the 3B-style layer; 40 sampled (head, row) pairs in the oracle."""
-    T = 4096
+@pytest.mark.parametrize("T", [4096, 8192])
+def test_prefill_long_prompt_sampled_rows(td, T):
+    """The prompts the bench line times (3B-style layer); 40 sampled (head, row) pairs in the oracle."""
     case = small_case(dtype="bf16", B=1, Hq=24, Hkv=8, D=128, Smax=T, T=T, seq_lens=[T], seed=6, heavy=0.01)
     out, lse, st = _run(td, case)
     assert st == 0
     rng = np.random.default_rng(0)
     orc = oracle.load()
     kn, vn = to_numpy(case.k_cache), to_numpy(case.v_cache)
-    for _ in range(40):
-        hq, t = int(rng.integers(0, 24)), int(rng.integers(0, T))
+    picks = [(0, 0), (23, T - 1), (5, T - 64)] + [(int(rng.integers(0, 24)), int(rng.integers(0, T))) for _ in range(37)]
+    for hq, t in picks:  # the first row, the last rows of the prompt, then random ones
         kvh = hq // 3
         qrow = to_numpy(case.q[:, hq:hq + 1, t])  # [1, 1, D]
         ref, ref_lse, _ = orc.attention(qrow, kn[:, kvh:kvh + 1], vn[:, kvh:kvh + 1], np.array([t + 1], np.int32),
