@@ -631,36 +631,39 @@ def run_td(args, world, rank, local):
 
 
 def run_e2e(td, args, w, case, kc, vc, C, R, sl_pre, sl_post, ws, dev, bytes_call, world):
-    """Through the public Python API with host buffers: per call H2D of q and the new rows, D2H of out."""
+    """Through the public Python API with host buffers: each step copies its R calls' inputs (q and
+    the new rows, packed in one pinned buffer) to the device in one transfer, makes the R calls,
+    and reads all R outputs back in one transfer."""
     steps = max(1, min(args.steps, 10))
     gen = torch.Generator().manual_seed(2)
-    qh = torch.randn(R, w.B, w.Hq, w.D, generator=gen).to(torch.bfloat16).pin_memory()
-    knh = torch.randn(R, w.B, w.Hkv, 1, w.D, generator=gen).to(torch.bfloat16).pin_memory()
-    vnh = torch.randn(R, w.B, w.Hkv, 1, w.D, generator=gen).to(torch.bfloat16).pin_memory()
-    outh = torch.empty(R, w.B, w.Hq, w.D, dtype=torch.bfloat16).pin_memory()
-    qd = torch.empty(w.B, w.Hq, w.D, dtype=torch.bfloat16, device=dev)
-    knd = torch.empty(w.B, w.Hkv, 1, w.D, dtype=torch.bfloat16, device=dev)
-    vnd = torch.empty_like(knd)
-    outd = torch.empty_like(qd)
+    nq, nk = w.B * w.Hq * w.D, w.B * w.Hkv * w.D
+    per = nq + 2 * nk  # bf16 elements of one call's inputs: q, k_new, v_new
+    inh = torch.randn(R, per, generator=gen).to(torch.bfloat16).pin_memory()
+    outh = torch.empty(R, nq, dtype=torch.bfloat16).pin_memory()
+    ind = torch.empty(R, per, dtype=torch.bfloat16, device=dev)
+    outd = torch.empty(R, nq, dtype=torch.bfloat16, device=dev)
+    # per-call views of the packed device buffers (contiguous), made once
+    views = [(ind[i, :nq].view(w.B, w.Hq, 1, w.D), ind[i, nq:nq + nk].view(w.B, w.Hkv, 1, w.D),
+              ind[i, nq + nk:].view(w.B, w.Hkv, 1, w.D), outd[i].view(w.B, w.Hq, 1, w.D)) for i in range(R)]
     s = torch.cuda.Stream(dev)
 
     def one_step():
         with torch.cuda.stream(s):
+            ind.copy_(inh, non_blocking=True)
             for i in range(R):
-                c = i % C
-                qd.copy_(qh[i], non_blocking=True)
-                knd.copy_(knh[i], non_blocking=True)
-                vnd.copy_(vnh[i], non_blocking=True)
-                td.td_rope_append_attn(qd[:, :, None], knd, vnd, kc[c], vc[c], sl_pre, case.scale, 0, advance=False,
-                                       out=outd[:, :, None], workspace=ws, stream=s)
-                outh[i].copy_(outd, non_blocking=True)
+                q, kn, vn, o = views[i]
+                td.td_rope_append_attn(q, kn, vn, kc[i % C], vc[i % C], sl_pre, case.scale, 0, advance=False,
+                                       out=o, workspace=ws, stream=s)
+            outh.copy_(outd, non_blocking=True)
 
     one_step()
     s.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(s)
+    t0 = time.perf_counter()
     for _ in range(steps):
         one_step()
+    host_s = time.perf_counter() - t0
     e1.record(s)
     e1.synchronize()
     ms = e0.elapsed_time(e1)
@@ -668,11 +671,12 @@ def run_e2e(td, args, w, case, kc, vc, C, R, sl_pre, sl_post, ws, dev, bytes_cal
         t = torch.tensor([ms], dtype=torch.float64, device=dev)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         ms = float(t[0])
-    per_call_in = (qh[0].numel() + knh[0].numel() + vnh[0].numel()) * 2
     return {"value": round(world * steps * R * bytes_call / (ms * 1e-3) / 1e9, 1), "unit": "GB/s",
-            "h2d_bytes_per_step": R * per_call_in, "d2h_bytes_per_step": R * outh[0].numel() * 2,
+            "h2d_bytes_per_step": inh.numel() * 2, "d2h_bytes_per_step": outh.numel() * 2,
             "steps": steps, "us_per_call": round(ms * 1e3 / (steps * R), 3),
-            "path": "python binding td_rope_append_attn (one launch per call), pinned host q/new rows in, out back"}
+            "host_us_per_call": round(host_s * 1e6 / (steps * R), 3),
+            "path": "python binding td_rope_append_attn (one launch per call); per step, the calls' inputs "
+                    "(q and new rows) in one pinned host-to-device copy and their outputs in one copy back"}
 
 
 def cpu_baseline(case, w, L, seconds):
