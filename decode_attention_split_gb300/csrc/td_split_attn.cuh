@@ -85,7 +85,7 @@ __device__ __forceinline__ int attended_len(const SplitParams &p, int32_t raw, u
 }
 
 // A chunk's partial result for its row block: acc[R][D] (unnormalised p @ V sums), then
-// m[R] (natural-log units) and l[R]; padded to whole 16-byte units so blocks can be
+// m[R] (base-2 units) and l[R]; padded to whole 16-byte units so blocks can be
 // bulk-copied and every acc row is 16-byte aligned.
 __host__ __device__ constexpr int part_block_floats(int R, int D) { return (R * (D + 2) + 3) / 4 * 4; }
 
@@ -297,14 +297,12 @@ __device__ void merge_group(const SplitParams &p, float *smem_f, int smem_floats
   const int BF = part_block_floats(R, D);
   const long long g = ((long long)b * p.Hkv + kvh) * p.RB + rb;
   const float *src = p.ws_part + g * p.ns_ws * (long long)BF;
-  float *acc = smem_f;          // [ROWS][D] running weighted sums
-  float *st = acc + ROWS * D;   // M[ROWS], Lsum[ROWS], rescale[ROWS], (pad)
-  float *fac = st + 4 * ROWS;   // [ROWS][kFB] factors exp(m_c - M) of the staged chunks
+  float *acc = smem_f;          // [ROWS][D] running weighted sums (between rounds)
+  float *st = acc + ROWS * D;   // M[ROWS], Lsum[ROWS], rescale[ROWS], 1 / Lsum[ROWS]
+  float *fac = st + 4 * ROWS;   // [ROWS][kFB] factors 2^(m_c - M) of the staged chunks
   float *stage = fac + ROWS * kFB;
   int FB = (smem_floats - merge_fixed_floats<D, ROWS>()) / BF;
   if (FB > kFB) FB = kFB;
-#pragma unroll 1
-  for (int i = tid; i < nv * D; i += kThreads) acc[i] = 0.f;
   if (tid < nv) {
     st[tid] = -INFINITY;
     st[ROWS + tid] = 0.f;
@@ -312,6 +310,7 @@ __device__ void merge_group(const SplitParams &p, float *smem_f, int smem_floats
 #pragma unroll 1
   for (int c0 = 0; c0 < NC; c0 += FB) {
     const int nb = min(FB, NC - c0);
+    const bool last = c0 + nb >= NC;
     if (tid == 0) {
       fence_proxy_async_global();
       mbar_arrive_expect_tx(smem_u32(bar), (uint32_t)(nb * BF * 4));
@@ -323,7 +322,7 @@ __device__ void merge_group(const SplitParams &p, float *smem_f, int smem_floats
     }
     phase ^= 1u;
     __syncthreads();  // staged blocks and the previous round's statistics are visible
-    // per-row statistics of this block: a warp per row, lanes over chunks
+    // per-row statistics of this block (base 2): a warp per row, lanes over chunks
 #pragma unroll 1
     for (int r = warp; r < nv; r += kWarps) {
       float mv[2], lv[2];
@@ -342,46 +341,54 @@ __device__ void merge_group(const SplitParams &p, float *smem_f, int smem_floats
       float ls = 0.f;
 #pragma unroll
       for (int k = 0; k < 2; ++k) {
-        const float f = lv[k] > 0.f ? expf(mv[k] - base) : 0.f;
+        const float f = lv[k] > 0.f ? exp2f(mv[k] - base) : 0.f;
         if (lane + 32 * k < nb) fac[r * kFB + lane + 32 * k] = f;
         ls = fmaf(lv[k], f, ls);
       }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) ls += __shfl_xor_sync(0xffffffffu, ls, o);
       if (lane == 0) {
-        const float alpha = expf(Mo - base);
+        const float alpha = exp2f(Mo - base);
+        const float Ls = st[ROWS + r] * alpha + ls;
         st[r] = Mn;
-        st[ROWS + r] = st[ROWS + r] * alpha + ls;
+        st[ROWS + r] = Ls;
         st[2 * ROWS + r] = alpha;
+        st[3 * ROWS + r] = Ls > 0.f ? 1.f / Ls : 0.f;
+        if (last && p.lse != nullptr)
+          p.lse[out_row_of(p, b, kvh, rb, r)] = Ls > 0.f ? (Mn + log2f(Ls)) * kLn2 : -INFINITY;
       }
     }
     __syncthreads();
-    // weighted sums, four dims per thread
+    // weighted sums, four dims per thread; in the last round they are the output
 #pragma unroll 1
     for (int idx = tid; idx < nv * D4; idx += kThreads) {
       const int r = idx / D4, d = (idx % D4) * 4;
       const float *a = stage + r * D + d;
       const float *f = fac + r * kFB;
-      const float sc = st[2 * ROWS + r];
-      float4 x = *reinterpret_cast<const float4 *>(acc + r * D + d);
-      x.x *= sc, x.y *= sc, x.z *= sc, x.w *= sc;
+      float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (c0 > 0) {
+        const float sc = st[2 * ROWS + r];
+        x = *reinterpret_cast<const float4 *>(acc + r * D + d);
+        x.x *= sc, x.y *= sc, x.z *= sc, x.w *= sc;
+      }
 #pragma unroll 4
       for (int c = 0; c < nb; ++c) {
         const float4 v = *reinterpret_cast<const float4 *>(a + c * BF);
         const float w = f[c];
         x.x = fmaf(v.x, w, x.x), x.y = fmaf(v.y, w, x.y), x.z = fmaf(v.z, w, x.z), x.w = fmaf(v.w, w, x.w);
       }
-      *reinterpret_cast<float4 *>(acc + r * D + d) = x;
+      if (last) {
+        const float inv = st[3 * ROWS + r];
+        E *o = static_cast<E *>(p.out) + out_row_of(p, b, kvh, rb, r) * D + d;
+        store_elem<E>(o + 0, x.x * inv);
+        store_elem<E>(o + 1, x.y * inv);
+        store_elem<E>(o + 2, x.z * inv);
+        store_elem<E>(o + 3, x.w * inv);
+      } else {
+        *reinterpret_cast<float4 *>(acc + r * D + d) = x;
+      }
     }
     __syncthreads();  // the next block overwrites the staging area
-  }
-#pragma unroll 1
-  for (int idx = tid; idx < nv * D; idx += kThreads) {
-    const int r = idx / D, d = idx % D;
-    const long long orow = out_row_of(p, b, kvh, rb, r);
-    const float Ls = st[ROWS + r];
-    store_elem<E>(static_cast<E *>(p.out) + orow * D + d, Ls > 0.f ? acc[idx] / Ls : 0.f);
-    if (d == 0 && p.lse != nullptr) p.lse[orow] = Ls > 0.f ? st[r] + logf(Ls) : -INFINITY;
   }
 }
 
@@ -440,7 +447,7 @@ __device__ void finish_item(const SplitParams &p, float *smem_f, int smem_floats
     } else {
       *reinterpret_cast<float4 *>(blk + r * D + d) = A;
       if (d == 0) {
-        blk[R * D + r] = Ls > 0.f ? M * kLn2 : -INFINITY;
+        blk[R * D + r] = Ls > 0.f ? M : -INFINITY;
         blk[R * D + R + r] = Ls;
       }
     }
