@@ -152,6 +152,10 @@ __device__ void place_new_rows(const SplitParams &p, unsigned char *stage, int b
   fence_proxy_async_smem();
 }
 
+// Rise (base 2) of a row's scores above its reference maximum before that maximum moves and
+// the accumulators are rescaled.
+constexpr float kMaxGap = 8.f;
+
 // One warp's step over 16 keys of a landed stage (keys key0 .. key0+15, rows kr .. kr+15 of
 // the stage's tiles): S = Q K^T over two 8-key n tiles, masking by the rows' visible-key
 // limits `lim`, the online softmax in base 2, then O += P V. kt / vt address bf16 K / V
@@ -190,16 +194,19 @@ __device__ __forceinline__ void warp_keys16(const uint32_t (&qa)[D / 16][4], uin
       }
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-    const float m_new = fmaxf(m_run[h], mx);
-    const float base = m_new == -INFINITY ? 0.f : m_new;
-    alpha[h] = exp2f(m_run[h] - base);
-    m_run[h] = m_new;
+    // the reference maximum moves only when the row's scores rise more than kMaxGap above
+    // it (a row's first finite scores always move it), so most steps leave the accumulators'
+    // scale alone; probabilities stay below 2^kMaxGap. A row with no visible key keeps -inf.
+    const bool move = mx > m_run[h] + kMaxGap;
+    alpha[h] = move ? exp2_approx(m_run[h] - mx) : 1.f;
+    if (move) m_run[h] = mx;
+    const float base = m_run[h] == -INFINITY ? 0.f : m_run[h];
     float ps = 0.f;
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
-        const float pv = exp2f(sc[nt][2 * h + e] - base);
+        const float pv = exp2_approx(sc[nt][2 * h + e] - base);
         sc[nt][2 * h + e] = pv;
         ps += pv;
       }
