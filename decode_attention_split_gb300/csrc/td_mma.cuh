@@ -38,6 +38,15 @@ __device__ __forceinline__ void ldmatrix_x4_trans(uint32_t (&r)[4], uint32_t add
                : "r"(addr));
 }
 
+// Transpose of an 8x8 b16 matrix held one word per thread in the mma fragment layout
+// (thread t: row t/4, columns 2(t%4), 2(t%4)+1): afterwards thread t holds the same
+// positions of the transpose.
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+
 // 16-byte copy global -> shared that bypasses L1; src_bytes < 16 fills the rest with zeros
 // (0 reads nothing).
 __device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src, uint32_t src_bytes) {

@@ -93,8 +93,8 @@ cudaError_t launch_mma(const SplitParams &p, int grid, int smem, cudaStream_t st
     return cudaErrorInvalidValue;
   a.p = p;
   if (p.RB == 1) {
-    // the decode instantiation: its shared-memory opt-in, once per device (the plan's
-    // occupancy query set the other's)
+    // the decode instantiations (rows on the m side, or at most 8 rows on the n side): their
+    // shared-memory opt-in, once per device (the plan's occupancy query set the other's)
     static std::mutex mu;
     static bool done[kMaxDevices] = {};
     int device = 0;
@@ -102,15 +102,18 @@ cudaError_t launch_mma(const SplitParams &p, int grid, int smem, cudaStream_t st
     {
       std::lock_guard<std::mutex> lock(mu);
       if (!done[device]) {
-        const cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void *>(&split_attn_mma_kernel<D, true>),
-                                                   cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return e;
+        for (const void *fn : {reinterpret_cast<const void *>(&split_attn_mma_kernel<D, true, false>),
+                               reinterpret_cast<const void *>(&split_attn_mma_kernel<D, true, true>)}) {
+          const cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+          if (e != cudaSuccess) return e;
+        }
         done[device] = true;
       }
     }
-    return launch_pdl(split_attn_mma_kernel<D, true>, dim3(grid), dim3(kThreads), smem, stream, a);
+    if (p.R <= 8) return launch_pdl(split_attn_mma_kernel<D, true, true>, dim3(grid), dim3(kThreads), smem, stream, a);
+    return launch_pdl(split_attn_mma_kernel<D, true, false>, dim3(grid), dim3(kThreads), smem, stream, a);
   }
-  return launch_pdl(split_attn_mma_kernel<D, false>, dim3(grid), dim3(kThreads), smem, stream, a);
+  return launch_pdl(split_attn_mma_kernel<D, false, false>, dim3(grid), dim3(kThreads), smem, stream, a);
 }
 
 template <int D>
@@ -118,7 +121,7 @@ KernelRef mma_ref_of() {
   // the ring plus 1024 bytes of slack for its alignment
   constexpr int smem = MmaCfg<D, kPersistentStages<D>>::RING_BYTES + 1024;
   static_assert(smem + 8448 <= 227 * 1024, "mma kernel shared memory");
-  return KernelRef{reinterpret_cast<const void *>(&split_attn_mma_kernel<D, false>), smem, &launch_mma<D>};
+  return KernelRef{reinterpret_cast<const void *>(&split_attn_mma_kernel<D, false, false>), smem, &launch_mma<D>};
 }
 
 KernelRef pick_mma(int D, int MT) {

@@ -233,6 +233,79 @@ __device__ __forceinline__ void warp_keys16(const uint32_t (&qa)[D / 16][4], uin
   }
 }
 
+// The same step for at most 8 query rows, with the roles of keys and rows swapped so that
+// the rows fill the 8-wide n side of the tile instead of 16 rows of the m side:
+//   S^T = K Q^T  (m: the 16 keys, n: the 8 rows, k: head dims; K from ldmatrix, Q^T held
+//                as B fragments qb),
+//   O^T += V^T P^T  (m: 16 head dims per tile, n: the rows, k: the 16 keys; V^T from
+//                ldmatrix.trans, P^T from the score accumulators by one movmatrix
+//                transpose per 8 keys).
+// A thread holds keys gid and gid + 8 of rows 2*tig and 2*tig + 1, so a row's reductions
+// run over the 8 lanes of one tig. Half the tensor-core tiles, exponentials and output
+// registers of warp_keys16 when a kv head has 8 query rows or fewer (decode with grouped
+// heads). o[dt] holds O^T of dims 16*dt + gid (+8) and rows 2*tig (+1).
+template <int D>
+__device__ __forceinline__ void warp_keys16_n8(const uint32_t (&qb)[D / 16][2], uint32_t kt, uint32_t vt, int kr,
+                                               int key0, const int (&lim)[2], float qscale, float (&o)[D / 16][4],
+                                               float (&m_run)[2], float (&l_run)[2]) {
+  constexpr int TK = 64, KSD = D / 16;
+  const int lane = threadIdx.x & 31, gid = lane >> 2;
+  // two accumulators (even and odd k steps) halve the dependent chain of tensor-core tiles
+  float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+  const int krow = kr + (lane & 7) + ((lane >> 3) & 1) * 8;
+#pragma unroll
+  for (int j = 0; j < KSD; ++j) {
+    uint32_t ak[4];
+    ldmatrix_x4(ak, kt + tma_swz<TK>(krow, 2 * j + (lane >> 4)));
+    mma_bf16_16816((j & 1) ? sb : sa, ak, qb[j][0], qb[j][1]);
+  }
+  float sc[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) sc[i] = sa[i] + sb[i];
+  // scale to base-2 units and mask; element i is key gid + 8 * (i >> 1) of row 2*tig + (i & 1)
+  float alpha[2];
+#pragma unroll
+  for (int e = 0; e < 2; ++e) {
+#pragma unroll
+    for (int hk = 0; hk < 2; ++hk) {
+      const int key = key0 + gid + 8 * hk;
+      sc[2 * hk + e] = key < lim[e] ? sc[2 * hk + e] * qscale : -INFINITY;
+    }
+    float mx = fmaxf(sc[e], sc[2 + e]);
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+    // lazy reference maximum, as in warp_keys16
+    const bool move = mx > m_run[e] + kMaxGap;
+    alpha[e] = move ? exp2_approx(m_run[e] - mx) : 1.f;
+    if (move) m_run[e] = mx;
+    const float base = m_run[e] == -INFINITY ? 0.f : m_run[e];
+    const float p0 = exp2_approx(sc[e] - base), p1 = exp2_approx(sc[2 + e] - base);
+    sc[e] = p0;
+    sc[2 + e] = p1;
+    l_run[e] = l_run[e] * alpha[e] + (p0 + p1);  // this thread's keys; lanes summed at the end
+  }
+  if (__any_sync(0xffffffffu, alpha[0] != 1.f || alpha[1] != 1.f)) {
+#pragma unroll
+    for (int dt = 0; dt < KSD; ++dt) {
+      o[dt][0] *= alpha[0];
+      o[dt][1] *= alpha[1];
+      o[dt][2] *= alpha[0];
+      o[dt][3] *= alpha[1];
+    }
+  }
+  // P^T as the B operand: keys 2*tig (+1) (+8) of row gid
+  const uint32_t pb0 = movmatrix_trans(pack_bf16x2(sc[0], sc[1]));
+  const uint32_t pb1 = movmatrix_trans(pack_bf16x2(sc[2], sc[3]));
+  const int vrow = kr + (lane & 7) + (lane >> 4) * 8;
+#pragma unroll
+  for (int dt = 0; dt < KSD; ++dt) {
+    uint32_t av[4];
+    ldmatrix_x4_trans(av, vt + tma_swz<TK>(vrow, 2 * dt + ((lane >> 3) & 1)));
+    mma_bf16_16816(o[dt], av, pb0, pb1);
+  }
+}
+
 // Streams keys [c0, c1) of kv head kvh of sequence b (attended length L) for the query rows
 // of row block rb through the ring at `smem` (1024-byte aligned; NST stages with barriers
 // s_bars; `seq` counts the stages this CTA has consumed, for the barrier parities) and leaves
@@ -241,7 +314,7 @@ __device__ __forceinline__ void warp_keys16(const uint32_t (&qa)[D / 16][4], uin
 // Returns false, CTA-uniformly, if a copy never completed: the status bit is set, the other
 // copies in flight have been waited for, and the combine area holds empty partials.
 // Ends with a __syncthreads.
-template <int D, int NST>
+template <int D, int NST, bool NARROW = false>
 __device__ bool stream_chunk(const MmaArgs &a, unsigned char *smem, uint64_t *s_bars, uint32_t &seq, int b, int kvh,
                              int rb, int L, int c0, int c1) {
   using C = MmaCfg<D, NST>;
@@ -309,20 +382,22 @@ __device__ bool stream_chunk(const MmaArgs &a, unsigned char *smem, uint64_t *s_
     for (int s2 = 0; s2 < min(NST - 1, nstages); ++s2) issue(s2);
   }
 
-  // keys visible to rows r0 = gid and r1 = gid + 8 of this row block
+  // keys visible to this thread's rows of the row block: gid and gid + 8 (m16 layout) or
+  // 2*tig and 2*tig + 1 (narrow layout)
   int lim[2];
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
-    const int r = gid + 8 * h;
+    const int r = NARROW ? 2 * tig + h : gid + 8 * h;
     const int gr = rb * p.R + r;
     const bool valid = r < p.R && gr < GT;
     lim[h] = valid ? min(max(L - p.T + gr % p.T + 1, 0), c1) : 0;
   }
-  uint32_t qa[C::KSD][4];  // query rows as mma A fragments, read once the first stage lands
-
-  float o[C::NTD][4];
+  // query rows as mma A fragments (narrow: B fragments), read once the first stage lands
+  uint32_t qa[C::KSD][NARROW ? 2 : 4];
+  constexpr int NO = NARROW ? C::KSD : C::NTD;  // output tiles
+  float o[NO][4];
 #pragma unroll
-  for (int nt = 0; nt < C::NTD; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
+  for (int nt = 0; nt < NO; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
   float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
 
   int consumed = 0;
@@ -352,15 +427,33 @@ __device__ bool stream_chunk(const MmaArgs &a, unsigned char *smem, uint64_t *s_
       break;
     }
     if (st == 0) {
+      if constexpr (NARROW) {
+        // rows 0..7: matrices of 16-byte chunks 4j .. 4j+3 are B words of k steps 2j, 2j+1
 #pragma unroll
-      for (int j = 0; j < C::KSD; ++j)
-        ldmatrix_x4(qa[j], qtile + swz<C::ROWB>(((lane >> 3) & 1) * 8 + (lane & 7), 2 * j + (lane >> 4)));
+        for (int j = 0; j < C::KSD / 2; ++j) {
+          uint32_t w[4];
+          ldmatrix_x4(w, qtile + swz<C::ROWB>(lane & 7, 4 * j + (lane >> 3)));
+          qa[2 * j][0] = w[0];
+          qa[2 * j][1] = w[1];
+          qa[2 * j + 1][0] = w[2];
+          qa[2 * j + 1][1] = w[3];
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < C::KSD; ++j)
+          ldmatrix_x4(qa[j], qtile + swz<C::ROWB>(((lane >> 3) & 1) * 8 + (lane & 7), 2 * j + (lane >> 4)));
+      }
       __syncthreads();  // every warp holds its query fragments before that buffer is refilled
     }
     if (tid == 0 && st + NST - 1 < nstages) issue(st + NST - 1);
     const int kr = warp * C::TKW;  // first key row (within the stage) of this warp's step
     const int key0 = j0 + kr;
-    if (key0 < c1) warp_keys16<D>(qa, kt, vt, kr, key0, lim, p.qscale, o, m_run, l_run);
+    if (key0 < c1) {
+      if constexpr (NARROW)
+        warp_keys16_n8<D>(qa, kt, vt, kr, key0, lim, p.qscale, o, m_run, l_run);
+      else
+        warp_keys16<D>(qa, kt, vt, kr, key0, lim, p.qscale, o, m_run, l_run);
+    }
     consumed = st + 1;
   }
   if (!ok) {
@@ -376,14 +469,39 @@ __device__ bool stream_chunk(const MmaArgs &a, unsigned char *smem, uint64_t *s_
   seq += nstages;
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
-    l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 1);
-    l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 2);
+    if constexpr (NARROW) {
+      l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 4);
+      l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 8);
+      l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 16);
+    } else {
+      l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 1);
+      l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 2);
+    }
   }
   __syncthreads();  // ring idle: reuse it as the combine area
   float *combine = reinterpret_cast<float *>(smem);
   float *cm = combine;
   float *cl = combine + kWarps * kMmaRows;
   float *ca = combine + 2 * kWarps * kMmaRows;
+  if constexpr (NARROW) {
+    // rows 2*tig + e; rows 8..15 of the combine area are not used (at most 8 rows exist)
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int r = 2 * tig + e;
+      if (gid == 0) {
+        cm[warp * kMmaRows + r] = m_run[e];
+        cl[warp * kMmaRows + r] = l_run[e];
+      }
+      float *row = &ca[(warp * kMmaRows + r) * D];
+#pragma unroll
+      for (int dt = 0; dt < C::KSD; ++dt) {
+        row[16 * dt + gid] = o[dt][e];
+        row[16 * dt + gid + 8] = o[dt][2 + e];
+      }
+    }
+    __syncthreads();
+    return ok;
+  }
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     const int r = gid + 8 * h;
@@ -475,8 +593,9 @@ __device__ __forceinline__ unsigned char *align1024(unsigned char *p) {
 // EARLY_PLAN (launched when one row block covers a kv head, i.e. decode): the plan is made
 // on the lengths as they read before the wait for the previous kernel and kept after it if
 // they read the same then (measured on the 3B-style layer: 4k 11.4 -> 10.5 us, 32k 25.7 ->
-// 25.5 us). The other instantiation plans after the wait.
-template <int D, bool EARLY_PLAN>
+// 25.5 us). The other instantiation plans after the wait. NARROW (a kv head's rows fit 8):
+// the warps step with warp_keys16_n8.
+template <int D, bool EARLY_PLAN, bool NARROW = false>
 __global__ void __launch_bounds__(kThreads, 2) split_attn_mma_kernel(const __grid_constant__ MmaArgs a) {
   constexpr int NST = kPersistentStages<D>;
   using C = MmaCfg<D, NST>;
@@ -540,7 +659,7 @@ __global__ void __launch_bounds__(kThreads, 2) split_attn_mma_kernel(const __gri
     const int rb = rest % p.RB;
     const int kvh = rest / p.RB;
     const int c0 = c * S;
-    const bool ok = stream_chunk<D, NST>(a, smem, s_bars, seq, b, kvh, rb, L, c0, min(c0 + S, L));
+    const bool ok = stream_chunk<D, NST, NARROW>(a, smem, s_bars, seq, b, kvh, rb, L, c0, min(c0 + S, L));
     finish_item<E, D, kMmaRows, kWarps>(p, combine, C::RING_BYTES / 4, &s_merge_bar, merge_phase, b, kvh, rb, c, NC,
                                         &s_last);
     // the combine and merge wrote the ring through the generic proxy; the next item's first

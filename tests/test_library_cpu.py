@@ -124,9 +124,10 @@ def test_hot_kernels_have_no_spills(lib):
     log = open(td_build.PTXAS_LOG).read()
     entries = re.findall(r"Compiling entry function '(\w+)'.*?\n(?:.*?\n)*?\s+(\d+) bytes stack frame, (\d+) bytes "
                          r"spill stores, (\d+) bytes spill loads", log)
-    hot = {"split_attn_mma_kernelILi128ELb1E", "split_attn_mma_kernelILi128ELb0E", "split_attn_mma_kernelILi64ELb1E",
-           "split_attn_mma_kernelILi64ELb0E", "split_attn_kernelIfLi64ELi2E", "split_attn_cluster_kernelILi128E",
-           "split_attn_q8_kernelILi128E", "prefill_kernelILi128E"}
+    hot = {"split_attn_mma_kernelILi128ELb1ELb1E", "split_attn_mma_kernelILi128ELb1ELb0E",
+           "split_attn_mma_kernelILi128ELb0ELb0E", "split_attn_mma_kernelILi64ELb1ELb1E",
+           "split_attn_mma_kernelILi64ELb1ELb0E", "split_attn_mma_kernelILi64ELb0ELb0E", "split_attn_kernelIfLi64ELi2E",
+           "split_attn_cluster_kernelILi128E", "split_attn_q8_kernelILi128E", "prefill_kernelILi128E"}
     seen = set()
     for name, _stack, st, ld in entries:
         for h in hot:
