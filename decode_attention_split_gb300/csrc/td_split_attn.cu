@@ -180,9 +180,12 @@ constexpr int cluster_smem() {
 static_assert(cluster_smem<128>() + 1024 <= 227 * 1024 && cluster_smem<64>() + 1024 <= 227 * 1024,
               "cluster kernel shared memory");
 
-const void *cluster_fn(int D) {
-  return D == 64 ? reinterpret_cast<const void *>(&split_attn_cluster_kernel<64>)
-                 : reinterpret_cast<const void *>(&split_attn_cluster_kernel<128>);
+const void *cluster_fn(int D, bool narrow) {
+  if (narrow)
+    return D == 64 ? reinterpret_cast<const void *>(&split_attn_cluster_kernel<64, true>)
+                   : reinterpret_cast<const void *>(&split_attn_cluster_kernel<128, true>);
+  return D == 64 ? reinterpret_cast<const void *>(&split_attn_cluster_kernel<64, false>)
+                 : reinterpret_cast<const void *>(&split_attn_cluster_kernel<128, false>);
 }
 
 cudaLaunchConfig_t cluster_config(int D, int grid, int cs, cudaStream_t stream, cudaLaunchAttribute *attr) {
@@ -210,7 +213,8 @@ cudaError_t launch_cluster(const SplitParams &p, int grid, int cs, cudaStream_t 
   a.p = p;
   cudaLaunchAttribute attr[2];
   const cudaLaunchConfig_t cfg = cluster_config(D, grid, cs, stream, attr);
-  return cudaLaunchKernelEx(&cfg, split_attn_cluster_kernel<D>, a);
+  if (p.R <= 8) return cudaLaunchKernelEx(&cfg, split_attn_cluster_kernel<D, true>, a);
+  return cudaLaunchKernelEx(&cfg, split_attn_cluster_kernel<D, false>, a);
 }
 
 // variant: row padding RP of the CUDA-core kernel, or m tiles MT of the tensor-core kernel
@@ -241,21 +245,26 @@ int blocks_per_sm(int device, int slot, const KernelRef &k) {
 }
 
 // Clusters of `cs` CTAs (2, 4, 8 or 16) of the cluster kernel that the device holds at once;
-// sets the kernel's shared-memory and cluster-size opt-ins on first use. 0 on error.
+// sets the shared-memory and cluster-size opt-ins of both instantiations on first use and
+// asks about the wider one (the narrow one needs fewer registers). 0 on error.
 int active_clusters(int device, int D, int cs) {
   const int di = D == 64 ? 0 : 1, ci = cs == 2 ? 0 : cs == 4 ? 1 : cs == 8 ? 2 : 3;
   std::lock_guard<std::mutex> lock(g_mu);
   if (device < 0 || device >= kMaxDevices) return 0;
   if (g_clusters[device][di][ci] > 0) return g_clusters[device][di][ci] - 1;
-  const void *fn = cluster_fn(D);
   cudaLaunchAttribute attr[2];
   cudaLaunchConfig_t cfg = cluster_config(D, cs, cs, nullptr, attr);
   cfg.numAttrs = 1;  // the cluster shape alone
   int n = 0;
-  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)cfg.dynamicSmemBytes) !=
-          cudaSuccess ||
-      cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess ||
-      cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess) {
+  bool ok = true;
+  for (const bool narrow : {true, false}) {
+    const void *fn = cluster_fn(D, narrow);
+    ok = ok &&
+         cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)cfg.dynamicSmemBytes) ==
+             cudaSuccess &&
+         cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess;
+  }
+  if (!ok || cudaOccupancyMaxActiveClusters(&n, cluster_fn(D, false), &cfg) != cudaSuccess) {
     cudaGetLastError();
     n = 0;
   }

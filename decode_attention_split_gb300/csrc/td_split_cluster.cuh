@@ -18,7 +18,8 @@
 
 namespace td {
 
-template <int D>
+// NARROW: a group has at most 8 query rows and the warps step with warp_keys16_n8.
+template <int D, bool NARROW = false>
 __global__ void __launch_bounds__(kThreads, 1) split_attn_cluster_kernel(const __grid_constant__ MmaArgs a) {
   constexpr int NST = kClusterStages<D>;
   constexpr int D4 = D / 4;
@@ -67,7 +68,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_attn_cluster_kernel(const _
   const int c0 = min((int)rank * S, L);
   const int c1 = min(c0 + S, L);
   uint32_t seq = 0;
-  stream_chunk<D, NST>(a, smem, s_bars, seq, b, kvh, rb, L, c0, c1);
+  stream_chunk<D, NST, NARROW>(a, smem, s_bars, seq, b, kvh, rb, L, c0, c1);
   const float *combine = reinterpret_cast<const float *>(smem);
   float *blk = reinterpret_cast<float *>(smem) + C::COMBINE_FLOATS;  // acc[R][D], m[R], l[R]
   combine_block<D>(combine, blk, R, nv);
