@@ -163,14 +163,32 @@ cudaError_t launch_q8(const SplitParams &p, int grid, int smem, cudaStream_t str
   Q8Args a;
   if (!encode_q8_maps(&a, p, D)) return cudaErrorInvalidValue;
   a.p = p;
-  return launch_pdl(split_attn_q8_kernel<D>, dim3(grid), dim3(kThreads), smem, stream, a);
+  if (p.R <= 8) {
+    // the narrow instantiation's shared-memory opt-in, once per device (the plan's occupancy
+    // query set the other's)
+    static std::mutex mu;
+    static bool done[kMaxDevices] = {};
+    int device = 0;
+    if (cudaGetDevice(&device) != cudaSuccess || device < 0 || device >= kMaxDevices) return cudaErrorInvalidDevice;
+    {
+      std::lock_guard<std::mutex> lock(mu);
+      if (!done[device]) {
+        const cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void *>(&split_attn_q8_kernel<D, true>),
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        done[device] = true;
+      }
+    }
+    return launch_pdl(split_attn_q8_kernel<D, true>, dim3(grid), dim3(kThreads), smem, stream, a);
+  }
+  return launch_pdl(split_attn_q8_kernel<D, false>, dim3(grid), dim3(kThreads), smem, stream, a);
 }
 
 template <int D>
 KernelRef q8_ref_of() {
   constexpr int smem = Q8Cfg<D, kQ8Stages<D>>::SMEM_BYTES;
   static_assert(smem + 8704 <= 227 * 1024, "q8 kernel shared memory");
-  return KernelRef{reinterpret_cast<const void *>(&split_attn_q8_kernel<D>), smem, &launch_q8<D>};
+  return KernelRef{reinterpret_cast<const void *>(&split_attn_q8_kernel<D, false>), smem, &launch_q8<D>};
 }
 
 template <int D>

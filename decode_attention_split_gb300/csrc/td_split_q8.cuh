@@ -155,10 +155,11 @@ __device__ __forceinline__ void warp_keys32_q8(const uint32_t (&qa)[D / 16][4], 
       }
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-    const float m_new = fmaxf(m_run[h], mx);
-    const float base = m_new == -INFINITY ? 0.f : m_new;
-    alpha[h] = exp2_approx(m_run[h] - base);
-    m_run[h] = m_new;
+    // lazy reference maximum (see warp_keys16): rows with no visible key are never rescaled
+    const bool move = mx > m_run[h] + kMaxGap;
+    alpha[h] = move ? exp2_approx(m_run[h] - mx) : 1.f;
+    if (move) m_run[h] = mx;
+    const float base = m_run[h] == -INFINITY ? 0.f : m_run[h];
     float ps = 0.f;
 #pragma unroll
     for (int nt = 0; nt < 4; ++nt)
@@ -204,9 +205,125 @@ __device__ __forceinline__ void warp_keys32_q8(const uint32_t (&qa)[D / 16][4], 
   }
 }
 
+// The same step for at most 8 query rows with keys and rows swapped, as warp_keys16_n8 does
+// for bf16 caches: S^T = K Q^T (m: 16 keys, n: the rows) and O^T += V^T P'^T (m: 16 output
+// dims, k: 16 keys), for each 16-key half of the warp's 32 keys. Fragment orders
+// (g = lane / 4, c = lane % 4):
+//  - scores: ldmatrix gives thread (g, c) codes 4c .. 4c+3 of a 16-dim block of keys g and
+//    g + 8; they fill k slots 2c, 2c+1, 2c+8, 2c+9 of the A fragment, and qn (the query rows
+//    as B fragments) holds row g's dims 4c .. 4c+3 in the same slots. The accumulators start
+//    at minus the rows' score bias qbn (rows 2c, 2c+1);
+//  - P V: the transposed ldmatrix gives thread (g, c) dims 2g, 2g+1 of keys 2c, 2c+1; bytes
+//    0, 2 (dim 2g) fill the A fragment of the even-dim tile o[2i], bytes 1, 3 the odd one
+//    o[2i+1]. Tile rows m < 8 are dims 32i + 2m (+1), rows m >= 8 dims 32i + 16 + 2(m - 8)
+//    (+1), so thread (g, c) holds dims 32i + 2g, +1 (rows 2c, 2c+1 in o[2i][0..1], o[2i+1][0..1])
+//    and 32i + 16 + 2g, +1 (in [2..3]);
+//  - ob: 1152 * sum(P') of rows 2c, 2c+1 (the output's code bias), from the same B operands.
+template <int D, bool MASK>
+__device__ __forceinline__ void warp_keys32_q8_n8(const uint32_t (&qn)[D / 16][2], const float (&qbn)[2], uint32_t kt,
+                                                  uint32_t vt, int kr, int key0, int kend, const int (&lim)[2],
+                                                  float qscale, const float *ks, const float *vs,
+                                                  float (&o)[D / 16][4], float (&ob)[4], float (&m_run)[2],
+                                                  float (&l_run)[2]) {
+  constexpr int NX = D / 32;  // ldmatrix.x4 per 16 keys: 16 keys x 32 dims
+  const int lane = threadIdx.x & 31, gid = lane >> 2;
+  const int lrow = kr + (lane & 7) + ((lane >> 3) & 1) * 8, lch = lane >> 4;
+  const uint32_t c1152[4] = {kF16x2_1152, kF16x2_1152, kF16x2_1152, kF16x2_1152};
+  float sc[2][4];  // per 16-key half: keys gid, gid + 8 of rows 2c, 2c+1
+#pragma unroll
+  for (int hf = 0; hf < 2; ++hf) {
+    sc[hf][0] = sc[hf][2] = -qbn[0];
+    sc[hf][1] = sc[hf][3] = -qbn[1];
+  }
+#pragma unroll
+  for (int i = 0; i < NX; ++i)
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+      uint32_t r[4];  // keys 0-7 / 8-15 of dims 32i .. 32i+15, then of dims 32i+16 .. 32i+31
+      ldmatrix_x4(r, kt + q8_swz<D>(lrow + 16 * hf, 2 * i + lch));
+#pragma unroll
+      for (int blk = 0; blk < 2; ++blk) {
+        const uint32_t f0 = r[2 * blk] ^ kFlip, f1 = r[2 * blk + 1] ^ kFlip;
+        const uint32_t ak[4] = {codes_f16x2(f0, kSelB01), codes_f16x2(f1, kSelB01), codes_f16x2(f0, kSelB23),
+                                codes_f16x2(f1, kSelB23)};
+        mma_f16_16816(sc[hf], ak, qn[2 * i + blk][0], qn[2 * i + blk][1]);
+      }
+    }
+  float alpha[2];
+  float vss[2][2];  // value scales of keys gid, gid + 8 of each half
+#pragma unroll
+  for (int hf = 0; hf < 2; ++hf)
+#pragma unroll
+    for (int hk = 0; hk < 2; ++hk) {
+      const int r = kr + 16 * hf + 8 * hk + gid;
+      const float kss = ks[r] * qscale;
+      const int key = key0 + 16 * hf + 8 * hk + gid;
+      // keys past the sequence: a stale scale must not meet a zero probability
+      vss[hf][hk] = !MASK || key < kend ? vs[r] : 0.f;
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const float v = sc[hf][2 * hk + e] * kss;
+        sc[hf][2 * hk + e] = !MASK || key < lim[e] ? v : -INFINITY;
+      }
+    }
+#pragma unroll
+  for (int e = 0; e < 2; ++e) {
+    float mx = fmaxf(fmaxf(sc[0][e], sc[0][2 + e]), fmaxf(sc[1][e], sc[1][2 + e]));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+    const bool move = mx > m_run[e] + kMaxGap;
+    alpha[e] = move ? exp2_approx(m_run[e] - mx) : 1.f;
+    if (move) m_run[e] = mx;
+    const float base = m_run[e] == -INFINITY ? 0.f : m_run[e];
+    float ps = 0.f;
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf)
+#pragma unroll
+      for (int hk = 0; hk < 2; ++hk) {
+        const float pv = exp2_approx(sc[hf][2 * hk + e] - base);
+        sc[hf][2 * hk + e] = pv * vss[hf][hk];
+        ps += pv;
+      }
+    l_run[e] = l_run[e] * alpha[e] + ps;  // this thread's keys; lanes summed at the end
+  }
+  if (__any_sync(0xffffffffu, alpha[0] != 1.f || alpha[1] != 1.f)) {
+#pragma unroll
+    for (int t = 0; t < D / 16; ++t) {
+      o[t][0] *= alpha[0];
+      o[t][1] *= alpha[1];
+      o[t][2] *= alpha[0];
+      o[t][3] *= alpha[1];
+    }
+    ob[0] *= alpha[0];
+    ob[1] *= alpha[1];
+    ob[2] *= alpha[0];
+    ob[3] *= alpha[1];
+  }
+#pragma unroll
+  for (int hf = 0; hf < 2; ++hf) {
+    // P'^T as the B operand: keys 2c, 2c+1 (+8) of row gid
+    const uint32_t pb0 = movmatrix_trans(pack_f16x2(sc[hf][0], sc[hf][1]));
+    const uint32_t pb1 = movmatrix_trans(pack_f16x2(sc[hf][2], sc[hf][3]));
+    mma_f16_16816(ob, c1152, pb0, pb1);
+#pragma unroll
+    for (int i = 0; i < NX; ++i) {
+      uint32_t r[4];  // transposed: keys 0-7 / 8-15 of dims 32i .. 32i+15, then of 32i+16 ..
+      ldmatrix_x4_trans(r, vt + q8_swz<D>(lrow + 16 * hf, 2 * i + lch));
+      const uint32_t f0 = r[0] ^ kFlip, f1 = r[1] ^ kFlip, f2 = r[2] ^ kFlip, f3 = r[3] ^ kFlip;
+      const uint32_t ae[4] = {codes_f16x2(f0, kSelB02), codes_f16x2(f2, kSelB02), codes_f16x2(f1, kSelB02),
+                              codes_f16x2(f3, kSelB02)};
+      const uint32_t ao[4] = {codes_f16x2(f0, kSelB13), codes_f16x2(f2, kSelB13), codes_f16x2(f1, kSelB13),
+                              codes_f16x2(f3, kSelB13)};
+      mma_f16_16816(o[2 * i], ae, pb0, pb1);
+      mma_f16_16816(o[2 * i + 1], ao, pb0, pb1);
+    }
+  }
+}
+
 // Streams keys [c0, c1) of (b, kvh) for row block rb, as stream_chunk does for bf16 caches,
 // leaving the same combine area (at the start of `smem`).
-template <int D, int NST>
+template <int D, int NST, bool NARROW = false>
 __device__ bool stream_chunk_q8(const Q8Args &a, unsigned char *smem, uint64_t *s_bars, uint32_t &seq, int b, int kvh,
                                 int rb, int L, int c0, int c1) {
   using C = Q8Cfg<D, NST>;
@@ -239,14 +356,18 @@ __device__ bool stream_chunk_q8(const Q8Args &a, unsigned char *smem, uint64_t *
   // fp16's range is an fp16 value; the scale stays out of them, its product would round),
   // dims in the order the key fragments take (slots 2c, 2c+1 <- dims 4c, 4c+1; slots 2c+8,
   // 2c+9 <- dims 4c+2, 4c+3)
-  uint32_t qa[D / 16][4];
+  // (narrow layout: row gid as B fragments qa[ks][0..1], limits of rows 2c, 2c+1)
+  uint32_t qa[D / 16][NARROW ? 2 : 4];
   int lim[2];
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
-    const int r = gid + 8 * h;
+    const int lr = NARROW ? 2 * tig + h : gid + 8 * h;  // the row whose limit this thread applies
+    const int lgr = rb * p.R + lr;
+    lim[h] = lr < p.R && lgr < GT ? min(max(L - p.T + lgr % p.T + 1, 0), c1) : 0;
+    if (NARROW && h == 1) break;  // one query row per thread in the narrow layout
+    const int r = NARROW ? gid : gid + 8 * h;
     const int gr = rb * p.R + r;
     const bool valid = r < p.R && gr < GT;
-    lim[h] = valid ? min(max(L - p.T + gr % p.T + 1, 0), c1) : 0;
     const int hq = kvh * p.G + (valid ? gr / p.T : 0), t = valid ? gr % p.T : 0;
     const uint2 *qrow = reinterpret_cast<const uint2 *>(static_cast<const __nv_bfloat16 *>(p.q) +
                                                         (((size_t)b * p.Hq + hq) * p.T + t) * D);
@@ -255,25 +376,39 @@ __device__ bool stream_chunk_q8(const Q8Args &a, unsigned char *smem, uint64_t *
       uint2 w = valid ? qrow[ks * 4 + tig] : make_uint2(0u, 0u);
       const float2 lo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w.x));
       const float2 hi = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w.y));
-      qa[ks][h] = pack_f16x2(lo.x, lo.y);
-      qa[ks][2 + h] = pack_f16x2(hi.x, hi.y);
+      if constexpr (NARROW) {
+        qa[ks][0] = pack_f16x2(lo.x, lo.y);
+        qa[ks][1] = pack_f16x2(hi.x, hi.y);
+      } else {
+        qa[ks][h] = pack_f16x2(lo.x, lo.y);
+        qa[ks][2 + h] = pack_f16x2(hi.x, hi.y);
+      }
     }
   }
-  // the rows' score bias 1152 * sum(q), from the same fragments
+  // the rows' score bias 1152 * sum(q), from the same fragments (narrow: rows 2c, 2c+1)
   float qb[2];
   {
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    if constexpr (NARROW) {
+      const uint32_t c1152[4] = {kF16x2_1152, kF16x2_1152, kF16x2_1152, kF16x2_1152};
 #pragma unroll
-    for (int ks = 0; ks < D / 16; ++ks) mma_f16_16816(acc, qa[ks], kF16x2_1152, kF16x2_1152);
-    qb[0] = acc[0];
-    qb[1] = acc[2];
+      for (int ks = 0; ks < D / 16; ++ks) mma_f16_16816(acc, c1152, qa[ks][0], qa[ks][1]);
+      qb[0] = acc[0];
+      qb[1] = acc[1];
+    } else {
+#pragma unroll
+      for (int ks = 0; ks < D / 16; ++ks) mma_f16_16816(acc, qa[ks], kF16x2_1152, kF16x2_1152);
+      qb[0] = acc[0];
+      qb[1] = acc[2];
+    }
   }
   // keys every existing row of the block sees (a warp-uniform bound for the unmasked step)
   int lim_all = c1;
   for (int r = 0; r < min(p.R, GT - rb * p.R); ++r) lim_all = min(lim_all, max(L - p.T + (rb * p.R + r) % p.T + 1, 0));
-  float o[D / 8][4], ob[4] = {0.f, 0.f, 0.f, 0.f};
+  constexpr int NO = NARROW ? D / 16 : D / 8;  // output tiles
+  float o[NO][4], ob[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-  for (int nt = 0; nt < D / 8; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
+  for (int nt = 0; nt < NO; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
   float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
 
   int consumed = 0;
@@ -294,12 +429,21 @@ __device__ bool stream_chunk_q8(const Q8Args &a, unsigned char *smem, uint64_t *
     if (key0 < c1) {
       const uint32_t kt = sbase + buf * C::CODES_STAGE;
       const float *scl = reinterpret_cast<const float *>(smem + C::SCALE_OFF + buf * 2 * C::SCALE_SLOT) + (j0 & 3);
-      if (key0 + 32 <= lim_all)
-        warp_keys32_q8<D, false>(qa, qb, kt, kt + C::CODE_BYTES, kr, key0, L, lim, p.qscale, scl,
-                                 scl + C::SCALE_SLOT / 4, o, ob, m_run, l_run);
-      else
-        warp_keys32_q8<D, true>(qa, qb, kt, kt + C::CODE_BYTES, kr, key0, L, lim, p.qscale, scl,
-                                scl + C::SCALE_SLOT / 4, o, ob, m_run, l_run);
+      if constexpr (NARROW) {
+        if (key0 + 32 <= lim_all)
+          warp_keys32_q8_n8<D, false>(qa, qb, kt, kt + C::CODE_BYTES, kr, key0, L, lim, p.qscale, scl,
+                                      scl + C::SCALE_SLOT / 4, o, ob, m_run, l_run);
+        else
+          warp_keys32_q8_n8<D, true>(qa, qb, kt, kt + C::CODE_BYTES, kr, key0, L, lim, p.qscale, scl,
+                                     scl + C::SCALE_SLOT / 4, o, ob, m_run, l_run);
+      } else {
+        if (key0 + 32 <= lim_all)
+          warp_keys32_q8<D, false>(qa, qb, kt, kt + C::CODE_BYTES, kr, key0, L, lim, p.qscale, scl,
+                                   scl + C::SCALE_SLOT / 4, o, ob, m_run, l_run);
+        else
+          warp_keys32_q8<D, true>(qa, qb, kt, kt + C::CODE_BYTES, kr, key0, L, lim, p.qscale, scl,
+                                  scl + C::SCALE_SLOT / 4, o, ob, m_run, l_run);
+      }
     }
     consumed = st + 1;
   }
@@ -314,14 +458,41 @@ __device__ bool stream_chunk_q8(const Q8Args &a, unsigned char *smem, uint64_t *
   seq += nstages;
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
-    l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 1);
-    l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 2);
+    if constexpr (NARROW) {
+      l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 4);
+      l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 8);
+      l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 16);
+    } else {
+      l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 1);
+      l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 2);
+    }
   }
   __syncthreads();  // ring idle: reuse it as the combine area
   float *combine = reinterpret_cast<float *>(smem);
   float *cm = combine;
   float *cl = combine + kWarps * kMmaRows;
   float *ca = combine + 2 * kWarps * kMmaRows;
+  if constexpr (NARROW) {
+    // rows 2c + e; thread (g, c) holds dims 32i + 2g, +1 and 32i + 16 + 2g, +1
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int r = 2 * tig + e;
+      if (gid == 0) {
+        cm[warp * kMmaRows + r] = m_run[e];
+        cl[warp * kMmaRows + r] = l_run[e];
+      }
+      const float bias = ob[e];  // 1152 * sum(p) of row r
+      float *row = &ca[(warp * kMmaRows + r) * D];
+#pragma unroll
+      for (int i = 0; i < D / 32; ++i) {
+        *reinterpret_cast<float2 *>(&row[32 * i + 2 * gid]) = make_float2(o[2 * i][e] - bias, o[2 * i + 1][e] - bias);
+        *reinterpret_cast<float2 *>(&row[32 * i + 16 + 2 * gid]) =
+            make_float2(o[2 * i][2 + e] - bias, o[2 * i + 1][2 + e] - bias);
+      }
+    }
+    __syncthreads();
+    return ok;
+  }
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     const int r = gid + 8 * h;
@@ -342,7 +513,8 @@ __device__ bool stream_chunk_q8(const Q8Args &a, unsigned char *smem, uint64_t *
 
 // Persistent kernel over an int8 cache: the same items, chunks and fused merge as
 // split_attn_mma_kernel.
-template <int D>
+// NARROW: a row block has at most 8 rows and the warps step with warp_keys32_q8_n8.
+template <int D, bool NARROW = false>
 __global__ void __launch_bounds__(kThreads, 2) split_attn_q8_kernel(const __grid_constant__ Q8Args a) {
   constexpr int NST = kQ8Stages<D>;
   using C = Q8Cfg<D, NST>;
@@ -398,7 +570,7 @@ __global__ void __launch_bounds__(kThreads, 2) split_attn_q8_kernel(const __grid
     const int rb = rest % p.RB;
     const int kvh = rest / p.RB;
     const int c0 = c * S;
-    const bool ok = stream_chunk_q8<D, NST>(a, smem, s_bars, seq, b, kvh, rb, L, c0, min(c0 + S, L));
+    const bool ok = stream_chunk_q8<D, NST, NARROW>(a, smem, s_bars, seq, b, kvh, rb, L, c0, min(c0 + S, L));
     finish_item<E, D, kMmaRows, kWarps>(p, combine, C::RING_BYTES / 4, &s_merge_bar, merge_phase, b,
                                         kvh, rb, c, NC, &s_last);
     fence_proxy_async_smem();
