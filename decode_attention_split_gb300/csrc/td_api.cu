@@ -57,6 +57,7 @@ td_status prepare(td_dtype dtype, const void *q, const void *k_cache, const void
   p->ns_ws = plan->ns_ws;
   p->p_target = plan->p_target;
   p->min_chunk = plan->min_chunk;
+  p->warm_stages = plan->warm;
   p->qscale = scale * td::kLog2e;
   p->done = p->counters + (size_t)B * Hkv * plan->RB;
   return TD_OK;

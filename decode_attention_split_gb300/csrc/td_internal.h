@@ -22,6 +22,7 @@ struct SplitPlan {
   int grid;      // CTAs launched
   int smem;      // dynamic shared memory per CTA
   int min_chunk; // smallest automatic chunk (keys)
+  int warm;      // 64-row units of K and V each CTA warms in L2 before the wait for the previous kernel
   int cluster;   // 0: persistent kernel; else CTAs per cluster of the cluster kernel (grid = groups x cluster)
   bool q8;       // int8 cache (codes + per-row scales): the quantised-cache kernel
   size_t off_part, bytes;  // workspace layout: counters, then partial blocks

@@ -91,6 +91,7 @@ extern "C" td_status td_decode_attn_noalloc(td_dtype dtype, const void *q, const
   p.ns_ws = plan.ns_ws;
   p.p_target = plan.p_target;
   p.min_chunk = plan.min_chunk;
+  p.warm_stages = plan.warm;
   p.qscale = scale * td::kLog2e;
   return td::launch_split(dtype, D, plan, p, s) == cudaSuccess ? TD_OK : TD_ERR_CUDA;
 }

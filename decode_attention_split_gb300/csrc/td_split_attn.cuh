@@ -52,6 +52,7 @@ struct SplitParams {
   int ns_ws;            // partial slots per row in the workspace
   int p_target;         // CTAs the automatic chunk size aims to fill
   int min_chunk;        // smallest automatic chunk (keys)
+  int warm_stages;      // 64-row units of its first chunk each CTA warms in L2 before the wait
   float qscale;         // scale * log2(e)
   // Fused step (tensor-core kernels only; k_new == null for plain attention): the T new rows
   // of each (b, kv head) go to cache rows seq_lens[b] .. seq_lens[b]+T-1 in this launch, the

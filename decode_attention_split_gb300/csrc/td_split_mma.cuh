@@ -59,11 +59,9 @@ struct MmaCfg {
 // Ring depth of the persistent kernel (two CTAs per SM) and of the cluster kernel (one).
 template <int D>
 constexpr int kPersistentStages = D == 128 ? 3 : 4;
-// Stages of a CTA's first chunk warmed in L2 before the wait for the previous kernel: up to
-// 16 when one row block reads the kv head, 4 when several do (measured on the 3B-style layer:
-// 32k decode 29.0 us without, 26.5 with 4, 26.1 with 16; the 6-token verify, two row
-// blocks, 27.8 / 27.5 / 29.9).
-__device__ __forceinline__ int prefetch_stages(const SplitParams &p) { return p.RB == 1 ? 16 : 4; }
+// Units of 64 rows of a CTA's first chunk warmed in L2 before the wait for the previous
+// kernel; the host sizes it from the device's L2 (plan_split).
+__device__ __forceinline__ int prefetch_stages(const SplitParams &p) { return p.warm_stages; }
 template <int D>
 constexpr int kClusterStages = D == 128 ? 3 : 6;
 
