@@ -102,7 +102,7 @@ SMALL = [
     ("bf16", 64, 15, 5, 300, [257, 11], 7),
     ("bf16", 128, 24, 8, 520, [520, 100], 0),
     ("bf16", 128, 24, 8, 520, [519, 16], 1),
-    ("bf16", 128, 32, 4, 260, [260, 5], 0),    # 8 heads per kv head: two row blocks
+    ("bf16", 128, 32, 4, 260, [260, 5], 0),    # 8 heads per kv head: the narrow tile's full 8 rows
     ("bf16", 128, 20, 4, 130, [130], 0),       # 5 heads: ragged row block
     ("bf16", 128, 8, 8, 200, [200, 3, 64], 100),
     ("bf16", 64, 8, 1, 400, [400, 399, 31, 2], 0),
@@ -120,6 +120,28 @@ def test_decode_small(td, dtype, D, Hq, Hkv, Smax, lens, split):
 @pytest.mark.parametrize("split", [0, 1, 16, 64, 128, 256, 1024, 4096, 37])
 def test_decode_split_sweep(td, split):
     case = small_case(dtype="bf16", B=2, Hq=24, Hkv=8, D=128, Smax=4096, seq_lens=[4096, 1500], seed=3, heavy=0.01)
+    check_case(td, case, split=split)
+
+
+# Rows per kv head on either side of the narrow tile's limit: 8 or fewer put the keys on the
+# m side and the rows on n (warp_keys16_n8), 9 to 16 take one 16-row m tile, more take
+# several row blocks; verify rows carry their own causal limits inside a tile.
+TILE_EDGES = [
+    # D, Hq, Hkv, Smax, T, lengths, split
+    (128, 14, 2, 700, 1, [700, 129], 0),   # 7 rows
+    (64, 16, 2, 700, 1, [700, 1], 0),      # 8 rows
+    (128, 18, 2, 700, 1, [650, 64], 0),    # 9 rows
+    (64, 32, 2, 700, 1, [700, 333], 0),    # 16 rows
+    (128, 4, 2, 300, 4, [300, 70], 0),     # verify, 8 rows
+    (128, 4, 2, 300, 4, [300, 4], 13),     # verify, 8 rows, the whole sequence new
+    (64, 6, 2, 300, 3, [300, 5], 19),      # verify, 9 rows
+]
+
+
+@pytest.mark.parametrize("D,Hq,Hkv,Smax,T,lens,split", TILE_EDGES)
+def test_narrow_tile_edges(td, D, Hq, Hkv, Smax, T, lens, split):
+    case = small_case(dtype="bf16", B=len(lens), Hq=Hq, Hkv=Hkv, D=D, Smax=Smax, T=T, seq_lens=lens,
+                      seed=Hq + T + split, heavy=0.02)
     check_case(td, case, split=split)
 
 

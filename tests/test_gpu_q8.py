@@ -99,6 +99,9 @@ Q8 = [
     (128, 32, 8, 200, 6, [200, 70], 0),         # verify
     (64, 8, 1, 400, 1, [400, 399, 31, 2], 37),
     (128, 24, 8, 4096, 1, [4096, 1500, 0], 0),  # several chunks, an empty sequence
+    (128, 16, 2, 700, 1, [700, 129], 0),        # 8 rows per kv head: the narrow tile's limit
+    (64, 18, 2, 700, 1, [650, 64], 0),          # 9 rows: one 16-row m tile
+    (128, 4, 2, 300, 4, [300, 70], 0),          # verify, 8 rows, each with its own causal limit
 ]
 
 
