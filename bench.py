@@ -259,11 +259,13 @@ def time_graph(graph, stream, reps, warm=2):
 def kernel_label(td, w) -> str:
     """Which split-attention kernel the timed call runs, from the library's own launch plan."""
     plan = td.td_split_plan(w.torch_dtype, w.B, w.Hq, w.Hkv, w.Smax, w.D, w.T, 0)
+    # query rows per CTA: 8 or fewer go on the n side of the tensor-core tile (the narrow tile)
+    tile = "narrow tile" if plan["rows"] <= 8 else "m16 tile"
     names = {
         "tensor_core_persistent": f"split_attn_mma_kernel<{w.D}> (persistent, fused split + workspace merge, "
-                                  f"mma.sync bf16, TMA)",
+                                  f"mma.sync bf16 {tile}, TMA)",
         "tensor_core_cluster": f"split_attn_cluster_kernel<{w.D}> (clusters of {plan['cluster']}, on-chip merge, "
-                               f"mma.sync bf16, TMA)",
+                               f"mma.sync bf16 {tile}, TMA)",
         "cuda_core": f"split_attn_kernel<{w.D}> (CUDA cores)",
     }
     return f"{names[plan['kernel']]}, grid {plan['grid']}, timed alone"
