@@ -19,6 +19,7 @@ struct SplitPlan {
   int RB;        // row blocks per kv head
   int ns_ws;     // partial slots per query row
   int p_target;  // CTAs that fill the GPU once
+  bool spare;    // p_target leaves one slot per group for the previous call's merging CTAs
   int grid;      // CTAs launched
   int smem;      // dynamic shared memory per CTA
   int min_chunk; // smallest automatic chunk (keys)

@@ -159,12 +159,12 @@ bool encode_q8_maps(Q8Args *a, const SplitParams &p, int D) {
 }
 
 template <int D>
-cudaError_t launch_q8(const SplitParams &p, int grid, int smem, cudaStream_t stream) {
+cudaError_t launch_q8(const SplitParams &p, int grid, int smem, bool early, cudaStream_t stream) {
   Q8Args a;
   if (!encode_q8_maps(&a, p, D)) return cudaErrorInvalidValue;
   a.p = p;
   if (p.R <= 8) {
-    // the narrow instantiation's shared-memory opt-in, once per device (the plan's occupancy
+    // the narrow instantiations' shared-memory opt-in, once per device (the plan's occupancy
     // query set the other's)
     static std::mutex mu;
     static bool done[kMaxDevices] = {};
@@ -173,22 +173,25 @@ cudaError_t launch_q8(const SplitParams &p, int grid, int smem, cudaStream_t str
     {
       std::lock_guard<std::mutex> lock(mu);
       if (!done[device]) {
-        const cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void *>(&split_attn_q8_kernel<D, true>),
-                                                   cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return e;
+        for (const void *fn : {reinterpret_cast<const void *>(&split_attn_q8_kernel<D, true, false>),
+                               reinterpret_cast<const void *>(&split_attn_q8_kernel<D, true, true>)}) {
+          const cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+          if (e != cudaSuccess) return e;
+        }
         done[device] = true;
       }
     }
-    return launch_pdl(split_attn_q8_kernel<D, true>, dim3(grid), dim3(kThreads), smem, stream, a);
+    if (early) return launch_pdl(split_attn_q8_kernel<D, true, true>, dim3(grid), dim3(kThreads), smem, stream, a);
+    return launch_pdl(split_attn_q8_kernel<D, true, false>, dim3(grid), dim3(kThreads), smem, stream, a);
   }
-  return launch_pdl(split_attn_q8_kernel<D, false>, dim3(grid), dim3(kThreads), smem, stream, a);
+  return launch_pdl(split_attn_q8_kernel<D, false, false>, dim3(grid), dim3(kThreads), smem, stream, a);
 }
 
 template <int D>
 KernelRef q8_ref_of() {
   constexpr int smem = Q8Cfg<D, kQ8Stages<D>>::SMEM_BYTES;
   static_assert(smem + 8704 <= 227 * 1024, "q8 kernel shared memory");
-  return KernelRef{reinterpret_cast<const void *>(&split_attn_q8_kernel<D, false>), smem, &launch_q8<D>};
+  return KernelRef{reinterpret_cast<const void *>(&split_attn_q8_kernel<D, false, false>), smem, nullptr};
 }
 
 template <int D>
@@ -358,10 +361,12 @@ td_status plan_split(td_dtype dtype, int B, int Hq, int Hkv, int T, int Smax, in
   // groups are few, leave one slot per group free: the previous call's merging CTAs (one per
   // group) hold theirs until it ends, and with the slots to spare every CTA of this call is
   // resident early enough to warm L2 with its first stages before that end (3B-style layer,
-  // B = 1: 32k 26.3 -> 25.7 us, 16k 17.75 -> 17.4 us; the two-row-block verify is slower
-  // this way, 27.5 -> 28.3 us, and keeps the full grid).
+  // B = 1: 32k 26.3 -> 25.7 us, 16k 17.75 -> 17.4 us; the 8-bit cache with its early plan,
+  // see split_attn_q8_kernel; the two-row-block verify is slower this way, 27.5 -> 28.3 us,
+  // and keeps the full grid). Only while the groups are at most 1/16 of the slots: 64 groups
+  // of the 8-bit kernel (B = 8) lost 13-15 % this way.
   const long long slots = (long long)sms * per_sm;
-  const bool spare = mma && !q8 && RB == 1 && (long long)B * U * 4 <= slots;
+  const bool spare = mma && RB == 1 && (long long)B * U * 16 <= slots;
   const long long p_target = slots - (spare ? (long long)B * U : 0);
   long long ns;
   if (split > 0) {
@@ -381,6 +386,7 @@ td_status plan_split(td_dtype dtype, int B, int Hq, int Hkv, int T, int Smax, in
   plan->RB = (int)RB;
   plan->ns_ws = (int)ns;
   plan->p_target = (int)p_target;
+  plan->spare = spare;
   plan->grid = (int)(items_max < p_target ? items_max : p_target);
   if (plan->grid < 1) plan->grid = 1;
   plan->smem = k.smem;
@@ -428,7 +434,8 @@ td_status plan_split(td_dtype dtype, int B, int Hq, int Hkv, int T, int Smax, in
 cudaError_t launch_split(td_dtype dtype, int D, const SplitPlan &plan, const SplitParams &p, cudaStream_t stream) {
   cudaError_t e;
   if (plan.q8) {
-    e = D == 64 ? launch_q8<64>(p, plan.grid, plan.smem, stream) : launch_q8<128>(p, plan.grid, plan.smem, stream);
+    e = D == 64 ? launch_q8<64>(p, plan.grid, plan.smem, plan.spare, stream)
+                : launch_q8<128>(p, plan.grid, plan.smem, plan.spare, stream);
   } else if (plan.cluster > 0) {
     e = D == 64 ? launch_cluster<64>(p, plan.grid, plan.cluster, stream)
                 : launch_cluster<128>(p, plan.grid, plan.cluster, stream);

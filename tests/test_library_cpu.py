@@ -127,8 +127,8 @@ def test_hot_kernels_have_no_spills(lib):
     hot = {"split_attn_mma_kernelILi128ELb1ELb1E", "split_attn_mma_kernelILi128ELb1ELb0E",
            "split_attn_mma_kernelILi128ELb0ELb0E", "split_attn_mma_kernelILi64ELb1ELb1E",
            "split_attn_mma_kernelILi64ELb1ELb0E", "split_attn_mma_kernelILi64ELb0ELb0E", "split_attn_kernelIfLi64ELi2E",
-           "split_attn_cluster_kernelILi128ELb0E", "split_attn_cluster_kernelILi128ELb1E", "split_attn_q8_kernelILi128ELb0E",
-           "split_attn_q8_kernelILi128ELb1E",
+           "split_attn_cluster_kernelILi128ELb0E", "split_attn_cluster_kernelILi128ELb1E", "split_attn_q8_kernelILi128ELb0ELb0E",
+           "split_attn_q8_kernelILi128ELb1ELb0E", "split_attn_q8_kernelILi128ELb1ELb1E",
            "prefill_kernelILi128E"}
     seen = set()
     for name, _stack, st, ld in entries:
