@@ -88,10 +88,17 @@ def measured_peaks():
         return {"hbm_gbs": FALLBACK_HBM_GBS}, "fallback"
 
 
+def _code_only(text: str) -> str:
+    """C/C++ source without its comments and blank lines (what the compiler sees)."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "\n".join(ln.rstrip() for ln in text.splitlines() if ln.strip())
+
+
 def kernel_source_hash() -> str:
-    """Hash of the sources the timed decode kernel is built from: the translation units that
+    """Hash of the code the timed decode kernel is built from: the translation units that
     define and launch it (td_split_attn.cu, td_api.cu) with every header they include,
-    transitively, and td.h."""
+    transitively, and td.h, comments and blank lines left out."""
     src = os.path.join(ROOT, "decode_attention_split_gb300", "csrc")
     seen, todo = set(), ["td_split_attn.cu", "td_api.cu"]
     while todo:
@@ -103,10 +110,10 @@ def kernel_source_hash() -> str:
             todo += re.findall(r'^#include "([^"]+)"', f.read(), flags=re.M)
     h = hashlib.sha256()
     for name in sorted(seen):
-        with open(os.path.join(src, name), "rb") as f:
-            h.update(name.encode() + f.read())
-    with open(os.path.join(ROOT, "include", "td.h"), "rb") as f:
-        h.update(f.read())
+        with open(os.path.join(src, name)) as f:
+            h.update(name.encode() + _code_only(f.read()).encode())
+    with open(os.path.join(ROOT, "include", "td.h")) as f:
+        h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

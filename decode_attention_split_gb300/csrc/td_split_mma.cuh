@@ -11,7 +11,9 @@
 //   scores  S[rows x 16 keys] = Q[rows x D] . K^T   (B operand from K rows via ldmatrix)
 //   output  O[rows x D]      += P[rows x 16 keys] . V (B operand via ldmatrix.trans)
 // with fp32 accumulation; P is rounded to bf16 for the second product while the softmax
-// statistics (m, l) stay fp32.
+// statistics (m, l) stay fp32. A kv head with at most 8 query rows (decode with grouped
+// heads) takes the narrow tile instead: keys on the M side and the rows on the 8-wide N side
+// (S^T = K Q^T, O^T += V^T P^T; warp_keys16_n8), half the tensor-core tiles per step.
 //
 // K/V stages of 64 rows are fetched by the TMA engine (cp.async.bulk.tensor: one thread
 // issues one box of 64 rows x 128 bytes per half-row) through a 3-D tensor map over the
