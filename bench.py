@@ -117,6 +117,22 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
+def max_over_ranks(values, device) -> list:
+    """Each value's maximum over the ranks of the default process group (the slowest rank's
+    time); the values unchanged when there is no group or a single rank."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(v) for v in values]
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t]
+
+
+def whole_job_gbs(world: int, calls_per_rank: int, bytes_call: int, ms: float) -> float:
+    """GB/s of the whole job: every rank's calls' bytes over the slowest rank's time (ms)."""
+    return world * calls_per_rank * bytes_call / (ms * 1e-3) / 1e9
+
+
 def recorded_traffic(kernel: str, workload_key: str):
     """DRAM bytes per launch from a committed ncu summary, if it was taken on the current kernel source."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
@@ -552,9 +568,7 @@ def run_td(args, world, rank, local):
         ms_rope = time_graph(graphs["rope"], s, max(3, args.steps // 4), warm=2) * args.steps / max(3, args.steps // 4)
     ms = e0.elapsed_time(e1)
     if world > 1:
-        t = torch.tensor([ms, ms_attn], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms, ms_attn = float(t[0]), float(t[1])
+        ms, ms_attn = max_over_ranks([ms, ms_attn], dev)
         torch.distributed.barrier()
 
     # correctness of what was timed: one more replay of the step graph, then its call 0 (which
@@ -575,7 +589,7 @@ def run_td(args, world, rank, local):
         checked = bool(np.all(np.abs(got - ref) <= 2e-2 + 1e-2 * np.abs(ref)))
 
     total_calls = args.steps * R
-    value = world * total_calls * bytes_call / (ms * 1e-3) / 1e9
+    value = whole_job_gbs(world, total_calls, bytes_call, ms)
     us_attn = ms_attn * 1e3 / total_calls
     achieved = bytes_call / (us_attn * 1e-6) / 1e9
 
@@ -677,10 +691,8 @@ def run_e2e(td, args, w, case, kc, vc, C, R, sl_pre, sl_post, ws, dev, bytes_cal
     e1.synchronize()
     ms = e0.elapsed_time(e1)
     if world > 1:
-        t = torch.tensor([ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t[0])
-    return {"value": round(world * steps * R * bytes_call / (ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+        ms = max_over_ranks([ms], dev)[0]
+    return {"value": round(whole_job_gbs(world, steps * R, bytes_call, ms), 1), "unit": "GB/s",
             "h2d_bytes_per_step": inh.numel() * 2, "d2h_bytes_per_step": outh.numel() * 2,
             "steps": steps, "us_per_call": round(ms * 1e3 / (steps * R), 3),
             "host_us_per_call": round(host_s * 1e6 / (steps * R), 3),
