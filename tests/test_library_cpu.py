@@ -137,3 +137,169 @@ def test_hot_kernels_have_no_spills(lib):
                 seen.add(h)
                 assert int(st) == 0 and int(ld) == 0, (name, st, ld)
     assert seen == hot
+
+
+# ------------------------------------------------------------- the later calls' host checks
+
+NAN = float("nan")
+
+
+def _call(fn, order, defaults, kw):
+    a = dict(defaults)
+    a.update(kw)
+    return fn(*[a[k] for k in order])
+
+
+ROPE_APPEND = ("dtype", "q", "q_out", "Hq", "k_new", "v_new", "cos", "sin", "kc", "vc", "sl", "B", "Hkv", "T", "Smax",
+               "D", "adv", "st", "stream")
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(dtype=3), TD_ERR_UNSUPPORTED),
+    (dict(k_new=None), TD_ERR_INVALID_ARG),
+    (dict(q=FAKE), TD_ERR_INVALID_ARG),            # q without q_out
+    (dict(q=FAKE, q_out=FAKE, Hq=0), TD_ERR_INVALID_ARG),
+    (dict(T=0), TD_ERR_INVALID_ARG),
+    (dict(D=8), TD_ERR_UNSUPPORTED),               # a bf16 row of 16 bytes is not two 16-byte halves
+    (dict(cos=FAKE + 4), TD_ERR_UNSUPPORTED),      # misaligned table
+])
+def test_rope_append_rejects_bad_arguments_on_host(lib, kw, expect):
+    d = dict(dtype=1, q=None, q_out=None, Hq=0, k_new=FAKE, v_new=FAKE, cos=FAKE, sin=FAKE, kc=FAKE, vc=FAKE, sl=FAKE,
+             B=1, Hkv=2, T=1, Smax=16, D=64, adv=1, st=None, stream=None)
+    assert _call(lib.td_rope_kv_append, ROPE_APPEND, d, kw) == expect
+
+
+FUSED = ("dtype", "q", "k_new", "v_new", "cos", "sin", "kc", "vc", "sl", "B", "Hq", "Hkv", "T", "Smax", "D", "scale",
+         "split", "adv", "out", "lse", "ws", "wsb", "st", "stream")
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(k_new=None), TD_ERR_INVALID_ARG),
+    (dict(cos=FAKE), TD_ERR_INVALID_ARG),          # a cosine table without the sine table
+    (dict(dtype=0), TD_ERR_UNSUPPORTED),           # the fused step is bf16 only
+    (dict(k_new=FAKE + 8), TD_ERR_UNSUPPORTED),
+    (dict(q=None), TD_ERR_INVALID_ARG),
+    (dict(D=96), TD_ERR_UNSUPPORTED),
+    (dict(scale=NAN), TD_ERR_INVALID_ARG),
+    (dict(Hq=5), TD_ERR_INVALID_ARG),
+])
+def test_fused_step_rejects_bad_arguments_on_host(lib, kw, expect):
+    d = dict(dtype=1, q=FAKE, k_new=FAKE, v_new=FAKE, cos=None, sin=None, kc=FAKE, vc=FAKE, sl=FAKE, B=1, Hq=4, Hkv=2,
+             T=1, Smax=64, D=128, scale=0.1, split=0, adv=1, out=FAKE, lse=None, ws=FAKE, wsb=1 << 20, st=None,
+             stream=None)
+    assert _call(lib.td_rope_append_attn, FUSED, d, kw) == expect
+
+
+SPEC = ("target", "draft", "tokens", "u", "B", "G", "V", "temp", "n_acc", "next", "ws", "wsb", "st", "stream")
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(target=None), TD_ERR_INVALID_ARG),
+    (dict(u=None), TD_ERR_INVALID_ARG),            # sampling needs the uniforms
+    (dict(draft=None), TD_ERR_INVALID_ARG),        # and the draft rows
+    (dict(temp=-1.0), TD_ERR_INVALID_ARG),
+    (dict(temp=NAN), TD_ERR_INVALID_ARG),
+    (dict(G=17), TD_ERR_UNSUPPORTED),
+    (dict(n_acc=FAKE + 2), TD_ERR_UNSUPPORTED),
+    (dict(target=FAKE + 4), TD_ERR_UNSUPPORTED),   # V % 4 == 0: rows are read 16 bytes at a time
+    (dict(wsb=16), TD_ERR_WORKSPACE),
+    (dict(temp=0.0, draft=None, u=None, wsb=16), TD_ERR_WORKSPACE),  # greedy needs neither
+])
+def test_spec_accept_rejects_bad_arguments_on_host(lib, kw, expect):
+    d = dict(target=FAKE, draft=FAKE, tokens=FAKE, u=FAKE, B=1, G=4, V=1000, temp=1.0, n_acc=FAKE, next=FAKE, ws=FAKE,
+             wsb=1 << 26, st=None, stream=None)
+    assert _call(lib.td_spec_accept, SPEC, d, kw) == expect
+
+
+def test_spec_workspace_bytes(lib):
+    assert lib.td_spec_workspace_bytes(1, 17, 1000) == 0
+    assert lib.td_spec_workspace_bytes(0, 4, 1000) == 0
+    n1, n8 = lib.td_spec_workspace_bytes(1, 4, 128256), lib.td_spec_workspace_bytes(8, 4, 128256)
+    assert 0 < n1 < n8 and n1 % 256 == 0
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(dtype=3), TD_ERR_UNSUPPORTED),
+    (dict(x=None), TD_ERR_INVALID_ARG),
+    (dict(rows=0), TD_ERR_INVALID_ARG),
+    (dict(scales=FAKE + 2), TD_ERR_UNSUPPORTED),
+])
+def test_quantize_q8_rejects_bad_arguments_on_host(lib, kw, expect):
+    d = dict(dtype=1, x=FAKE, rows=4, D=128, codes=FAKE, scales=FAKE, stream=None)
+    assert _call(lib.td_quantize_q8, ("dtype", "x", "rows", "D", "codes", "scales", "stream"), d, kw) == expect
+
+
+APPEND_Q8 = ("dtype", "k_new", "v_new", "kc", "ks", "vc", "vs", "sl", "B", "Hkv", "T", "Smax", "D", "adv", "st",
+             "stream")
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(dtype=3), TD_ERR_UNSUPPORTED),
+    (dict(k_new=None), TD_ERR_INVALID_ARG),
+    (dict(vs=None), TD_ERR_INVALID_ARG),
+    (dict(T=0), TD_ERR_INVALID_ARG),
+    (dict(ks=FAKE + 2), TD_ERR_UNSUPPORTED),
+    (dict(B=65536), TD_ERR_UNSUPPORTED),
+])
+def test_append_q8_rejects_bad_arguments_on_host(lib, kw, expect):
+    d = dict(dtype=1, k_new=FAKE, v_new=FAKE, kc=FAKE, ks=FAKE, vc=FAKE, vs=FAKE, sl=FAKE, B=2, Hkv=2, T=1, Smax=16,
+             D=64, adv=1, st=None, stream=None)
+    assert _call(lib.td_kv_append_q8, APPEND_Q8, d, kw) == expect
+
+
+VERIFY_Q8 = ("q", "kc", "ks", "vc", "vs", "sl", "B", "Hq", "Hkv", "T", "Smax", "D", "scale", "split", "out", "lse",
+             "ws", "wsb", "st", "stream")
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(ks=None), TD_ERR_INVALID_ARG),
+    (dict(Smax=66), TD_ERR_UNSUPPORTED),           # scale rows step by whole 16-byte units
+    (dict(vs=FAKE + 4), TD_ERR_UNSUPPORTED),
+    (dict(q=None), TD_ERR_INVALID_ARG),
+    (dict(D=96), TD_ERR_UNSUPPORTED),
+    (dict(Hq=5), TD_ERR_INVALID_ARG),
+    (dict(T=65), TD_ERR_UNSUPPORTED),              # a chunk longer than the cache
+    (dict(scale=NAN), TD_ERR_INVALID_ARG),
+])
+def test_q8_attention_rejects_bad_arguments_on_host(lib, kw, expect):
+    d = dict(q=FAKE, kc=FAKE, ks=FAKE, vc=FAKE, vs=FAKE, sl=FAKE, B=1, Hq=4, Hkv=2, T=1, Smax=64, D=128, scale=0.1,
+             split=0, out=FAKE, lse=None, ws=FAKE, wsb=1 << 20, st=None, stream=None)
+    assert _call(lib.td_verify_attn_q8, VERIFY_Q8, d, kw) == expect
+    if "T" not in kw:  # the decode entry point is the verify call with T = 1
+        order = tuple(k for k in VERIFY_Q8 if k != "T")
+        assert _call(lib.td_decode_attn_q8, order, d, kw) == expect
+
+
+PREFILL = ("q", "kc", "vc", "sl", "B", "Hq", "Hkv", "T", "Smax", "D", "scale", "out", "lse", "st", "stream")
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(q=None), TD_ERR_INVALID_ARG),
+    (dict(Hq=5), TD_ERR_INVALID_ARG),
+    (dict(T=0), TD_ERR_INVALID_ARG),
+    (dict(scale=NAN), TD_ERR_INVALID_ARG),
+    (dict(D=96), TD_ERR_UNSUPPORTED),
+    (dict(T=65), TD_ERR_UNSUPPORTED),              # longer than the cache
+    (dict(out=FAKE + 8), TD_ERR_UNSUPPORTED),
+])
+def test_prefill_rejects_bad_arguments_on_host(lib, kw, expect):
+    d = dict(q=FAKE, kc=FAKE, vc=FAKE, sl=FAKE, B=1, Hq=4, Hkv=2, T=64, Smax=64, D=128, scale=0.1, out=FAKE,
+             lse=None, st=None, stream=None)
+    assert _call(lib.td_prefill_attn, PREFILL, d, kw) == expect
+
+
+NOALLOC = ("dtype", "q", "kc", "vc", "sl", "B", "Hq", "Hkv", "Smax", "D", "scale", "split", "out", "lse", "st",
+           "stream")
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(q=None), TD_ERR_INVALID_ARG),
+    (dict(scale=NAN), TD_ERR_INVALID_ARG),
+    (dict(D=96), TD_ERR_UNSUPPORTED),
+    (dict(dtype=7), TD_ERR_UNSUPPORTED),
+    (dict(Hq=5), TD_ERR_INVALID_ARG),
+])
+def test_noalloc_rejects_bad_arguments_on_host(lib, kw, expect):
+    d = dict(dtype=1, q=FAKE, kc=FAKE, vc=FAKE, sl=FAKE, B=1, Hq=4, Hkv=2, Smax=64, D=128, scale=0.1, split=0,
+             out=FAKE, lse=None, st=None, stream=None)
+    assert _call(lib.td_decode_attn_noalloc, NOALLOC, d, kw) == expect
