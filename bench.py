@@ -400,7 +400,7 @@ def prefill_point(td, dev, T=4096, B=1, Hq=24, Hkv=8, D=128, reps=20):
             "frac_of_peak": round(tf / peak, 4), "peak_kind": f"bf16_tflops of {kind}"}
 
 
-def sweep_point(td, name, L, dev, l2_bytes, peak, budget_calls=200):
+def sweep_point(td, name, L, dev, l2_bytes, peak, budget_calls=200, split=0):
     """Attention kernel alone on one workload point: graph of R launches over rotating caches."""
     w = WORKLOADS[name]
     case = make_case(w, seq_len=L if not w.ragged else None)
@@ -414,17 +414,17 @@ def sweep_point(td, name, L, dev, l2_bytes, peak, budget_calls=200):
     sl = case.seq_lens.to(dev)
     R = max(C, budget_calls)
     out = torch.empty_like(q)
-    ws = td.make_workspace(w.B, w.Hq, w.Hkv, w.Smax, w.D, w.T, 0, device=dev)
+    ws = td.make_workspace(w.B, w.Hq, w.Hkv, w.Smax, w.D, w.T, split, device=dev)
     s = torch.cuda.Stream(dev)
 
     def calls():
         for i in range(R):
             c = i % C
             if w.T == 1:
-                td.td_decode_attn(q[:, :, 0], kc[c], vc[c], sl, case.scale, 0, out=out[:, :, 0], workspace=ws,
+                td.td_decode_attn(q[:, :, 0], kc[c], vc[c], sl, case.scale, split, out=out[:, :, 0], workspace=ws,
                                   stream=s)
             else:
-                td.td_verify_attn(q, kc[c], vc[c], sl, case.scale, 0, out=out, workspace=ws, stream=s)
+                td.td_verify_attn(q, kc[c], vc[c], sl, case.scale, split, out=out, workspace=ws, stream=s)
 
     with torch.cuda.stream(s):
         calls()
@@ -437,9 +437,9 @@ def sweep_point(td, name, L, dev, l2_bytes, peak, budget_calls=200):
     gbs = bytes_call / (us * 1e-6) / 1e9
     del kc, vc
     torch.cuda.empty_cache()
-    return {"workload": name, "seq_len": L if not w.ragged else "ragged", "us_per_call": round(us, 3),
-            "kv_gbs": round(gbs, 1), "frac_of_measured_hbm": round(gbs / peak, 4), "kv_bytes": bytes_call,
-            "cache_copies": C}
+    return {"workload": name, "seq_len": L if not w.ragged else "ragged", "split": split or "auto",
+            "dtype": w.dtype, "us_per_call": round(us, 3), "kv_gbs": round(gbs, 1),
+            "frac_of_measured_hbm": round(gbs / peak, 4), "kv_bytes": bytes_call, "cache_copies": C}
 
 
 def profile_row(td, args, dev):
@@ -600,11 +600,12 @@ def run_td(args, world, rank, local):
     if rank != 0:
         return
     cpu = None if (args.no_cpu or world > 1) else cpu_baseline(case, w, L, args.cpu_seconds)
+    ctable = None if (args.no_cpu or args.no_sweep or world > 1) else cpu_table()
     sweep = next_rows = None
     if not args.no_sweep:
         del kc, vc
         torch.cuda.empty_cache()
-        sweep = []
+        sweep = [sweep_point(td, "tiny_fp32", 128, dev, l2, peak, split=WORKLOADS["tiny_fp32"].split)]
         for name in ("smollm2_360m", "llama3b"):
             for Ls in WORKLOADS[name].seq_lens:
                 sweep.append(sweep_point(td, name, Ls, dev, l2, peak))
@@ -645,6 +646,7 @@ def run_td(args, world, rank, local):
                      "algorithmic_bytes_per_launch": bytes_call},
         "e2e": e2e,
         "cpu_baseline": cpu,
+        "cpu_table": ctable,
         "sweep": sweep,
         "next_rows": next_rows,
         "kernel_source": kernel_source_hash(),
@@ -711,6 +713,61 @@ def cpu_baseline(case, w, L, seconds):
     dt = (time.perf_counter() - t0) / n
     return {"value": round(kv_read_bytes(w, L) / dt / 1e9, 3), "unit": "GB/s", "cores": orc.num_threads,
             "kind": "oracle", "sample": f"{n} full calls (B=1, 24 heads x {L} keys, fp64), {dt * 1e3:.1f} ms each"}
+
+
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo), with the architecture."""
+    import platform
+    import subprocess
+    name = ""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            key, _, val = line.partition(":")
+            if key.strip() in ("Model name", "Vendor ID") and val.strip() and not name.endswith(val.strip()):
+                name = (name + " " + val.strip()).strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    if not name:
+        try:
+            for line in open("/proc/cpuinfo"):
+                if line.lower().startswith(("model name", "cpu part")):
+                    name = line.split(":", 1)[1].strip()
+                    break
+        except OSError:
+            pass
+    return f"{name or 'unknown'} ({platform.machine()}, {os.cpu_count()} logical CPUs)"
+
+
+def cpu_table(reps: int = 3):
+    """The oracle (fp64) on every workload point, single-threaded and on all host cores: median of
+    `reps` full calls each. A reported baseline, not a target."""
+    import oracle
+    orc = oracle.load()
+    cores = os.cpu_count() or 1
+    rows = []
+    points = [("tiny_fp32", 128)] + [("smollm2_360m", L) for L in WORKLOADS["smollm2_360m"].seq_lens] + \
+        [("llama3b", L) for L in WORKLOADS["llama3b"].seq_lens] + [("ragged8", None), ("verify6", 16390)]
+    for name, L in points:
+        w = WORKLOADS[name]
+        case = make_case(w, seq_len=L if not w.ragged else None)
+        qn, kn, vn, sn = (to_numpy(x) for x in (case.q, case.k_cache, case.v_cache, case.seq_lens))
+        nbytes = kv_read_bytes(w, case.seq_lens.tolist())
+        row = {"workload": name, "seq_len": L if L is not None else "ragged", "kv_bytes": nbytes}
+        for label, threads in (("single_thread", 1), ("all_cores", cores)):
+            orc.set_num_threads(threads)
+            times = []
+            for _ in range(reps):
+                t0 = time.perf_counter()
+                orc.attention(qn, kn, vn, sn, case.scale)
+                times.append(time.perf_counter() - t0)
+            med = sorted(times)[len(times) // 2]
+            row[label] = {"threads": threads, "us_per_call": round(med * 1e6, 1),
+                          "kv_gbs": round(nbytes / med / 1e9, 4)}
+        rows.append(row)
+    orc.set_num_threads(cores)
+    return {"cpu": cpu_model(), "statistic": f"median of {reps} full calls", "kind": "oracle (fp64 C, OpenMP)",
+            "rows": rows}
 
 
 def main():

@@ -28,6 +28,7 @@ SYMBOLS = (
     "td_verify_attn",
     "td_lse_merge",
     "td_decode_attn_noalloc",
+    "td_selftest_wait_timeout",
 )
 
 _lock = threading.Lock()
@@ -84,6 +85,8 @@ def _declare(lib):
     lib.td_lse_merge.restype = i
     lib.td_decode_attn_noalloc.argtypes = [i, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, vp, vp, vp]
     lib.td_decode_attn_noalloc.restype = i
+    lib.td_selftest_wait_timeout.argtypes = [ll, vp, vp, vp]
+    lib.td_selftest_wait_timeout.restype = i
     return lib
 
 

@@ -8,10 +8,21 @@ namespace {
 
 thread_local int g_last_cuda_error = 0;
 
+}  // namespace
+
+namespace td {
+
 td_status cuda_fail(cudaError_t e) {
+  cudaGetLastError();  // a launch error is reported once, by the call that met it
   g_last_cuda_error = (int)e;
   return TD_ERR_CUDA;
 }
+
+}  // namespace td
+
+namespace {
+
+using td::cuda_fail;
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }

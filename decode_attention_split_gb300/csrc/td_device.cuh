@@ -58,14 +58,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Waits for phase `parity` of an mbarrier to complete; false after kWaitLimitCycles.
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+// Waits for phase `parity` of an mbarrier to complete; false once `limit` SM cycles have
+// passed without it.
+__device__ __forceinline__ bool mbar_wait_bounded_for(uint32_t bar, uint32_t parity, long long limit) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (!mbar_try_wait(bar, parity)) {
-    if (clock64() - t0 > kWaitLimitCycles) return false;
+    if (clock64() - t0 > limit) return false;
   }
   return true;
+}
+
+// The kernels' wait: false after kWaitLimitCycles.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+  return mbar_wait_bounded_for(bar, parity, kWaitLimitCycles);
 }
 
 // Orders this thread's earlier generic-proxy global accesses (and those it has observed, e.g.

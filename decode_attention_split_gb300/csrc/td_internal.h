@@ -29,6 +29,10 @@ struct SplitPlan {
   size_t off_part, bytes;  // workspace layout: counters, then partial blocks
 };
 
+// Records a failed CUDA call for td_last_cuda_error (and clears the runtime's last-error slot,
+// so a later call does not report it as its own); returns TD_ERR_CUDA.
+td_status cuda_fail(cudaError_t e);
+
 // Fills *plan for the current device; TD_OK, or an error for unsupported shapes.
 // q8: the caches hold int8 codes with per-row scales (q and out are bf16; dtype must be TD_BF16).
 td_status plan_split(td_dtype dtype, int B, int Hq, int Hkv, int T, int Smax, int D, int split, SplitPlan *plan,

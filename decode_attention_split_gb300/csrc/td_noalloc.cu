@@ -31,12 +31,15 @@ void *g_scratch_addr[kMaxDevices] = {};
 // and cached.
 td_status scratch_address(void **addr) {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return TD_ERR_CUDA;
+  const cudaError_t ed = cudaGetDevice(&dev);
+  if (ed != cudaSuccess) return td::cuda_fail(ed);
   if (dev < 0 || dev >= kMaxDevices) return TD_ERR_UNSUPPORTED;
   std::lock_guard<std::mutex> lock(g_mu);
   if (g_scratch_addr[dev] == nullptr) {
     void *p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_scratch) != cudaSuccess || p == nullptr) return TD_ERR_CUDA;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_scratch);
+    if (e != cudaSuccess) return td::cuda_fail(e);
+    if (p == nullptr) return td::cuda_fail(cudaErrorInvalidSymbol);
     g_scratch_addr[dev] = p;
   }
   *addr = g_scratch_addr[dev];
@@ -56,18 +59,24 @@ extern "C" td_status td_decode_attn_noalloc(td_dtype dtype, const void *q, const
   if (!isfinite(scale)) return TD_ERR_INVALID_ARG;
   td::SplitPlan plan;
   const td_status st = td::plan_split(dtype, B, Hq, Hkv, 1, Smax, D, split, &plan);
+  if (st == TD_ERR_CUDA) return td::cuda_fail(cudaGetLastError());
   if (st != TD_OK) return st;
   if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
       !aligned(seq_lens, 4) || (lse != nullptr && !aligned(lse, 4)) || (dev_status != nullptr && !aligned(dev_status, 4)))
     return TD_ERR_UNSUPPORTED;
-  if (plan.bytes > kScratchBytes) return TD_ERR_WORKSPACE;  // the shape needs more scratch than the array holds
+  // the shape needs more scratch than the array holds: the same test a caller can make with
+  // td_decode_workspace_bytes (the largest layout over the element types), so the documented
+  // limit and this check agree
+  if (plan.bytes > kScratchBytes || td_decode_workspace_bytes(B, Hq, Hkv, Smax, D, 1, split) > kScratchBytes)
+    return TD_ERR_WORKSPACE;
   void *scratch = nullptr;
   const td_status sa = scratch_address(&scratch);
   if (sa != TD_OK) return sa;
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   // the completion counters must start at zero; the previous call (any shape) may have left
   // partial results where this layout keeps its counters
-  if (cudaMemsetAsync(scratch, 0, plan.off_part, s) != cudaSuccess) return TD_ERR_CUDA;
+  const cudaError_t em = cudaMemsetAsync(scratch, 0, plan.off_part, s);
+  if (em != cudaSuccess) return td::cuda_fail(em);
   unsigned char *ws = static_cast<unsigned char *>(scratch);
   td::SplitParams p = {};
   p.q = q;
@@ -93,5 +102,6 @@ extern "C" td_status td_decode_attn_noalloc(td_dtype dtype, const void *q, const
   p.min_chunk = plan.min_chunk;
   p.warm_stages = plan.warm;
   p.qscale = scale * td::kLog2e;
-  return td::launch_split(dtype, D, plan, p, s) == cudaSuccess ? TD_OK : TD_ERR_CUDA;
+  const cudaError_t e = td::launch_split(dtype, D, plan, p, s);
+  return e == cudaSuccess ? TD_OK : td::cuda_fail(e);
 }

@@ -123,7 +123,6 @@ td_status td_split_plan(td_dtype dtype, int B, int Hq, int Hkv, int Smax, int D,
                         int *grid, int *cluster, int *rows);
 
 /*
- * Cache append:/*
  * Cache append: for each b with 0 <= L = seq_lens[b] and L + T <= Smax, copies
  * k_new[b, h, t, :] to k_cache[b, h, L + t, :] (and v likewise) bit for bit for all h < Hkv,
  * t < T. With advance != 0, seq_lens[b] += T afterwards (same launch, after every read of
@@ -280,6 +279,19 @@ td_status td_verify_attn_q8(const void *q, const int8_t *k_codes, const float *k
 td_status td_prefill_attn(const void *q, const void *k_cache, const void *v_cache, const int32_t *seq_lens, int B,
                           int Hq, int Hkv, int T, int Smax, int D, float scale, void *out, float *lse,
                           uint32_t *dev_status, void *stream);
+
+/*
+ * Diagnostic of the bounded wait (the pages describe no such call; it exists so that the
+ * failure path every kernel relies on can be exercised without a fault). One CTA waits for
+ * the first phase of an mbarrier that nothing arrives on and no copy completes, with the
+ * kernels' wait routine and a limit of limit_cycles SM cycles (1 .. 1e9, about half a second
+ * at most; TD_ERR_INVALID_ARG outside). The wait gives up, the kernel ORs
+ * TD_DEV_WAIT_TIMEOUT into *dev_status (device, required) and returns; nothing is in flight
+ * when it gives up. waited_cycles (device, nullable, 8-byte aligned) receives the cycles the
+ * wait took. Asynchronous on `stream`.
+ */
+td_status td_selftest_wait_timeout(long long limit_cycles, uint32_t *dev_status, long long *waited_cycles,
+                                   void *stream);
 
 /*
  * Decode attention without a workspace argument: the same computation and arguments as

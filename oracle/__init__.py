@@ -105,6 +105,8 @@ class Oracle:
         lib.orc_spec_accept.argtypes = [vp, vp, vp, vp, i, i, i, d, vp, vp]
         lib.orc_spec_accept.restype = ctypes.c_uint
         lib.orc_num_threads.restype = i
+        lib.orc_set_num_threads.argtypes = [i]
+        lib.orc_set_num_threads.restype = None
         lib.orc_mutant.restype = i
         self.lib = lib
         self.mutant = lib.orc_mutant()
@@ -112,6 +114,10 @@ class Oracle:
     @property
     def num_threads(self) -> int:
         return self.lib.orc_num_threads()
+
+    def set_num_threads(self, n: int) -> None:
+        """Threads of later calls (timing only; results do not depend on it)."""
+        self.lib.orc_set_num_threads(int(n))
 
     @staticmethod
     def _shapes(q, k, v, seq_lens):

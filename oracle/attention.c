@@ -74,6 +74,16 @@ int orc_num_threads(void) {
 #endif
 }
 
+/* Threads later parallel loops use (n >= 1); for timing the oracle single-threaded and on all
+ * cores. No effect on the arithmetic: each row is computed by one thread in a fixed order. */
+void orc_set_num_threads(int n) {
+#ifdef _OPENMP
+  if (n >= 1) omp_set_num_threads(n);
+#else
+  (void)n;
+#endif
+}
+
 /* Element i of a stored array, widened exactly to fp64. A bf16 number is the upper half of
  * an IEEE binary32 number: widening places its 16 bits above 16 zero bits. */
 static double widen(int dtype, const void *base, int64_t i) {

@@ -11,7 +11,8 @@ import torch
 
 import oracle
 from decode_attention_split_gb300.workloads import WORKLOADS, make_case, small_case, to_numpy
-from parity import assert_lse_close, assert_out_close, oracle_attention
+from parity import (assert_lse_close, assert_out_close, assert_value_close, case_value_stats, oracle_attention,
+                    value_stats)
 
 pytestmark = pytest.mark.gpu
 
@@ -46,6 +47,8 @@ def check_case(td, case, split=0, **kw):
     out, lse, st = run_attention(td, case, split=split, **kw)
     ref, ref_lse, ref_st = oracle_attention(case, **kw)
     assert_out_close(out, ref, case.w.dtype)
+    if case.w.dtype == "bf16":
+        assert_value_close(out, ref, case_value_stats(case, ref_lse, **kw))
     assert_lse_close(lse, ref_lse)
     assert st == ref_st
     return out, lse
@@ -169,6 +172,7 @@ def test_verify_short_sequence_flags(td):
     ref, ref_lse, ref_st = oracle_attention(case)
     assert st == ref_st == td.DEV_VERIFY_SHORT
     assert_out_close(out, ref, "bf16")
+    assert_value_close(out, ref, case_value_stats(case, ref_lse))
     assert_lse_close(lse, ref_lse)
 
 
@@ -254,6 +258,7 @@ def test_workload_ragged8_append_then_attend(td, split):
     out, lse = td.td_decode_attn(case.q.cuda()[:, :, 0], kc, vc, sl, case.scale, split, return_lse=True)
     ref, ref_lse, _ = oracle.load().attention(to_numpy(case.q), ek, ev, es, case.scale)
     assert_out_close(out.cpu()[:, :, None], ref, "bf16")
+    assert_value_close(out.cpu()[:, :, None], ref, value_stats(to_numpy(case.q), ek, ev, es, case.scale, ref_lse))
     assert_lse_close(lse.cpu()[:, :, None], ref_lse)
 
 
@@ -268,6 +273,7 @@ def test_workload_verify6_append_then_verify(td, split):
     out, lse = td.td_verify_attn(case.q.cuda(), kc, vc, sl, case.scale, split, return_lse=True)
     ref, ref_lse, _ = oracle.load().attention(to_numpy(case.q), ek, ev, es, case.scale)
     assert_out_close(out.cpu(), ref, "bf16")
+    assert_value_close(out.cpu(), ref, value_stats(to_numpy(case.q), ek, ev, es, case.scale, ref_lse))
     assert_lse_close(lse.cpu(), ref_lse)
 
 
@@ -332,6 +338,7 @@ def test_empty_sequence(td):
     assert torch.isneginf(lse[0]).all() and torch.isneginf(lse[2]).all() and torch.isfinite(lse[1]).all()
     ref, ref_lse, _ = oracle_attention(case)
     assert_out_close(out, ref, "bf16")
+    assert_value_close(out, ref, case_value_stats(case, ref_lse))
 
 
 def test_all_empty_batch(td):
@@ -347,6 +354,7 @@ def test_lengths_out_of_range_are_clamped_and_flagged(td):
     ref, ref_lse, ref_st = oracle_attention(case)
     assert ref_st == st
     assert_out_close(out, ref, "bf16")
+    assert_value_close(out, ref, case_value_stats(case, ref_lse))
     assert_lse_close(lse, ref_lse)
 
 
@@ -395,9 +403,11 @@ def test_graph_capture_and_replay(td):
         g.replay()
         torch.cuda.synchronize()
         orc.kv_append(to_numpy(knh), to_numpy(vnh), ek, ev, es, advance=True)
-        ref, _, _ = orc.attention(to_numpy(qh), ek, ev, es, case.scale)
+        ref, ref_lse, _ = orc.attention(to_numpy(qh), ek, ev, es, case.scale)
         assert sl.cpu().numpy().tolist() == es.tolist()
         assert_out_close(out.cpu(), ref, "bf16", what=f"replay {step}")
+        assert_value_close(out.cpu(), ref, value_stats(to_numpy(qh), ek, ev, es, case.scale, ref_lse),
+                           what=f"replay {step}")
 
 
 def test_binding_errors(td):

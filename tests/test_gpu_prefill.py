@@ -11,7 +11,7 @@ import torch
 
 import oracle
 from decode_attention_split_gb300.workloads import small_case, to_numpy
-from parity import assert_lse_close, assert_out_close
+from parity import assert_lse_close, assert_out_close, assert_value_close, value_stats
 
 pytestmark = pytest.mark.gpu
 
@@ -50,10 +50,11 @@ def test_prefill_against_oracle(td, B, Hq, Hkv, D, Smax, T, lens):
     case = small_case(dtype="bf16", B=B, Hq=Hq, Hkv=Hkv, D=D, Smax=Smax, T=T, seq_lens=lens, seed=T + D,
                       heavy=0.02)
     out, lse, st = _run(td, case)
-    ref, ref_lse, ref_st = oracle.load().attention(to_numpy(case.q), to_numpy(case.k_cache),
-                                                   to_numpy(case.v_cache), case.seq_lens.numpy(), case.scale)
+    args = (to_numpy(case.q), to_numpy(case.k_cache), to_numpy(case.v_cache), case.seq_lens.numpy(), case.scale)
+    ref, ref_lse, ref_st = oracle.load().attention(*args)
     assert st == ref_st
     assert_out_close(out, ref, "bf16")
+    assert_value_close(out, ref, value_stats(*args, ref_lse))
     assert_lse_close(lse, ref_lse)
 
 
@@ -61,10 +62,11 @@ def test_prefill_chunk_longer_than_sequence_flags(td):
     """Rows that see no key give 0 and -inf and the verify-short bit, as td_verify_attn."""
     case = small_case(dtype="bf16", B=1, Hq=2, Hkv=1, D=128, Smax=64, T=40, seq_lens=[30], seed=3)
     out, lse, st = _run(td, case)
-    ref, ref_lse, ref_st = oracle.load().attention(to_numpy(case.q), to_numpy(case.k_cache),
-                                                   to_numpy(case.v_cache), case.seq_lens.numpy(), case.scale)
+    args = (to_numpy(case.q), to_numpy(case.k_cache), to_numpy(case.v_cache), case.seq_lens.numpy(), case.scale)
+    ref, ref_lse, ref_st = oracle.load().attention(*args)
     assert st == ref_st == td.DEV_VERIFY_SHORT
     assert_out_close(out, ref, "bf16")
+    assert_value_close(out, ref, value_stats(*args, ref_lse))
     assert_lse_close(lse, ref_lse)
 
 
@@ -74,9 +76,10 @@ def test_prefill_never_reads_past_the_length(td):
     k[:, :, 333:] = float("nan")
     v[:, :, 333:] = float("nan")
     out, lse, _ = _run(td, case, k, v)
-    ref, ref_lse, _ = oracle.load().attention(to_numpy(case.q), to_numpy(case.k_cache), to_numpy(case.v_cache),
-                                              case.seq_lens.numpy(), case.scale)
+    args = (to_numpy(case.q), to_numpy(case.k_cache), to_numpy(case.v_cache), case.seq_lens.numpy(), case.scale)
+    ref, ref_lse, _ = oracle.load().attention(*args)
     assert_out_close(out, ref, "bf16")
+    assert_value_close(out, ref, value_stats(*args, ref_lse))
     assert_lse_close(lse, ref_lse)
 
 
@@ -102,9 +105,10 @@ def test_prefill_long_prompt_sampled_rows(td, T):
     for hq, t in picks:  # the first row, the last rows of the prompt, then random ones
         kvh = hq // 3
         qrow = to_numpy(case.q[:, hq:hq + 1, t])  # [1, 1, D]
-        ref, ref_lse, _ = orc.attention(qrow, kn[:, kvh:kvh + 1], vn[:, kvh:kvh + 1], np.array([t + 1], np.int32),
-                                        case.scale)
+        args = (qrow, kn[:, kvh:kvh + 1], vn[:, kvh:kvh + 1], np.array([t + 1], np.int32), case.scale)
+        ref, ref_lse, _ = orc.attention(*args)
         assert_out_close(out[:, hq:hq + 1, t], ref, "bf16", what=f"row ({hq}, {t})")
+        assert_value_close(out[:, hq:hq + 1, t], ref, value_stats(*args, ref_lse), what=f"row ({hq}, {t})")
         assert_lse_close(lse[:, hq:hq + 1, t], ref_lse)
 
 
@@ -117,7 +121,8 @@ def test_prefill_zero_and_negative_scale(td, scale):
     out, lse = td.td_prefill_attn(case.q.cuda(), case.k_cache.cuda(), case.v_cache.cuda(), case.seq_lens.cuda(),
                                   scale, dev_status=st, return_lse=True)
     torch.cuda.synchronize()
-    ref, ref_lse, _ = oracle.load().attention(to_numpy(case.q), to_numpy(case.k_cache), to_numpy(case.v_cache),
-                                              case.seq_lens.numpy(), scale)
+    args = (to_numpy(case.q), to_numpy(case.k_cache), to_numpy(case.v_cache), case.seq_lens.numpy(), scale)
+    ref, ref_lse, _ = oracle.load().attention(*args)
     assert_out_close(out.cpu(), ref, "bf16")
+    assert_value_close(out.cpu(), ref, value_stats(*args, ref_lse))
     assert_lse_close(lse.cpu(), ref_lse)

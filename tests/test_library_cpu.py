@@ -303,3 +303,19 @@ def test_noalloc_rejects_bad_arguments_on_host(lib, kw, expect):
     d = dict(dtype=1, q=FAKE, kc=FAKE, vc=FAKE, sl=FAKE, B=1, Hq=4, Hkv=2, Smax=64, D=128, scale=0.1, split=0,
              out=FAKE, lse=None, st=None, stream=None)
     assert _call(lib.td_decode_attn_noalloc, NOALLOC, d, kw) == expect
+
+
+SELFTEST = ("limit", "st", "waited", "stream")
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(limit=0), TD_ERR_INVALID_ARG),
+    (dict(limit=-5), TD_ERR_INVALID_ARG),
+    (dict(limit=2_000_000_000), TD_ERR_INVALID_ARG),   # past the half-second cap
+    (dict(st=None), TD_ERR_INVALID_ARG),
+    (dict(st=FAKE + 2), TD_ERR_UNSUPPORTED),
+    (dict(waited=FAKE + 4), TD_ERR_UNSUPPORTED),
+])
+def test_wait_timeout_diagnostic_rejects_bad_arguments_on_host(lib, kw, expect):
+    d = dict(limit=1000, st=FAKE, waited=None, stream=None)
+    assert _call(lib.td_selftest_wait_timeout, SELFTEST, d, kw) == expect

@@ -1,51 +1,70 @@
-"""td_decode_attn_noalloc through the C ABI, against td_decode_attn.
+"""td_decode_attn_noalloc through the C ABI, against the oracle and against td_decode_attn.
 
-The entry point serves callers that cannot allocate device memory (its scratch is a fixed
-array inside the library). Two calls in a row, with different shapes, so the second call
-runs on the scratch the first left behind; each must match the workspace entry point within
-the bf16 tolerance. A shape beyond the array's size is refused on the host. This file is collected last so a run stopping at its first failure has
-already run every other test.
+The entry point serves callers that cannot allocate device memory: a plugin or launch hook
+that is handed only its input and output pointers, or a serving loop that must not allocate
+once it runs. Its scratch is a fixed array inside the library. Four calls in a row on that one
+array, with different shapes, element types and split sizes (a bf16 3B-style layer, the
+fp32 config with its named split 64, the bf16 360M layer, the 3B-style layer with an explicit
+split), so every call after the first runs on scratch an earlier call left behind. Each must
+match the oracle (the stated tolerance and, for bf16, the value-side bound) and the workspace
+entry point on the same inputs. A shape beyond the array's size is refused on the host. This
+file is collected last so a run stopping at its first failure has already run every other
+test.
 """
 import ctypes
 
 import pytest
 import torch
 
-from decode_attention_split_gb300.workloads import make_case
-from parity import assert_lse_close, assert_out_close
+from decode_attention_split_gb300.workloads import make_case, to_numpy
+from parity import assert_lse_close, assert_out_close, check_bf16_attention, oracle_attention
 
 pytestmark = pytest.mark.gpu
 
+_DTYPE = {torch.float32: 0, torch.bfloat16: 1}
 
-def _noalloc(lib, q, kc, vc, sl, scale, out, lse, status):
+
+def _noalloc(lib, q, kc, vc, sl, scale, split, out, lse, status):
     B, Hq, D = q.shape
     _, Hkv, Smax, _ = kc.shape
-    st = lib.td_decode_attn_noalloc(1, q.data_ptr(), kc.data_ptr(), vc.data_ptr(), sl.data_ptr(), B, Hq, Hkv, Smax,
-                                    D, ctypes.c_float(scale), 0, out.data_ptr(), lse.data_ptr(), status.data_ptr(),
-                                    torch.cuda.current_stream().cuda_stream)
-    return st
+    return lib.td_decode_attn_noalloc(_DTYPE[q.dtype], q.data_ptr(), kc.data_ptr(), vc.data_ptr(), sl.data_ptr(), B,
+                                      Hq, Hkv, Smax, D, ctypes.c_float(scale), split, out.data_ptr(), lse.data_ptr(),
+                                      status.data_ptr(), torch.cuda.current_stream().cuda_stream)
 
 
-def test_noalloc_matches_workspace_entry_point_twice():
+CALLS = [("llama3b", 4096, 0), ("tiny_fp32", 128, 64), ("smollm2_360m", 4096, 0), ("llama3b", 16384, 512)]
+
+
+def test_noalloc_matches_oracle_and_workspace_entry_point_in_a_row():
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     from decode_attention_split_gb300 import _lib, build
     build.build()
     import decode_attention_split_gb300 as td
     lib = _lib.lib()
-    for name, L in (("llama3b", 4096), ("smollm2_360m", 4096)):
+    for name, L, split in CALLS:
         case = make_case(name, seq_len=L)
+        dt = case.w.dtype
         q = case.q[:, :, 0].contiguous().cuda()
         kc, vc, sl = case.k_cache.cuda(), case.v_cache.cuda(), case.seq_lens.cuda()
-        ref, ref_lse = td.td_decode_attn(q, kc, vc, sl, case.scale, 0, return_lse=True)
         out = torch.full_like(q, float("nan"))
-        lse = torch.full(ref_lse.shape, float("nan"), dtype=torch.float32, device="cuda")
+        lse = torch.full(q.shape[:2], float("nan"), dtype=torch.float32, device="cuda")
         status = torch.zeros(1, dtype=torch.int32, device="cuda")
-        assert _noalloc(lib, q, kc, vc, sl, case.scale, out, lse, status) == 0
+        assert _noalloc(lib, q, kc, vc, sl, case.scale, split, out, lse, status) == 0, name
         torch.cuda.synchronize()
         assert int(status.item()) == 0
-        assert_out_close(out.cpu(), ref.double().cpu().numpy(), "bf16", what=f"{name} out")
-        assert_lse_close(lse.cpu(), ref_lse.double().cpu().numpy(), what=f"{name} lse")
+        what = f"{name} L={L} split={split}"
+        if dt == "bf16":
+            check_bf16_attention(out.cpu(), lse.cpu(), to_numpy(case.q[:, :, 0]), to_numpy(case.k_cache),
+                                 to_numpy(case.v_cache), to_numpy(case.seq_lens), case.scale, what=what)
+        else:
+            ref, ref_lse, _ = oracle_attention(case)
+            assert_out_close(out.cpu()[:, :, None], ref, dt, what=what)
+            assert_lse_close(lse.cpu()[:, :, None], ref_lse, what=f"{what} lse")
+        ws_out, ws_lse = td.td_decode_attn(q, kc, vc, sl, case.scale, split, return_lse=True)
+        torch.cuda.synchronize()
+        assert_out_close(out.cpu(), ws_out.double().cpu().numpy(), dt, what=f"{what} vs workspace call")
+        assert_lse_close(lse.cpu(), ws_lse.double().cpu().numpy(), what=f"{what} lse vs workspace call")
 
 
 def test_noalloc_rejects_shapes_beyond_its_scratch():
@@ -63,4 +82,4 @@ def test_noalloc_rejects_shapes_beyond_its_scratch():
     out = torch.empty_like(q)
     lse = torch.empty(16, 32, dtype=torch.float32, device="cuda")
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
-    assert _noalloc(lib, q, kc, kc, sl, 0.1, out, lse, status) == 3  # TD_ERR_WORKSPACE
+    assert _noalloc(lib, q, kc, kc, sl, 0.1, 0, out, lse, status) == 3  # TD_ERR_WORKSPACE
