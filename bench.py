@@ -282,13 +282,17 @@ def time_graph(graph, stream, reps, warm=2):
 def kernel_label(td, w) -> str:
     """Which split-attention kernel the timed call runs, from the library's own launch plan."""
     plan = td.td_split_plan(w.torch_dtype, w.B, w.Hq, w.Hkv, w.Smax, w.D, w.T, 0)
-    # query rows per CTA: 8 or fewer go on the n side of the tensor-core tile (the narrow tile)
-    tile = "narrow tile" if plan["rows"] <= 8 else "m16 tile"
+    # query rows per CTA: 8 or fewer go on one n8 tile, 17 to 24 on three (the narrow tiles)
+    r = plan["rows"]
+    tile = "narrow n8 tile" if r <= 8 else "m16 tile" if r <= 16 else "narrow 24-row tile"
     names = {
         "tensor_core_persistent": f"split_attn_mma_kernel<{w.D}> (persistent, fused split + workspace merge, "
                                   f"mma.sync bf16 {tile}, TMA)",
         "tensor_core_cluster": f"split_attn_cluster_kernel<{w.D}> (clusters of {plan['cluster']}, on-chip merge, "
                                f"mma.sync bf16 {tile}, TMA)",
+        "tensor_core_cluster_combine": f"split_attn_cc_kernel<{w.D}> (persistent clusters of {plan['cluster']}: "
+                                       f"chunk partials combined on chip, row-slice merges through the workspace, "
+                                       f"mma.sync bf16 {tile}, TMA)",
         "cuda_core": f"split_attn_kernel<{w.D}> (CUDA cores)",
     }
     return f"{names[plan['kernel']]}, grid {plan['grid']}, timed alone"

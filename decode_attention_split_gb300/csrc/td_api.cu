@@ -70,7 +70,9 @@ td_status prepare(td_dtype dtype, const void *q, const void *k_cache, const void
   p->min_chunk = plan->min_chunk;
   p->warm_stages = plan->warm;
   p->qscale = scale * td::kLog2e;
-  p->done = p->counters + (size_t)B * Hkv * plan->RB;
+  p->done = p->counters + plan->counters_n;
+  p->deferred = plan->deferred ? 1 : 0;
+  p->plan_out = p->counters + plan->counters_n + 1;
   return TD_OK;
 }
 

@@ -1,4 +1,5 @@
 // Instantiations, launch planning and per-device attribute cache for the split-attention kernel.
+#include <algorithm>
 #include <mutex>
 
 #include "td_internal.h"
@@ -86,34 +87,51 @@ bool encode_cache_map(CUtensorMap *map, const void *base, int B, int Hkv, int Sm
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The persistent kernel's instantiation for this launch: the tile by the rows; the plan made
+// before the wait for the previous kernel when one row block of at most 16 rows covers a kv
+// head (decode with grouped heads), after it otherwise (the 24-row tile has no registers to
+// spare for the early plan: it spilled).
+template <int D>
+cudaError_t launch_mma_tile(const MmaArgs &a, int grid, int smem, cudaStream_t stream) {
+  const int tile = tile_of_rows(a.p.R);
+  if (a.p.RB == 1 && tile == kTileN8)
+    return launch_pdl(split_attn_mma_kernel<D, true, kTileN8>, dim3(grid), dim3(kThreads), smem, stream, a);
+  if (a.p.RB == 1 && tile == kTileM16)
+    return launch_pdl(split_attn_mma_kernel<D, true, kTileM16>, dim3(grid), dim3(kThreads), smem, stream, a);
+  if (tile == kTileN8)
+    return launch_pdl(split_attn_mma_kernel<D, false, kTileN8>, dim3(grid), dim3(kThreads), smem, stream, a);
+  if (tile == kTileM16)
+    return launch_pdl(split_attn_mma_kernel<D, false, kTileM16>, dim3(grid), dim3(kThreads), smem, stream, a);
+  return launch_pdl(split_attn_mma_kernel<D, false, kTileN24>, dim3(grid), dim3(kThreads), smem, stream, a);
+}
+
 template <int D>
 cudaError_t launch_mma(const SplitParams &p, int grid, int smem, cudaStream_t stream) {
   MmaArgs a;
   if (!encode_cache_map(&a.kmap, p.k, p.B, p.Hkv, p.Smax, D) || !encode_cache_map(&a.vmap, p.v, p.B, p.Hkv, p.Smax, D))
     return cudaErrorInvalidValue;
   a.p = p;
-  if (p.RB == 1) {
-    // the decode instantiations (rows on the m side, or at most 8 rows on the n side): their
-    // shared-memory opt-in, once per device (the plan's occupancy query set the other's)
+  {
+    // every instantiation's shared-memory opt-in, once per device (the plan's occupancy query
+    // set the m16 late-plan one's)
     static std::mutex mu;
     static bool done[kMaxDevices] = {};
     int device = 0;
     if (cudaGetDevice(&device) != cudaSuccess || device < 0 || device >= kMaxDevices) return cudaErrorInvalidDevice;
-    {
-      std::lock_guard<std::mutex> lock(mu);
-      if (!done[device]) {
-        for (const void *fn : {reinterpret_cast<const void *>(&split_attn_mma_kernel<D, true, false>),
-                               reinterpret_cast<const void *>(&split_attn_mma_kernel<D, true, true>)}) {
-          const cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-          if (e != cudaSuccess) return e;
-        }
-        done[device] = true;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!done[device]) {
+      for (const void *fn : {reinterpret_cast<const void *>(&split_attn_mma_kernel<D, true, kTileN8>),
+                             reinterpret_cast<const void *>(&split_attn_mma_kernel<D, true, kTileM16>),
+                             reinterpret_cast<const void *>(&split_attn_mma_kernel<D, false, kTileN8>),
+                             reinterpret_cast<const void *>(&split_attn_mma_kernel<D, false, kTileM16>),
+                             reinterpret_cast<const void *>(&split_attn_mma_kernel<D, false, kTileN24>)}) {
+        const cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
       }
+      done[device] = true;
     }
-    if (p.R <= 8) return launch_pdl(split_attn_mma_kernel<D, true, true>, dim3(grid), dim3(kThreads), smem, stream, a);
-    return launch_pdl(split_attn_mma_kernel<D, true, false>, dim3(grid), dim3(kThreads), smem, stream, a);
   }
-  return launch_pdl(split_attn_mma_kernel<D, false, false>, dim3(grid), dim3(kThreads), smem, stream, a);
+  return launch_mma_tile<D>(a, grid, smem, stream);
 }
 
 template <int D>
@@ -121,7 +139,7 @@ KernelRef mma_ref_of() {
   // the ring plus 1024 bytes of slack for its alignment
   constexpr int smem = MmaCfg<D, kPersistentStages<D>>::RING_BYTES + 1024;
   static_assert(smem + 8448 <= 227 * 1024, "mma kernel shared memory");
-  return KernelRef{reinterpret_cast<const void *>(&split_attn_mma_kernel<D, false, false>), smem, &launch_mma<D>};
+  return KernelRef{reinterpret_cast<const void *>(&split_attn_mma_kernel<D, false, kTileM16>), smem, &launch_mma<D>};
 }
 
 KernelRef pick_mma(int D, int MT) {
@@ -201,12 +219,15 @@ constexpr int cluster_smem() {
 static_assert(cluster_smem<128>() + 1024 <= 227 * 1024 && cluster_smem<64>() + 1024 <= 227 * 1024,
               "cluster kernel shared memory");
 
-const void *cluster_fn(int D, bool narrow) {
-  if (narrow)
-    return D == 64 ? reinterpret_cast<const void *>(&split_attn_cluster_kernel<64, true>)
-                   : reinterpret_cast<const void *>(&split_attn_cluster_kernel<128, true>);
-  return D == 64 ? reinterpret_cast<const void *>(&split_attn_cluster_kernel<64, false>)
-                 : reinterpret_cast<const void *>(&split_attn_cluster_kernel<128, false>);
+const void *cluster_fn(int D, int tile) {
+  if (D == 64) {
+    if (tile == kTileN8) return reinterpret_cast<const void *>(&split_attn_cluster_kernel<64, kTileN8>);
+    if (tile == kTileM16) return reinterpret_cast<const void *>(&split_attn_cluster_kernel<64, kTileM16>);
+    return reinterpret_cast<const void *>(&split_attn_cluster_kernel<64, kTileN24>);
+  }
+  if (tile == kTileN8) return reinterpret_cast<const void *>(&split_attn_cluster_kernel<128, kTileN8>);
+  if (tile == kTileM16) return reinterpret_cast<const void *>(&split_attn_cluster_kernel<128, kTileM16>);
+  return reinterpret_cast<const void *>(&split_attn_cluster_kernel<128, kTileN24>);
 }
 
 cudaLaunchConfig_t cluster_config(int D, int grid, int cs, cudaStream_t stream, cudaLaunchAttribute *attr) {
@@ -234,8 +255,11 @@ cudaError_t launch_cluster(const SplitParams &p, int grid, int cs, cudaStream_t 
   a.p = p;
   cudaLaunchAttribute attr[2];
   const cudaLaunchConfig_t cfg = cluster_config(D, grid, cs, stream, attr);
-  if (p.R <= 8) return cudaLaunchKernelEx(&cfg, split_attn_cluster_kernel<D, true>, a);
-  return cudaLaunchKernelEx(&cfg, split_attn_cluster_kernel<D, false>, a);
+  switch (tile_of_rows(p.R)) {
+    case kTileN8: return cudaLaunchKernelEx(&cfg, split_attn_cluster_kernel<D, kTileN8>, a);
+    case kTileM16: return cudaLaunchKernelEx(&cfg, split_attn_cluster_kernel<D, kTileM16>, a);
+    default: return cudaLaunchKernelEx(&cfg, split_attn_cluster_kernel<D, kTileN24>, a);
+  }
 }
 
 // variant: row padding RP of the CUDA-core kernel, or m tiles MT of the tensor-core kernel
@@ -267,8 +291,8 @@ int blocks_per_sm(int device, int slot, const KernelRef &k) {
 }
 
 // Clusters of `cs` CTAs (2, 4, 8 or 16) of the cluster kernel that the device holds at once;
-// sets the shared-memory and cluster-size opt-ins of both instantiations on first use and
-// asks about the wider one (the narrow one needs fewer registers). 0 on error.
+// sets the shared-memory and cluster-size opt-ins of every instantiation on first use and
+// asks about the one with the most registers (the 24-row narrow tile's). 0 on error.
 int active_clusters(int device, int D, int cs) {
   const int di = D == 64 ? 0 : 1, ci = cs == 2 ? 0 : cs == 4 ? 1 : cs == 8 ? 2 : 3;
   std::lock_guard<std::mutex> lock(g_mu);
@@ -279,14 +303,14 @@ int active_clusters(int device, int D, int cs) {
   cfg.numAttrs = 1;  // the cluster shape alone
   int n = 0;
   bool ok = true;
-  for (const bool narrow : {true, false}) {
-    const void *fn = cluster_fn(D, narrow);
+  for (const int tile : {kTileN8, kTileM16, kTileN24}) {
+    const void *fn = cluster_fn(D, tile);
     ok = ok &&
          cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)cfg.dynamicSmemBytes) ==
              cudaSuccess &&
          cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess;
   }
-  if (!ok || cudaOccupancyMaxActiveClusters(&n, cluster_fn(D, false), &cfg) != cudaSuccess) {
+  if (!ok || cudaOccupancyMaxActiveClusters(&n, cluster_fn(D, kTileN24), &cfg) != cudaSuccess) {
     cudaGetLastError();
     n = 0;
   }
@@ -322,6 +346,33 @@ static int device_l2_bytes(int device) {
   return n;
 }
 
+// Shared memory of merge_slices_kernel: the staging of up to 46 chunks' slices of 4 rows at D = 128.
+constexpr int kMergeSlicesSmem = 100 * 1024;
+
+template <int D>
+cudaError_t launch_merge_slices_d(const SplitParams &p, cudaStream_t stream) {
+  static std::mutex mu;
+  static bool done[kMaxDevices] = {};
+  int device = 0;
+  if (cudaGetDevice(&device) != cudaSuccess || device < 0 || device >= kMaxDevices) return cudaErrorInvalidDevice;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (!done[device]) {
+      const cudaError_t e = cudaFuncSetAttribute(merge_slices_kernel<__nv_bfloat16, D>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kMergeSlicesSmem);
+      if (e != cudaSuccess) return e;
+      done[device] = true;
+    }
+  }
+  const int grid = p.B * p.Hkv * p.RB * ((p.R + kSliceRows - 1) / kSliceRows);
+  return launch_pdl(merge_slices_kernel<__nv_bfloat16, D>, dim3(grid), dim3(kThreads), kMergeSlicesSmem, stream, p,
+                    kMergeSlicesSmem / 4);
+}
+
+cudaError_t launch_merge_slices(int D, const SplitParams &p, cudaStream_t stream) {
+  return D == 64 ? launch_merge_slices_d<64>(p, stream) : launch_merge_slices_d<128>(p, stream);
+}
+
 td_status plan_split(td_dtype dtype, int B, int Hq, int Hkv, int T, int Smax, int D, int split, SplitPlan *plan,
                      bool q8) {
   if (dtype != TD_F32 && dtype != TD_BF16) return TD_ERR_UNSUPPORTED;
@@ -329,15 +380,17 @@ td_status plan_split(td_dtype dtype, int B, int Hq, int Hkv, int T, int Smax, in
   if (B < 1 || Hq < 1 || Hkv < 1 || T < 1 || Smax < 1 || split < 0 || Hq % Hkv != 0) return TD_ERR_INVALID_ARG;
   if (B > TD_MAX_BATCH || Smax > (1 << 30) || T > Smax) return TD_ERR_UNSUPPORTED;
   const long long GT = (long long)(Hq / Hkv) * T;
-  // bf16 caches: tensor-core kernel, one 16-row m tile per CTA, the group's rows split evenly
-  // over ceil(rows / 16) row blocks (a 24-row verify chunk: two blocks of 12, whose second
-  // read of each K/V tile is mostly served by L2, and two half-size merges in parallel);
-  // fp32 caches: CUDA-core kernel, up to 4 (D = 128) or 8 (D = 64) rows per CTA
+  // bf16 caches: tensor-core kernels, the group's rows split evenly over row blocks of at most
+  // 24 rows (tile_of_rows: up to 8 on the narrow n8 tile, 9 to 16 on one m16 tile, 17 to 24 on
+  // three n8 tiles, so a 24-row verify chunk reads each K/V tile once); the 8-bit cache kernel
+  // has no 24-row tile and takes blocks of at most 16 rows. fp32 caches: CUDA-core kernel, up
+  // to 4 (D = 128) or 8 (D = 64) rows per CTA
   const bool mma = dtype == TD_BF16;
   int R, variant;
   if (mma) {
     variant = 1;
-    const long long blocks = (GT + 15) / 16;
+    const long long most = q8 ? 16 : kMaxTileRows;
+    const long long blocks = (GT + most - 1) / most;
     R = (int)((GT + blocks - 1) / blocks);
   } else {
     const int rmax = D == 128 ? 4 : 8;
@@ -424,10 +477,17 @@ td_status plan_split(td_dtype dtype, int B, int Hq, int Hkv, int T, int Smax, in
     const long long warm = RB == 1 ? (l2 * 9 / 10) / ((long long)plan->grid * unit) : 4;
     plan->warm = (int)(warm < 1 ? 1 : warm > 16 ? 16 : warm);
   }
-  // completion counters, one per (b, kv head, row block), then the fused step's read count
-  const size_t counters = align256(((size_t)B * U + 1) * sizeof(int));
+  // the persistent kernel's merge for row blocks of more than 16 rows runs as a second kernel,
+  // one CTA per slice of kSliceRows rows of each group: one CTA staging every chunk's 24 rows
+  // (a verify block of four grouped heads x 6 tokens) took 28 us where the chunks streamed in 7
+  plan->deferred = mma && !q8 && plan->cluster == 0 && R > 16;
+  // completion counters, one per (b, kv head, row block), then the fused step's read count,
+  // then the deferred merge's plan (chunk size, attended lengths)
+  plan->counters_n = (int)((long long)B * U);
+  const size_t counters = align256(((size_t)plan->counters_n + 2 + B) * sizeof(int));
   plan->off_part = counters;
-  plan->bytes = plan->off_part + align256((size_t)B * U * ns * part_block_floats(R, D) * sizeof(float));
+  const size_t block = (size_t)std::max(part_block_floats(R, D), R * merge_row_floats(D));
+  plan->bytes = plan->off_part + align256((size_t)B * U * ns * block * sizeof(float));
   return TD_OK;
 }
 
@@ -444,6 +504,7 @@ cudaError_t launch_split(td_dtype dtype, int D, const SplitPlan &plan, const Spl
     if (k.fn == nullptr) return cudaErrorInvalidValue;
     e = k.launch(p, plan.grid, plan.smem, stream);
   }
+  if (e == cudaSuccess && plan.deferred) e = launch_merge_slices(D, p, stream);
   if (e != cudaSuccess) {
     cudaGetLastError();  // clear a launch error so it is reported once, by this call
     return e;

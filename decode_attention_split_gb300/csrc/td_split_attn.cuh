@@ -54,6 +54,12 @@ struct SplitParams {
   int min_chunk;        // smallest automatic chunk (keys)
   int warm_stages;      // 64-row units of its first chunk each CTA warms in L2 before the wait
   float qscale;         // scale * log2(e)
+  // Deferred merge (row blocks of more than 16 rows): chunk partials are published in the
+  // row-major layout (merge_row_floats) without a completion ticket, and merge_slices_kernel,
+  // launched next in the stream, merges them; the split kernel's CTA 0 records the chunk size
+  // and the attended lengths for it in `plan_out` ([0] chunk size, [1 + b] attended length).
+  int deferred;
+  int *plan_out;
   // Fused step (tensor-core kernels only; k_new == null for plain attention): the T new rows
   // of each (b, kv head) go to cache rows seq_lens[b] .. seq_lens[b]+T-1 in this launch, the
   // query and key rows rotated there first when rope tables are given, and every query row
@@ -89,6 +95,10 @@ __device__ __forceinline__ int attended_len(const SplitParams &p, int32_t raw, u
 // m[R] (base-2 units) and l[R]; padded to whole 16-byte units so blocks can be
 // bulk-copied and every acc row is 16-byte aligned.
 __host__ __device__ constexpr int part_block_floats(int R, int D) { return (R * (D + 2) + 3) / 4 * 4; }
+
+// Deferred merge: a chunk's partial is R rows of acc[D], m (base 2), l, padded to 16 bytes, so
+// a run of rows of one chunk is contiguous.
+__host__ __device__ constexpr int merge_row_floats(int D) { return D + 4; }
 
 
 template <typename E, int D, int RP>
@@ -393,16 +403,176 @@ __device__ void merge_group(const SplitParams &p, float *smem_f, int smem_floats
   }
 }
 
+// Rows of a slice of the deferred merge (one CTA of merge_slices_kernel each).
+constexpr int kSliceRows = 2;
+
+// Deferred merge of rows [s0, s1) of group (b, kv head, row block rb) over its NC chunk
+// partials in the row-major layout (merge_row_floats), staged from L2 by bulk asynchronous
+// copies (one contiguous run of rows per chunk), as many chunks at a time as `smem_floats`
+// holds, and merged online as merge_group does. Writes out and lse.
+template <typename E, int D>
+__device__ void merge_row_slice(const SplitParams &p, float *smem_f, int smem_floats, uint64_t *bar, uint32_t &phase,
+                                int b, int kvh, int rb, int NC, int s0, int s1) {
+  constexpr int RF = merge_row_floats(D), D4 = D / 4, kFB = 64;
+  static_assert(D4 % 8 == 0, "whole warps per pass of the weighted sums");
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int ns = s1 - s0;
+  const long long g = ((long long)b * p.Hkv + kvh) * p.RB + rb;
+  const float *src = p.ws_part + (g * p.ns_ws * p.R + s0) * (long long)RF;  // chunk c at + c * R * RF
+  float *acc = smem_f;            // [ns][D] running weighted sums (between rounds)
+  float *st = acc + ns * D;       // M[ns], Lsum[ns], rescale[ns], 1 / Lsum[ns]
+  float *fac = st + 4 * ns;       // [ns][kFB] factors 2^(m_c - M) of the staged chunks
+  float *stage = fac + ns * kFB;  // [FB][ns][RF], 16-byte aligned: ns * (D + 68) floats before it
+  int FB = (smem_floats - ns * (D + 4 + kFB)) / (ns * RF);
+  if (FB > kFB) FB = kFB;
+  if (tid < ns) {
+    st[tid] = -INFINITY;
+    st[ns + tid] = 0.f;
+  }
+#pragma unroll 1
+  for (int c0 = 0; c0 < NC; c0 += FB) {
+    const int nb = min(FB, NC - c0);
+    const bool last = c0 + nb >= NC;
+    if (tid == 0) {
+      fence_proxy_async_global();
+      mbar_arrive_expect_tx(smem_u32(bar), (uint32_t)(nb * ns * RF * 4));
+      for (int c = 0; c < nb; ++c)
+        bulk_g2s_plain(smem_u32(stage + c * ns * RF), src + (long long)(c0 + c) * p.R * RF, (uint32_t)(ns * RF * 4),
+                       smem_u32(bar));
+    }
+    if (!mbar_wait_bounded(smem_u32(bar), phase)) {
+      report(p.status, TD_DEV_WAIT_TIMEOUT);
+      mbar_wait_bounded(smem_u32(bar), phase);  // one more bounded wait for the copies in flight
+    }
+    phase ^= 1u;
+    __syncthreads();  // staged runs and the previous round's statistics are visible
+    // per-row statistics of this round (base 2): a warp per row, lanes over chunks
+#pragma unroll 1
+    for (int r = warp; r < ns; r += kWarps) {
+      float mv[2], lv[2];
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const int c = lane + 32 * k;
+        lv[k] = c < nb ? stage[(c * ns + r) * RF + D + 1] : 0.f;
+        mv[k] = lv[k] > 0.f ? stage[(c * ns + r) * RF + D] : -INFINITY;
+      }
+      float bm = fmaxf(mv[0], mv[1]);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, o));
+      const float Mo = st[r];
+      const float Mn = fmaxf(Mo, bm);
+      const float base = Mn == -INFINITY ? 0.f : Mn;
+      float ls = 0.f;
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const float f = lv[k] > 0.f ? exp2f(mv[k] - base) : 0.f;
+        if (lane + 32 * k < nb) fac[r * kFB + lane + 32 * k] = f;
+        ls = fmaf(lv[k], f, ls);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) ls += __shfl_xor_sync(0xffffffffu, ls, o);
+      if (lane == 0) {
+        const float alpha = exp2f(Mo - base);
+        const float Ls = st[ns + r] * alpha + ls;
+        st[r] = Mn;
+        st[ns + r] = Ls;
+        st[2 * ns + r] = alpha;
+        st[3 * ns + r] = Ls > 0.f ? 1.f / Ls : 0.f;
+        if (last && p.lse != nullptr)
+          p.lse[out_row_of(p, b, kvh, rb, s0 + r)] = Ls > 0.f ? (Mn + log2f(Ls)) * kLn2 : -INFINITY;
+      }
+    }
+    __syncthreads();
+    // weighted sums: four lanes per (row, four dims), each over every fourth staged chunk,
+    // summed by shuffles; in the last round they are the output
+#pragma unroll 1
+    for (int idx = tid; idx < ns * D4 * 4; idx += kThreads) {
+      const int q = idx & 3, pr = idx >> 2;
+      const int r = pr / D4, d = (pr % D4) * 4;
+      const float *a = stage + r * RF + d;
+      const float *f = fac + r * kFB;
+      float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+      for (int c = q; c < nb; c += 4) {
+        const float4 v = *reinterpret_cast<const float4 *>(a + c * ns * RF);
+        const float w = f[c];
+        x.x = fmaf(v.x, w, x.x), x.y = fmaf(v.y, w, x.y), x.z = fmaf(v.z, w, x.z), x.w = fmaf(v.w, w, x.w);
+      }
+#pragma unroll
+      for (int o = 1; o < 4; o <<= 1) {
+        x.x += __shfl_xor_sync(0xffffffffu, x.x, o);
+        x.y += __shfl_xor_sync(0xffffffffu, x.y, o);
+        x.z += __shfl_xor_sync(0xffffffffu, x.z, o);
+        x.w += __shfl_xor_sync(0xffffffffu, x.w, o);
+      }
+      if (q != 0) continue;
+      if (c0 > 0) {
+        const float sc = st[2 * ns + r];
+        const float4 y = *reinterpret_cast<const float4 *>(acc + r * D + d);
+        x.x = fmaf(y.x, sc, x.x), x.y = fmaf(y.y, sc, x.y), x.z = fmaf(y.z, sc, x.z), x.w = fmaf(y.w, sc, x.w);
+      }
+      if (last) {
+        const float inv = st[3 * ns + r];
+        E *o = static_cast<E *>(p.out) + out_row_of(p, b, kvh, rb, s0 + r) * D + d;
+        store_elem<E>(o + 0, x.x * inv);
+        store_elem<E>(o + 1, x.y * inv);
+        store_elem<E>(o + 2, x.z * inv);
+        store_elem<E>(o + 3, x.w * inv);
+      } else {
+        *reinterpret_cast<float4 *>(acc + r * D + d) = x;
+      }
+    }
+    __syncthreads();  // the next round overwrites the staging area
+  }
+}
+
+// Deferred merge ("tinydecode" and "llm-decode-cuda": the chunks' partials merged by
+// log-sum-exp in a second step): one CTA per (b, kv head, row block, slice of kSliceRows
+// rows), launched right after a split kernel with p.deferred set and scheduled while it drains
+// (programmatic dependent launch). The split kernel's CTA 0 recorded the chunk size and every
+// sequence's attended length in p.plan_out; sequences of one chunk were written out by the
+// split kernel itself. For row blocks of more than 16 rows (a 24-row verify block of four
+// grouped heads) the merge of every chunk's rows then runs in parallel across the row slices,
+// where one CTA per group would stage every chunk's 24 rows by itself.
+template <typename E, int D>
+__global__ void __launch_bounds__(kThreads) merge_slices_kernel(const SplitParams p, int smem_floats) {
+  extern __shared__ __align__(16) float msm[];
+  __shared__ __align__(8) uint64_t bar;
+  const int tid = threadIdx.x;
+  const int nsl = (p.R + kSliceRows - 1) / kSliceRows;
+  const int sl = blockIdx.x % nsl;
+  const int g = blockIdx.x / nsl;
+  const int rb = g % p.RB;
+  const int kvh = (g / p.RB) % p.Hkv;
+  const int b = g / (p.RB * p.Hkv);
+  if (tid == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    fence_mbar_init();
+  }
+  griddep_wait();  // the split kernel's partials and plan
+  griddep_launch_dependents();
+  __syncthreads();
+  const int S = p.plan_out[0];
+  const int L = p.plan_out[1 + b];
+  if (S <= 0 || L <= S) return;  // nothing to merge: no key, or one chunk written out directly
+  const int NC = (L + S - 1) / S;
+  const int nv = min(p.R, p.G * p.T - rb * p.R);
+  const int s0 = sl * kSliceRows, s1 = min(s0 + kSliceRows, nv);
+  if (s0 >= s1) return;
+  uint32_t phase = 0;
+  merge_row_slice<E, D>(p, msm, smem_floats, &bar, phase, b, kvh, rb, NC, s0, s1);
+}
+
 // Completes one work item (sequence b, kv head, row block rb, chunk c of NC).
 // The item's partial sources (warps or key slices) have written, in base-2 units,
-//   cm[NSRC][ROWS] (row max), cl[NSRC][ROWS] (row sum), ca[NSRC][ROWS][D] (unnormalised p @ V)
+//   cm[NSRC][ROWS] (row max), cl[NSRC][ROWS] (row sum), ca[NSRC][ROWS][CAS] (unnormalised p @ V)
 // at the start of the CTA's shared memory (`smem_f`, `smem_floats` floats free after this
 // call's combine), and a __syncthreads has made them visible. The sources are combined; a
 // chunk that is its sequence's only one writes out/lse, any other writes its partial block
-// to the workspace and takes a completion ticket, and the CTA holding the last ticket of
-// (b, kv head, row block) merges all chunks and zeroes the counter again. Ends with a
-// __syncthreads (the shared areas may be reused afterwards).
-template <typename E, int D, int ROWS, int NSRC>
+// to the workspace and, unless the merge is deferred, takes a completion ticket, and the CTA
+// holding the last ticket of (b, kv head, row block) merges all chunks and zeroes the counter
+// again. Ends with a __syncthreads (the shared areas may be reused afterwards).
+template <typename E, int D, int ROWS, int NSRC, int CAS = D>
 __device__ void finish_item(const SplitParams &p, float *smem_f, int smem_floats, uint64_t *merge_bar,
                             uint32_t &merge_phase, int b, int kvh, int rb, int c, int NC, int *s_last) {
   constexpr int D4 = D / 4;
@@ -412,29 +582,61 @@ __device__ void finish_item(const SplitParams &p, float *smem_f, int smem_floats
   const float *cm = smem_f;
   const float *cl = smem_f + NSRC * ROWS;
   const float *ca = smem_f + 2 * NSRC * ROWS;
+  // Many rows (more than 8): the factor 2^(m_w - M) of each source and row (0 for an empty
+  // source), the maximum and the sum are computed once per row first; few rows: each thread
+  // computes its row's from the sources itself (no extra barrier).
+  float *fac = smem_f + 2 * NSRC * ROWS + NSRC * ROWS * CAS;
+  float *rM = fac + NSRC * ROWS;
+  float *rL = rM + ROWS;
   const bool single = NC == 1;
   const int nv = min(R, GT - rb * R);  // rows of this block that exist
+  const bool rowwise = ROWS > 16 || nv > 8;  // always for 24-row blocks
   const long long g = ((long long)b * p.Hkv + kvh) * p.RB + rb;
-  float *blk = p.ws_part + (g * p.ns_ws + c) * (long long)part_block_floats(R, D);
-#pragma unroll 1
-  for (int idx = tid; idx < nv * D4; idx += kThreads) {
-    const int r = idx / D4, d = (idx % D4) * 4;
-    float M = -INFINITY;
+  if (rowwise) {
+    for (int r = tid; r < nv; r += kThreads) {
+      float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < NSRC; ++w) M = fmaxf(M, cm[w * ROWS + r]);
-    float Ls = 0.f;
-    float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (M != -INFINITY) {
+      for (int w = 0; w < NSRC; ++w) M = fmaxf(M, cm[w * ROWS + r]);
+      float Ls = 0.f;
 #pragma unroll
       for (int w = 0; w < NSRC; ++w) {
         const float mw = cm[w * ROWS + r];
-        if (mw != -INFINITY) {
-          const float f = exp2f(mw - M);
-          Ls = fmaf(cl[w * ROWS + r], f, Ls);
-          const float4 v = *reinterpret_cast<const float4 *>(ca + (w * ROWS + r) * D + d);
-          A.x = fmaf(v.x, f, A.x), A.y = fmaf(v.y, f, A.y), A.z = fmaf(v.z, f, A.z), A.w = fmaf(v.w, f, A.w);
-        }
+        const float f = mw == -INFINITY ? 0.f : exp2f(mw - M);
+        fac[w * ROWS + r] = f;
+        Ls = fmaf(cl[w * ROWS + r], f, Ls);
       }
+      rM[r] = M;
+      rL[r] = Ls;
+    }
+    __syncthreads();
+  }
+  float *blk = p.ws_part + (g * p.ns_ws + c) * (long long)part_block_floats(R, D);
+  float *row_blk = p.ws_part + (g * p.ns_ws + c) * (long long)R * merge_row_floats(D);
+#pragma unroll 1
+  for (int idx = tid; idx < nv * D4; idx += kThreads) {
+    const int r = idx / D4, d = (idx % D4) * 4;
+    float M, Ls = 0.f, f[NSRC];
+    if (rowwise) {
+      M = rM[r];
+      Ls = rL[r];
+#pragma unroll
+      for (int w = 0; w < NSRC; ++w) f[w] = fac[w * ROWS + r];
+    } else {
+      M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < NSRC; ++w) M = fmaxf(M, cm[w * ROWS + r]);
+#pragma unroll
+      for (int w = 0; w < NSRC; ++w) {
+        const float mw = cm[w * ROWS + r];
+        f[w] = mw == -INFINITY ? 0.f : exp2f(mw - M);
+        Ls = fmaf(cl[w * ROWS + r], f[w], Ls);
+      }
+    }
+    float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int w = 0; w < NSRC; ++w) {
+      const float4 v = *reinterpret_cast<const float4 *>(ca + (w * ROWS + r) * CAS + d);
+      A.x = fmaf(v.x, f[w], A.x), A.y = fmaf(v.y, f[w], A.y), A.z = fmaf(v.z, f[w], A.z), A.w = fmaf(v.w, f[w], A.w);
     }
     if (single) {
       const long long row = out_row_of(p, b, kvh, rb, r);
@@ -445,6 +647,13 @@ __device__ void finish_item(const SplitParams &p, float *smem_f, int smem_floats
       store_elem<E>(o + 2, A.z * inv);
       store_elem<E>(o + 3, A.w * inv);
       if (d == 0 && p.lse != nullptr) p.lse[row] = Ls > 0.f ? (M + log2f(Ls)) * kLn2 : -INFINITY;
+    } else if (p.deferred) {
+      float *dst = row_blk + r * merge_row_floats(D);
+      *reinterpret_cast<float4 *>(dst + d) = A;
+      if (d == 0) {
+        dst[D] = Ls > 0.f ? M : -INFINITY;
+        dst[D + 1] = Ls;
+      }
     } else {
       *reinterpret_cast<float4 *>(blk + r * D + d) = A;
       if (d == 0) {
@@ -453,7 +662,7 @@ __device__ void finish_item(const SplitParams &p, float *smem_f, int smem_floats
       }
     }
   }
-  if (!single) {
+  if (!single && !p.deferred) {
     __syncthreads();  // every thread's block writes happen before thread 0's release
     int *cnt = p.counters + g;
     if (tid == 0) {

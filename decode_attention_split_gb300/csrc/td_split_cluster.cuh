@@ -18,18 +18,20 @@
 
 namespace td {
 
-// NARROW: a group has at most 8 query rows and the warps step with warp_keys16_n8.
-template <int D, bool NARROW = false>
+// TILE: the warps' step for the group's rows (tile_of_rows).
+template <int D, int TILE = kTileM16>
 __global__ void __launch_bounds__(kThreads, 1) split_attn_cluster_kernel(const __grid_constant__ MmaArgs a) {
   constexpr int NST = kClusterStages<D>;
   constexpr int D4 = D / 4;
+  constexpr int TR = tile_rows<TILE>();
   using C = MmaCfg<D, NST>;
-  static_assert((C::COMBINE_FLOATS + kMmaRows * (D + 2)) * 4 <= C::RING_BYTES, "local block fits in the ring");
+  static_assert((combine_floats<D, TILE>() + TR * (D + 2)) * 4 <= C::RING_BYTES, "local block fits in the ring");
+  static_assert(combine_floats<D, TILE>() % 4 == 0, "the local block is 16-byte aligned");
   const SplitParams &p = a.p;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   __shared__ __align__(8) uint64_t s_bars[NST];
-  __shared__ float s_w[kMaxCluster][kMmaRows];  // CTA 0: merge weight of each block's rows
-  __shared__ float s_lse[kMmaRows];
+  __shared__ float s_w[kMaxCluster][TR];  // CTA 0: merge weight of each block's rows
+  __shared__ float s_lse[TR];
   __shared__ int s_flag;
 
   const int tid = threadIdx.x;
@@ -68,10 +70,10 @@ __global__ void __launch_bounds__(kThreads, 1) split_attn_cluster_kernel(const _
   const int c0 = min((int)rank * S, L);
   const int c1 = min(c0 + S, L);
   uint32_t seq = 0;
-  stream_chunk<D, NST, NARROW>(a, smem, s_bars, seq, b, kvh, rb, L, c0, c1);
+  stream_chunk<D, NST, TILE>(a, smem, s_bars, seq, b, kvh, rb, L, c0, c1);
   const float *combine = reinterpret_cast<const float *>(smem);
-  float *blk = reinterpret_cast<float *>(smem) + C::COMBINE_FLOATS;  // acc[R][D], m[R], l[R]
-  combine_block<D>(combine, blk, R, nv);
+  float *blk = reinterpret_cast<float *>(smem) + combine_floats<D, TILE>();  // acc[R][D], m[R], l[R]
+  combine_block<D, TR>(combine, blk, R, nv);
   cluster_sync_all();  // every CTA's block is written and visible to CTA 0
 
   if (rank == 0) {

@@ -13,7 +13,10 @@
 // with fp32 accumulation; P is rounded to bf16 for the second product while the softmax
 // statistics (m, l) stay fp32. A kv head with at most 8 query rows (decode with grouped
 // heads) takes the narrow tile instead: keys on the M side and the rows on the 8-wide N side
-// (S^T = K Q^T, O^T += V^T P^T; warp_keys16_n8), half the tensor-core tiles per step.
+// (S^T = K Q^T, O^T += V^T P^T; warp_keys16_n8), half the tensor-core tiles per step; a row
+// block of 17 to 24 rows (a speculative-verify chunk of a grouped kv head: 4 heads x 6
+// tokens) takes the same layout with three 8-wide N tiles (warp_keys16_n24), so each K/V tile
+// in shared memory serves all 24 rows once.
 //
 // K/V stages of 64 rows are fetched by the TMA engine (cp.async.bulk.tensor: one thread
 // issues one box of 64 rows x 128 bytes per half-row) through a 3-D tensor map over the
@@ -37,6 +40,32 @@ namespace td {
 
 constexpr int kMmaRows = 16;  // query rows per CTA: one m16 tile
 
+// Tile of a warp's 16-key step, by the query rows of a row block:
+//   kTileN8   at most 8 rows: keys on the m side, the rows on one 8-wide n tile (warp_keys16_n8);
+//   kTileM16  9 to 16 rows: the rows on the m side of one 16-row tile, keys on n (warp_keys16);
+//   kTileN24  17 to 24 rows: keys on the m side, the rows on three 8-wide n tiles
+//             (warp_keys16_n24).
+enum : int { kTileM16 = 0, kTileN8 = 1, kTileN24 = 2 };
+constexpr int kMaxTileRows = 24;
+// Rows of a tile's combine area and partial blocks.
+template <int TILE>
+__host__ __device__ constexpr int tile_rows() {
+  return TILE == kTileN24 ? kMaxTileRows : kMmaRows;
+}
+// Floats between consecutive rows of the combine area's p @ V sums: D + 4 puts the 32 lanes'
+// stores of one fragment (narrow layouts: dims gid (+8) of rows 2 tig (+1)) in 32 different
+// banks (4-way conflicts with a stride of D).
+template <int D>
+__host__ __device__ constexpr int combine_stride() {
+  return D + 4;
+}
+template <int D, int TILE>
+__host__ __device__ constexpr int combine_floats() {
+  return kWarps * tile_rows<TILE>() * (combine_stride<D>() + 2);
+}
+// Tile for a row block of R query rows.
+__host__ __device__ constexpr int tile_of_rows(int R) { return R <= 8 ? kTileN8 : R <= 16 ? kTileM16 : kTileN24; }
+
 template <int D, int NST_>
 struct MmaCfg {
   static constexpr int NST = NST_;            // ring stages
@@ -51,11 +80,11 @@ struct MmaCfg {
   static constexpr int RING_BYTES = NST * STAGE_BYTES;
   static constexpr int NTD = D / 8;           // 8-wide output n tiles
   static constexpr int KSD = D / 16;          // 16-deep score k steps
-  static constexpr int COMBINE_FLOATS = kWarps * kMmaRows * (D + 2);
+  static constexpr int COMBINE_FLOATS = kWarps * kMaxTileRows * (D + 6);  // the widest tile's
   static_assert(TKW == 16, "each warp takes one 16-key step per stage");
   static_assert(D % 64 == 0, "whole 128-byte halves");
   static_assert(COMBINE_FLOATS * 4 <= RING_BYTES, "combine area fits in the ring");
-  static_assert(kMmaRows * D * 2 <= TILE_BYTES, "the query tile fits in one K tile");
+  static_assert(kMaxTileRows * D * 2 <= TILE_BYTES, "the query tile fits in one K tile");
 };
 
 // Ring depth of the persistent kernel (two CTAs per SM) and of the cluster kernel (one).
@@ -306,18 +335,106 @@ __device__ __forceinline__ void warp_keys16_n8(const uint32_t (&qb)[D / 16][2], 
   }
 }
 
+// The narrow step for 17 to 24 query rows: warp_keys16_n8's layout with three 8-wide n tiles
+// (rows 8 nt .. 8 nt + 7 on tile nt), so one K and one V fragment load per 16 keys serve all
+// 24 rows. A thread holds keys gid and gid + 8 of rows 8 nt + 2 tig (+1) of each tile, i.e. six
+// rows, reduced over the 8 lanes that share a tig. o[nt][dt] holds O^T of dims 16 dt + gid (+8)
+// and rows 8 nt + 2 tig (+1); the row limits, maxima and sums are indexed 2 nt + e.
+template <int D>
+__device__ __forceinline__ void warp_keys16_n24(const uint32_t (&qb)[3][D / 16][2], uint32_t kt, uint32_t vt, int kr,
+                                                int key0, const int (&lim)[6], float qscale, float (&o)[3][D / 16][4],
+                                                float (&m_run)[6], float (&l_run)[6]) {
+  constexpr int TK = 64, KSD = D / 16;
+  const int lane = threadIdx.x & 31, gid = lane >> 2;
+  // three independent accumulators, one per n tile
+  float sc[3][4];
+#pragma unroll
+  for (int nt = 0; nt < 3; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+  const int krow = kr + (lane & 7) + ((lane >> 3) & 1) * 8;
+#pragma unroll
+  for (int j = 0; j < KSD; ++j) {
+    uint32_t ak[4];
+    ldmatrix_x4(ak, kt + tma_swz<TK>(krow, 2 * j + (lane >> 4)));
+#pragma unroll
+    for (int nt = 0; nt < 3; ++nt) mma_bf16_16816(sc[nt], ak, qb[nt][j][0], qb[nt][j][1]);
+  }
+  // scale to base-2 units and mask; element i of tile nt is key gid + 8 (i >> 1) of row
+  // 8 nt + 2 tig + (i & 1)
+  float alpha[6];
+#pragma unroll
+  for (int nt = 0; nt < 3; ++nt) {
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int ri = 2 * nt + e;
+#pragma unroll
+      for (int hk = 0; hk < 2; ++hk) {
+        const int key = key0 + gid + 8 * hk;
+        sc[nt][2 * hk + e] = key < lim[ri] ? sc[nt][2 * hk + e] * qscale : -INFINITY;
+      }
+      float mx = fmaxf(sc[nt][e], sc[nt][2 + e]);
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+      // lazy reference maximum, as in warp_keys16
+      const bool move = mx > m_run[ri] + kMaxGap;
+      alpha[ri] = move ? exp2_approx(m_run[ri] - mx) : 1.f;
+      if (move) m_run[ri] = mx;
+      const float base = m_run[ri] == -INFINITY ? 0.f : m_run[ri];
+      const float p0 = exp2_approx(sc[nt][e] - base), p1 = exp2_approx(sc[nt][2 + e] - base);
+      sc[nt][e] = p0;
+      sc[nt][2 + e] = p1;
+      l_run[ri] = l_run[ri] * alpha[ri] + (p0 + p1);  // this thread's keys; lanes summed at the end
+    }
+  }
+  bool rescale = false;
+#pragma unroll
+  for (int ri = 0; ri < 6; ++ri) rescale |= alpha[ri] != 1.f;
+  if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll
+    for (int nt = 0; nt < 3; ++nt)
+#pragma unroll
+      for (int dt = 0; dt < KSD; ++dt) {
+        o[nt][dt][0] *= alpha[2 * nt];
+        o[nt][dt][1] *= alpha[2 * nt + 1];
+        o[nt][dt][2] *= alpha[2 * nt];
+        o[nt][dt][3] *= alpha[2 * nt + 1];
+      }
+  }
+  // P^T of each n tile as B operands: keys 2 tig (+1) (+8) of row 8 nt + gid
+  uint32_t pb[3][2];
+#pragma unroll
+  for (int nt = 0; nt < 3; ++nt) {
+    pb[nt][0] = movmatrix_trans(pack_bf16x2(sc[nt][0], sc[nt][1]));
+    pb[nt][1] = movmatrix_trans(pack_bf16x2(sc[nt][2], sc[nt][3]));
+  }
+  const int vrow = kr + (lane & 7) + (lane >> 4) * 8;
+#pragma unroll
+  for (int dt = 0; dt < KSD; ++dt) {
+    uint32_t av[4];
+    ldmatrix_x4_trans(av, vt + tma_swz<TK>(vrow, 2 * dt + ((lane >> 3) & 1)));
+#pragma unroll
+    for (int nt = 0; nt < 3; ++nt) mma_bf16_16816(o[nt][dt], av, pb[nt][0], pb[nt][1]);
+  }
+}
+
 // Streams keys [c0, c1) of kv head kvh of sequence b (attended length L) for the query rows
 // of row block rb through the ring at `smem` (1024-byte aligned; NST stages with barriers
 // s_bars; `seq` counts the stages this CTA has consumed, for the barrier parities) and leaves
 // the four warps' partial results, in base-2 units, in the combine area at the start of the
-// ring: cm[4][16] (row max), cl[4][16] (row sum), ca[4][16][D] (unnormalised p @ V).
+// ring, TR = tile_rows<TILE>() rows per warp: cm[4][TR] (row max), cl[4][TR] (row sum),
+// ca[4][TR][CAS] (unnormalised p @ V, rows CAS = combine_stride<D>() floats apart). An empty
+// range (c0 == c1) leaves empty partials.
 // Returns false, CTA-uniformly, if a copy never completed: the status bit is set, the other
 // copies in flight have been waited for, and the combine area holds empty partials.
 // Ends with a __syncthreads.
-template <int D, int NST, bool NARROW = false>
+template <int D, int NST, int TILE = kTileM16>
 __device__ bool stream_chunk(const MmaArgs &a, unsigned char *smem, uint64_t *s_bars, uint32_t &seq, int b, int kvh,
                              int rb, int L, int c0, int c1) {
   using C = MmaCfg<D, NST>;
+  constexpr int TR = tile_rows<TILE>();
+  constexpr bool KEYS_ON_M = TILE != kTileM16;       // the narrow layouts
+  constexpr int NT = TILE == kTileN24 ? 3 : 1;       // n tiles of rows (narrow layouts)
+  constexpr int NL = 2 * NT;                         // query rows a thread holds
   const SplitParams &p = a.p;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int gid = lane >> 2, tig = lane & 3;
@@ -346,7 +463,7 @@ __device__ bool stream_chunk(const MmaArgs &a, unsigned char *smem, uint64_t *s_
   // refills last; they are read into registers before that buffer is refilled
   const uint32_t qtile = sbase + ((seq + NST - 1) % NST) * C::STAGE_BYTES;
   if (p.rope_cos == nullptr) {
-    for (int idx = tid; idx < kMmaRows * C::NCH; idx += kThreads) {
+    for (int idx = tid; idx < TR * C::NCH; idx += kThreads) {
       const int r = idx / C::NCH, ch = idx % C::NCH;
       const int gr = rb * p.R + r;
       const bool valid = r < p.R && gr < GT;
@@ -360,7 +477,7 @@ __device__ bool stream_chunk(const MmaArgs &a, unsigned char *smem, uint64_t *s_
     // fused step: query row (hq, t) rotated to its position L - T + t on the way in
     constexpr int NH = C::NCH / 2;
     unsigned char *qt = smem + ((seq + NST - 1) % NST) * C::STAGE_BYTES;
-    for (int idx = tid; idx < kMmaRows * NH; idx += kThreads) {
+    for (int idx = tid; idx < TR * NH; idx += kThreads) {
       const int r = idx / NH, ch = idx % NH;
       const int gr = rb * p.R + r;
       uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = lo;
@@ -382,23 +499,28 @@ __device__ bool stream_chunk(const MmaArgs &a, unsigned char *smem, uint64_t *s_
     for (int s2 = 0; s2 < min(NST - 1, nstages); ++s2) issue(s2);
   }
 
-  // keys visible to this thread's rows of the row block: gid and gid + 8 (m16 layout) or
-  // 2*tig and 2*tig + 1 (narrow layout)
-  int lim[2];
+  // keys visible to this thread's rows of the row block: gid and gid + 8 (m16 layout), or
+  // 8 nt + 2 tig and 8 nt + 2 tig + 1 of each n tile (narrow layouts)
+  int lim[NL];
 #pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const int r = NARROW ? 2 * tig + h : gid + 8 * h;
+  for (int h = 0; h < NL; ++h) {
+    const int r = KEYS_ON_M ? 8 * (h >> 1) + 2 * tig + (h & 1) : gid + 8 * h;
     const int gr = rb * p.R + r;
     const bool valid = r < p.R && gr < GT;
     lim[h] = valid ? min(max(L - p.T + gr % p.T + 1, 0), c1) : 0;
   }
-  // query rows as mma A fragments (narrow: B fragments), read once the first stage lands
-  uint32_t qa[C::KSD][NARROW ? 2 : 4];
-  constexpr int NO = NARROW ? C::KSD : C::NTD;  // output tiles
-  float o[NO][4];
+  // query rows as mma A fragments (narrow: B fragments of each n tile), read once the first
+  // stage lands
+  uint32_t qa[NT][C::KSD][KEYS_ON_M ? 2 : 4];
+  constexpr int NO = KEYS_ON_M ? C::KSD : C::NTD;  // output tiles per n tile
+  float o[NT][NO][4];
 #pragma unroll
-  for (int nt = 0; nt < NO; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
-  float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int i = 0; i < NO; ++i) o[nt][i][0] = o[nt][i][1] = o[nt][i][2] = o[nt][i][3] = 0.f;
+  float m_run[NL], l_run[NL];
+#pragma unroll
+  for (int h = 0; h < NL; ++h) m_run[h] = -INFINITY, l_run[h] = 0.f;
 
   int consumed = 0;
   bool ok = true;
@@ -427,21 +549,24 @@ __device__ bool stream_chunk(const MmaArgs &a, unsigned char *smem, uint64_t *s_
       break;
     }
     if (st == 0) {
-      if constexpr (NARROW) {
-        // rows 0..7: matrices of 16-byte chunks 4j .. 4j+3 are B words of k steps 2j, 2j+1
+      if constexpr (KEYS_ON_M) {
+        // rows 8 nt .. 8 nt + 7: matrices of 16-byte chunks 4j .. 4j+3 are B words of k steps
+        // 2j, 2j+1
 #pragma unroll
-        for (int j = 0; j < C::KSD / 2; ++j) {
-          uint32_t w[4];
-          ldmatrix_x4(w, qtile + swz<C::ROWB>(lane & 7, 4 * j + (lane >> 3)));
-          qa[2 * j][0] = w[0];
-          qa[2 * j][1] = w[1];
-          qa[2 * j + 1][0] = w[2];
-          qa[2 * j + 1][1] = w[3];
-        }
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int j = 0; j < C::KSD / 2; ++j) {
+            uint32_t w[4];
+            ldmatrix_x4(w, qtile + swz<C::ROWB>(8 * nt + (lane & 7), 4 * j + (lane >> 3)));
+            qa[nt][2 * j][0] = w[0];
+            qa[nt][2 * j][1] = w[1];
+            qa[nt][2 * j + 1][0] = w[2];
+            qa[nt][2 * j + 1][1] = w[3];
+          }
       } else {
 #pragma unroll
         for (int j = 0; j < C::KSD; ++j)
-          ldmatrix_x4(qa[j], qtile + swz<C::ROWB>(((lane >> 3) & 1) * 8 + (lane & 7), 2 * j + (lane >> 4)));
+          ldmatrix_x4(qa[0][j], qtile + swz<C::ROWB>(((lane >> 3) & 1) * 8 + (lane & 7), 2 * j + (lane >> 4)));
       }
       __syncthreads();  // every warp holds its query fragments before that buffer is refilled
     }
@@ -449,10 +574,12 @@ __device__ bool stream_chunk(const MmaArgs &a, unsigned char *smem, uint64_t *s_
     const int kr = warp * C::TKW;  // first key row (within the stage) of this warp's step
     const int key0 = j0 + kr;
     if (key0 < c1) {
-      if constexpr (NARROW)
-        warp_keys16_n8<D>(qa, kt, vt, kr, key0, lim, p.qscale, o, m_run, l_run);
+      if constexpr (TILE == kTileN24)
+        warp_keys16_n24<D>(qa, kt, vt, kr, key0, lim, p.qscale, o, m_run, l_run);
+      else if constexpr (TILE == kTileN8)
+        warp_keys16_n8<D>(qa[0], kt, vt, kr, key0, lim, p.qscale, o[0], m_run, l_run);
       else
-        warp_keys16<D>(qa, kt, vt, kr, key0, lim, p.qscale, o, m_run, l_run);
+        warp_keys16<D>(qa[0], kt, vt, kr, key0, lim, p.qscale, o[0], m_run, l_run);
     }
     consumed = st + 1;
   }
@@ -462,14 +589,14 @@ __device__ bool stream_chunk(const MmaArgs &a, unsigned char *smem, uint64_t *s_
     for (int st = consumed; st < issued; ++st)
       mbar_wait_bounded(smem_u32(&s_bars[(seq + st) % NST]), ((seq + st) / NST) & 1u);
     if (tid == 0) report(p.status, TD_DEV_WAIT_TIMEOUT);
-    m_run[0] = m_run[1] = -INFINITY;
-    l_run[0] = l_run[1] = 0.f;
+#pragma unroll
+    for (int h = 0; h < NL; ++h) m_run[h] = -INFINITY, l_run[h] = 0.f;
   }
   cp_async_wait<0>();
   seq += nstages;
 #pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    if constexpr (NARROW) {
+  for (int h = 0; h < NL; ++h) {
+    if constexpr (KEYS_ON_M) {
       l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 4);
       l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 8);
       l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 16);
@@ -479,26 +606,29 @@ __device__ bool stream_chunk(const MmaArgs &a, unsigned char *smem, uint64_t *s_
     }
   }
   __syncthreads();  // ring idle: reuse it as the combine area
+  constexpr int CAS = combine_stride<D>();
   float *combine = reinterpret_cast<float *>(smem);
   float *cm = combine;
-  float *cl = combine + kWarps * kMmaRows;
-  float *ca = combine + 2 * kWarps * kMmaRows;
-  if constexpr (NARROW) {
-    // rows 2*tig + e; rows 8..15 of the combine area are not used (at most 8 rows exist)
+  float *cl = combine + kWarps * TR;
+  float *ca = combine + 2 * kWarps * TR;
+  if constexpr (KEYS_ON_M) {
+    // rows 8 nt + 2 tig + e (the narrow n8 layout leaves rows 8..15 of its area unused)
 #pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      const int r = 2 * tig + e;
-      if (gid == 0) {
-        cm[warp * kMmaRows + r] = m_run[e];
-        cl[warp * kMmaRows + r] = l_run[e];
-      }
-      float *row = &ca[(warp * kMmaRows + r) * D];
+    for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-      for (int dt = 0; dt < C::KSD; ++dt) {
-        row[16 * dt + gid] = o[dt][e];
-        row[16 * dt + gid + 8] = o[dt][2 + e];
+      for (int e = 0; e < 2; ++e) {
+        const int r = 8 * nt + 2 * tig + e;
+        if (gid == 0) {
+          cm[warp * TR + r] = m_run[2 * nt + e];
+          cl[warp * TR + r] = l_run[2 * nt + e];
+        }
+        float *row = &ca[(warp * TR + r) * CAS];
+#pragma unroll
+        for (int dt = 0; dt < C::KSD; ++dt) {
+          row[16 * dt + gid] = o[nt][dt][e];
+          row[16 * dt + gid + 8] = o[nt][dt][2 + e];
+        }
       }
-    }
     __syncthreads();
     return ok;
   }
@@ -506,13 +636,13 @@ __device__ bool stream_chunk(const MmaArgs &a, unsigned char *smem, uint64_t *s_
   for (int h = 0; h < 2; ++h) {
     const int r = gid + 8 * h;
     if (tig == 0) {
-      cm[warp * kMmaRows + r] = m_run[h];
-      cl[warp * kMmaRows + r] = l_run[h];
+      cm[warp * TR + r] = m_run[h];
+      cl[warp * TR + r] = l_run[h];
     }
 #pragma unroll
     for (int nt = 0; nt < C::NTD; ++nt) {
-      float2 v = make_float2(o[nt][2 * h], o[nt][2 * h + 1]);
-      *reinterpret_cast<float2 *>(&ca[(warp * kMmaRows + r) * D + nt * 8 + 2 * tig]) = v;
+      float2 v = make_float2(o[0][nt][2 * h], o[0][nt][2 * h + 1]);
+      *reinterpret_cast<float2 *>(&ca[(warp * TR + r) * CAS + nt * 8 + 2 * tig]) = v;
     }
   }
   __syncthreads();
@@ -553,8 +683,10 @@ __device__ void prefetch_chunk_l2(const SplitParams &p, int b, int kvh, int c0, 
 // check, and an L2 prefetch of that chunk's first `n` stages, so the HBM latency of the
 // first stages overlaps the previous kernel's tail. A hint only: a wrong guess wastes a
 // prefetch, and the real plan is made after the wait. Batches of up to 8 sequences.
+// `item` is the CTA's first work item; a cluster of `parts` CTAs shares each item, this CTA
+// taking run `part` of its whole 64-key stages (as split_attn_cc_kernel cuts it).
 template <int D, bool Q8 = false>
-__device__ void prefetch_first_item(const SplitParams &p, int n) {
+__device__ void prefetch_first_item(const SplitParams &p, int n, int item, int part = 0, int parts = 1) {
   if (p.B > 8) return;
   long long all = 0;
   int longest = 0, first = 0;
@@ -567,15 +699,16 @@ __device__ void prefetch_first_item(const SplitParams &p, int n) {
   }
   const int S = first_chunk_size(p, all, longest);
   const int U = p.Hkv * p.RB;
-  int item = blockIdx.x;
   for (int b = 0; b < p.B; ++b) {
     // (a second read of the later lengths: still a guess)
     const int L = b == 0 ? first : attended_len(p, ld_relaxed(p.seq_lens + b), bits);
     const int NC = (L + S - 1) / S;
     if (item < NC * U) {
       const int c = item % NC, kvh = item / NC / p.RB;
-      const int c0 = c * S;
-      prefetch_chunk_l2<D, Q8>(p, b, kvh, c0, min(c0 + S, L), n);
+      const int c0 = c * S, c1 = min(c0 + S, L);
+      const int per = ((c1 - c0 + parts - 1) / parts + 63) / 64 * 64;
+      const int r0 = min(c0 + part * per, c1);
+      prefetch_chunk_l2<D, Q8>(p, b, kvh, r0, min(r0 + per, c1), n);
       return;
     }
     item -= NC * U;
@@ -593,14 +726,15 @@ __device__ __forceinline__ unsigned char *align1024(unsigned char *p) {
 // EARLY_PLAN (launched when one row block covers a kv head, i.e. decode): the plan is made
 // on the lengths as they read before the wait for the previous kernel and kept after it if
 // they read the same then (measured on the 3B-style layer: 4k 11.4 -> 10.5 us, 32k 25.7 ->
-// 25.5 us). The other instantiation plans after the wait. NARROW (a kv head's rows fit 8):
-// the warps step with warp_keys16_n8.
-template <int D, bool EARLY_PLAN, bool NARROW = false>
+// 25.5 us). The other instantiation plans after the wait. TILE: the warps' step for the row
+// block's rows (tile_of_rows).
+template <int D, bool EARLY_PLAN, int TILE = kTileM16>
 __global__ void __launch_bounds__(kThreads, 2) split_attn_mma_kernel(const __grid_constant__ MmaArgs a) {
   constexpr int NST = kPersistentStages<D>;
   using C = MmaCfg<D, NST>;
   using E = __nv_bfloat16;
-  static_assert((merge_fixed_floats<D, kMmaRows>() + part_block_floats(kMmaRows, D)) * 4 <= C::RING_BYTES,
+  constexpr int TR = tile_rows<TILE>();
+  static_assert((merge_fixed_floats<D, TR>() + part_block_floats(TR, D)) * 4 <= C::RING_BYTES,
                 "merge stages at least one chunk");
   const SplitParams &p = a.p;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -622,7 +756,7 @@ __global__ void __launch_bounds__(kThreads, 2) split_attn_mma_kernel(const __gri
   }
   uint32_t merge_phase = 0;
   uint32_t seq = 0;
-  if (tid == 0) prefetch_first_item<D>(p, prefetch_stages(p));
+  if (tid == 0) prefetch_first_item<D>(p, prefetch_stages(p), blockIdx.x);
   if constexpr (EARLY_PLAN) plan_items(p, s_len, s_prefix, &s_chunk, s_red, false);
   griddep_wait();  // inputs may come from the previous kernel in the stream
   griddep_launch_dependents();
@@ -634,6 +768,11 @@ __global__ void __launch_bounds__(kThreads, 2) split_attn_mma_kernel(const __gri
   const int S = s_chunk;
   const int W = s_prefix[p.B];
   const int rows = p.Hq * p.T;
+  if (p.deferred && blockIdx.x == 0) {
+    // the plan the deferred merge kernel follows
+    for (int b = tid; b < p.B; b += kThreads) p.plan_out[1 + b] = s_len[b];
+    if (tid == 0) p.plan_out[0] = S;
+  }
 
   // sequences with no key get no item: their rows are 0 with lse = -inf
   for (int b = blockIdx.x; b < p.B; b += gridDim.x) {
@@ -659,9 +798,9 @@ __global__ void __launch_bounds__(kThreads, 2) split_attn_mma_kernel(const __gri
     const int rb = rest % p.RB;
     const int kvh = rest / p.RB;
     const int c0 = c * S;
-    const bool ok = stream_chunk<D, NST, NARROW>(a, smem, s_bars, seq, b, kvh, rb, L, c0, min(c0 + S, L));
-    finish_item<E, D, kMmaRows, kWarps>(p, combine, C::RING_BYTES / 4, &s_merge_bar, merge_phase, b, kvh, rb, c, NC,
-                                        &s_last);
+    const bool ok = stream_chunk<D, NST, TILE>(a, smem, s_bars, seq, b, kvh, rb, L, c0, min(c0 + S, L));
+    finish_item<E, D, TR, kWarps, combine_stride<D>()>(p, combine, C::RING_BYTES / 4, &s_merge_bar, merge_phase, b, kvh,
+                                                       rb, c, NC, &s_last);
     // the combine and merge wrote the ring through the generic proxy; the next item's first
     // stages refill it through the asynchronous proxy
     fence_proxy_async_smem();
@@ -670,30 +809,30 @@ __global__ void __launch_bounds__(kThreads, 2) split_attn_mma_kernel(const __gri
   }
 }
 
-// Combines the kWarps partial sources left by stream_chunk (base-2 units) into one partial
-// block at `dst` (generic address, possibly another CTA's shared memory): acc[R][D], then
-// m[R] (natural-log units) and l[R], for rows r < nv.
-template <int D>
+// Combines the kWarps partial sources left by stream_chunk (base-2 units, TR rows per warp)
+// into one partial block at `dst` (generic address, possibly another CTA's shared memory):
+// acc[R][D], then m[R] (natural-log units) and l[R], for rows r < nv.
+template <int D, int TR>
 __device__ void combine_block(const float *combine, float *dst, int R, int nv) {
-  constexpr int D4 = D / 4;
+  constexpr int D4 = D / 4, CAS = combine_stride<D>();
   const float *cm = combine;
-  const float *cl = combine + kWarps * kMmaRows;
-  const float *ca = combine + 2 * kWarps * kMmaRows;
+  const float *cl = combine + kWarps * TR;
+  const float *ca = combine + 2 * kWarps * TR;
   for (int idx = threadIdx.x; idx < nv * D4; idx += kThreads) {
     const int r = idx / D4, d = (idx % D4) * 4;
     float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, cm[w * kMmaRows + r]);
+    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, cm[w * TR + r]);
     float Ls = 0.f;
     float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
     if (M != -INFINITY) {
 #pragma unroll
       for (int w = 0; w < kWarps; ++w) {
-        const float mw = cm[w * kMmaRows + r];
+        const float mw = cm[w * TR + r];
         if (mw != -INFINITY) {
           const float f = exp2f(mw - M);
-          Ls = fmaf(cl[w * kMmaRows + r], f, Ls);
-          const float4 v = *reinterpret_cast<const float4 *>(ca + (w * kMmaRows + r) * D + d);
+          Ls = fmaf(cl[w * TR + r], f, Ls);
+          const float4 v = *reinterpret_cast<const float4 *>(ca + (w * TR + r) * CAS + d);
           A.x = fmaf(v.x, f, A.x), A.y = fmaf(v.y, f, A.y), A.z = fmaf(v.z, f, A.z), A.w = fmaf(v.w, f, A.w);
         }
       }

@@ -543,7 +543,7 @@ __global__ void __launch_bounds__(kThreads, 2) split_attn_q8_kernel(const __grid
   }
   uint32_t merge_phase = 0;
   uint32_t seq = 0;
-  if (tid == 0) prefetch_first_item<D, true>(p, prefetch_stages(p));
+  if (tid == 0) prefetch_first_item<D, true>(p, prefetch_stages(p), blockIdx.x);
   // EARLY_PLAN: planned before the wait and kept when the lengths read the same after it,
   // as the bf16 decode kernel does. With the slots left free for the previous call's merging
   // CTAs this measured 4k 9.06 -> 8.07 us, 16k 13.05 -> 12.13, 32k 16.78 -> 15.95

@@ -202,8 +202,8 @@ CLUSTER = [
     (128, 24, 8, 300, 1, [65, 1, 0, 300, 299, 128, 64, 3]),    # 64 groups: clusters of 4
     (64, 64, 8, 1000, 1, [1000, 999, 500, 17, 1, 0, 640, 64]),  # 8 heads per kv head
     (64, 32, 8, 700, 1, [700] * 12 + [1, 0, 333, 64]),         # 128 groups: clusters of 2
-    (128, 32, 8, 700, 6, [690, 100]),                          # verify: 24 rows in two row blocks
-    (128, 32, 8, 64, 6, [64, 3]),                              # verify with a short sequence
+    (128, 32, 8, 700, 6, [690, 100, 350, 7]),                  # verify: 24 rows on the 24-row tile
+    (128, 32, 8, 64, 6, [64, 3, 60, 6]),                       # verify with short sequences
     (128, 24, 8, 1000, 1, [1000, 1000, 999, 1000]),            # Smax not a stage multiple
 ]
 
@@ -221,6 +221,44 @@ def test_cluster_kernel_against_oracle_and_persistent(td, D, Hq, Hkv, Smax, T, l
     assert td.td_split_plan(torch.bfloat16, B, Hq, Hkv, Smax, D, T, 128)["kernel"] == "tensor_core_persistent"
     out_p, lse_p = check_case(td, case, split=128)
     assert_out_close(out_c, out_p.double().numpy(), "bf16", what="cluster vs persistent")
+
+
+# ------------------------------------------------------------- 24-row tile, deferred merge
+
+DEFERRED = [
+    # D, Hq, Hkv, Smax, T, lengths, split: row blocks of 17 to 24 rows on the 24-row tile, whose
+    # chunks are merged by the second kernel, one CTA per slice of 4 rows
+    (128, 32, 8, 2000, 6, [1990], 0),          # verify: 24 rows, 6 slices
+    (128, 16, 4, 700, 6, [690, 100], 0),       # verify, two sequences
+    (128, 16, 4, 300, 6, [300, 6, 0], 0),      # a chunk of exactly T keys and an empty sequence
+    (128, 160, 8, 900, 1, [900], 0),           # 20 rows: decode on the 24-row tile
+    (64, 36, 2, 1000, 1, [1000, 999], 0),      # 18 rows at D = 64: a ragged last slice
+    (128, 32, 8, 2000, 6, [1990], 16),         # 125 chunks: the merge stages them in rounds
+    (128, 32, 8, 600, 6, [600, 33], 37),       # a 37-key split: ragged stages in every chunk
+    (128, 40, 4, 500, 2, [500], 0),            # 20 rows from 10 heads x 2 tokens
+]
+
+
+@pytest.mark.parametrize("D,Hq,Hkv,Smax,T,lens,split", DEFERRED)
+def test_deferred_merge_against_oracle(td, D, Hq, Hkv, Smax, T, lens, split):
+    B = len(lens)
+    plan = td.td_split_plan(torch.bfloat16, B, Hq, Hkv, Smax, D, T, split)
+    assert plan["kernel"] == "tensor_core_persistent" and 16 < plan["rows"] <= 24, plan
+    case = small_case(dtype="bf16", B=B, Hq=Hq, Hkv=Hkv, D=D, Smax=Smax, T=T, seq_lens=lens, seed=Smax + Hq + T,
+                      heavy=0.02)
+    check_case(td, case, split=split)
+
+
+def test_deferred_merge_repeat_calls_bit_identical(td):
+    case = small_case(dtype="bf16", B=1, Hq=32, Hkv=8, D=128, Smax=5000, T=6, seq_lens=[5000], seed=21)
+    q, k, v, sl = case.q.cuda(), case.k_cache.cuda(), case.v_cache.cuda(), case.seq_lens.cuda()
+    ws = td.make_workspace(1, 32, 8, 5000, 128, 6, 0)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    o1 = td.td_verify_attn(q, k, v, sl, case.scale, 0, workspace=ws, dev_status=st)
+    o2 = td.td_verify_attn(q, k, v, sl, case.scale, 0, workspace=ws, dev_status=st)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and int(st.item()) == 0
+    assert int(ws[:4 * 8].view(torch.int32).abs().sum()) == 0
 
 
 def test_automatic_split_fills_one_wave(td):

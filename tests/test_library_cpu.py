@@ -124,10 +124,13 @@ def test_hot_kernels_have_no_spills(lib):
     log = open(td_build.PTXAS_LOG).read()
     entries = re.findall(r"Compiling entry function '(\w+)'.*?\n(?:.*?\n)*?\s+(\d+) bytes stack frame, (\d+) bytes "
                          r"spill stores, (\d+) bytes spill loads", log)
-    hot = {"split_attn_mma_kernelILi128ELb1ELb1E", "split_attn_mma_kernelILi128ELb1ELb0E",
-           "split_attn_mma_kernelILi128ELb0ELb0E", "split_attn_mma_kernelILi64ELb1ELb1E",
-           "split_attn_mma_kernelILi64ELb1ELb0E", "split_attn_mma_kernelILi64ELb0ELb0E", "split_attn_kernelIfLi64ELi2E",
-           "split_attn_cluster_kernelILi128ELb0E", "split_attn_cluster_kernelILi128ELb1E", "split_attn_q8_kernelILi128ELb0ELb0E",
+    hot = {"split_attn_mma_kernelILi128ELb1ELi1E", "split_attn_mma_kernelILi128ELb1ELi0E",
+           "split_attn_mma_kernelILi128ELb0ELi2E", "split_attn_mma_kernelILi128ELb0ELi0E",
+           "split_attn_mma_kernelILi64ELb1ELi1E", "split_attn_mma_kernelILi64ELb1ELi0E",
+           "split_attn_mma_kernelILi64ELb0ELi0E", "split_attn_kernelIfLi64ELi2E",
+           "merge_slices_kernelI13__nv_bfloat16Li128E",
+           "split_attn_cluster_kernelILi128ELi0E", "split_attn_cluster_kernelILi128ELi1E",
+           "split_attn_cluster_kernelILi128ELi2E", "split_attn_q8_kernelILi128ELb0ELb0E",
            "split_attn_q8_kernelILi128ELb1ELb0E", "split_attn_q8_kernelILi128ELb1ELb1E",
            "prefill_kernelILi128E"}
     seen = set()
