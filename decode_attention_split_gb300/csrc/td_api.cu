@@ -71,8 +71,6 @@ td_status prepare(td_dtype dtype, const void *q, const void *k_cache, const void
   p->warm_stages = plan->warm;
   p->qscale = scale * td::kLog2e;
   p->done = p->counters + plan->counters_n;
-  p->deferred = plan->deferred ? 1 : 0;
-  p->plan_out = p->counters + plan->counters_n + 1;
   return TD_OK;
 }
 

@@ -109,6 +109,13 @@ __device__ __forceinline__ int32_t ld_relaxed(const int32_t *p) {
   return v;
 }
 
+// A load with acquire semantics at GPU scope (a completion counter other CTAs release to).
+__device__ __forceinline__ int32_t ld_acquire(const int32_t *p) {
+  int32_t v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
 // One bulk copy global -> shared through the TMA engine; completion is counted on `bar`
 // in bytes. dst, src and bytes must be multiples of 16.
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar,

@@ -25,9 +25,7 @@ struct SplitPlan {
   int min_chunk; // smallest automatic chunk (keys)
   int warm;      // 64-row units of K and V each CTA warms in L2 before the wait for the previous kernel
   int cluster;   // 0: persistent kernel; else CTAs per cluster of the cluster kernel (grid = groups x cluster)
-  int counters_n;  // completion counters before the fused step's read count in the workspace
-  bool deferred;   // row blocks of more than 16 rows: chunk partials merged by merge_slices_kernel, launched
-                   // after the split kernel (the workspace then also records the plan, after the read count)
+  int counters_n;  // completion and slice-merge counters before the fused step's read count in the workspace
   bool q8;       // int8 cache (codes + per-row scales): the quantised-cache kernel
   size_t off_part, bytes;  // workspace layout: counters, then partial blocks
 };

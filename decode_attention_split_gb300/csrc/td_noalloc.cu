@@ -103,8 +103,6 @@ extern "C" td_status td_decode_attn_noalloc(td_dtype dtype, const void *q, const
   p.warm_stages = plan.warm;
   p.qscale = scale * td::kLog2e;
   p.done = p.counters + plan.counters_n;
-  p.deferred = plan.deferred ? 1 : 0;
-  p.plan_out = p.counters + plan.counters_n + 1;
   const cudaError_t e = td::launch_split(dtype, D, plan, p, s);
   return e == cudaSuccess ? TD_OK : td::cuda_fail(e);
 }

@@ -346,33 +346,6 @@ static int device_l2_bytes(int device) {
   return n;
 }
 
-// Shared memory of merge_slices_kernel: the staging of up to 46 chunks' slices of 4 rows at D = 128.
-constexpr int kMergeSlicesSmem = 100 * 1024;
-
-template <int D>
-cudaError_t launch_merge_slices_d(const SplitParams &p, cudaStream_t stream) {
-  static std::mutex mu;
-  static bool done[kMaxDevices] = {};
-  int device = 0;
-  if (cudaGetDevice(&device) != cudaSuccess || device < 0 || device >= kMaxDevices) return cudaErrorInvalidDevice;
-  {
-    std::lock_guard<std::mutex> lock(mu);
-    if (!done[device]) {
-      const cudaError_t e = cudaFuncSetAttribute(merge_slices_kernel<__nv_bfloat16, D>,
-                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kMergeSlicesSmem);
-      if (e != cudaSuccess) return e;
-      done[device] = true;
-    }
-  }
-  const int grid = p.B * p.Hkv * p.RB * ((p.R + kSliceRows - 1) / kSliceRows);
-  return launch_pdl(merge_slices_kernel<__nv_bfloat16, D>, dim3(grid), dim3(kThreads), kMergeSlicesSmem, stream, p,
-                    kMergeSlicesSmem / 4);
-}
-
-cudaError_t launch_merge_slices(int D, const SplitParams &p, cudaStream_t stream) {
-  return D == 64 ? launch_merge_slices_d<64>(p, stream) : launch_merge_slices_d<128>(p, stream);
-}
-
 td_status plan_split(td_dtype dtype, int B, int Hq, int Hkv, int T, int Smax, int D, int split, SplitPlan *plan,
                      bool q8) {
   if (dtype != TD_F32 && dtype != TD_BF16) return TD_ERR_UNSUPPORTED;
@@ -477,17 +450,12 @@ td_status plan_split(td_dtype dtype, int B, int Hq, int Hkv, int T, int Smax, in
     const long long warm = RB == 1 ? (l2 * 9 / 10) / ((long long)plan->grid * unit) : 4;
     plan->warm = (int)(warm < 1 ? 1 : warm > 16 ? 16 : warm);
   }
-  // the persistent kernel's merge for row blocks of more than 16 rows runs as a second kernel,
-  // one CTA per slice of kSliceRows rows of each group: one CTA staging every chunk's 24 rows
-  // (a verify block of four grouped heads x 6 tokens) took 28 us where the chunks streamed in 7
-  plan->deferred = mma && !q8 && plan->cluster == 0 && R > 16;
-  // completion counters, one per (b, kv head, row block), then the fused step's read count,
-  // then the deferred merge's plan (chunk size, attended lengths)
-  plan->counters_n = (int)((long long)B * U);
-  const size_t counters = align256(((size_t)plan->counters_n + 2 + B) * sizeof(int));
+  // completion counters, one per (b, kv head, row block), then as many counts of finished
+  // slice merges, then the fused step's read count
+  plan->counters_n = (int)(2LL * B * U);
+  const size_t counters = align256(((size_t)plan->counters_n + 1) * sizeof(int));
   plan->off_part = counters;
-  const size_t block = (size_t)std::max(part_block_floats(R, D), R * merge_row_floats(D));
-  plan->bytes = plan->off_part + align256((size_t)B * U * ns * block * sizeof(float));
+  plan->bytes = plan->off_part + align256((size_t)B * U * ns * part_block_floats(R, D) * sizeof(float));
   return TD_OK;
 }
 
@@ -504,7 +472,6 @@ cudaError_t launch_split(td_dtype dtype, int D, const SplitPlan &plan, const Spl
     if (k.fn == nullptr) return cudaErrorInvalidValue;
     e = k.launch(p, plan.grid, plan.smem, stream);
   }
-  if (e == cudaSuccess && plan.deferred) e = launch_merge_slices(D, p, stream);
   if (e != cudaSuccess) {
     cudaGetLastError();  // clear a launch error so it is reported once, by this call
     return e;

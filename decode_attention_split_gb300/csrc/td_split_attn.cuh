@@ -42,8 +42,8 @@ struct SplitParams {
   const int32_t *seq_lens;
   void *out;            // [B, Hq, T, D]
   float *lse;           // [B, Hq, T] or null
-  float *ws_part;       // [B, Hkv, RB][ns_ws] partial blocks (see part_block_floats)
-  int *counters;        // [B, Hkv, RB]
+  float *ws_part;       // [B, Hkv, RB][ns_ws] partial blocks of R rows (see part_row_floats)
+  int *counters;        // [B, Hkv, RB] completion tickets, then [B, Hkv, RB] finished slice merges
   uint32_t *status;
   int B, Hq, Hkv, G, T, Smax;
   int R;                // query rows per CTA (<= RP)
@@ -54,12 +54,6 @@ struct SplitParams {
   int min_chunk;        // smallest automatic chunk (keys)
   int warm_stages;      // 64-row units of its first chunk each CTA warms in L2 before the wait
   float qscale;         // scale * log2(e)
-  // Deferred merge (row blocks of more than 16 rows): chunk partials are published in the
-  // row-major layout (merge_row_floats) without a completion ticket, and merge_slices_kernel,
-  // launched next in the stream, merges them; the split kernel's CTA 0 records the chunk size
-  // and the attended lengths for it in `plan_out` ([0] chunk size, [1 + b] attended length).
-  int deferred;
-  int *plan_out;
   // Fused step (tensor-core kernels only; k_new == null for plain attention): the T new rows
   // of each (b, kv head) go to cache rows seq_lens[b] .. seq_lens[b]+T-1 in this launch, the
   // query and key rows rotated there first when rope tables are given, and every query row
@@ -91,14 +85,11 @@ __device__ __forceinline__ int attended_len(const SplitParams &p, int32_t raw, u
   return L;
 }
 
-// A chunk's partial result for its row block: acc[R][D] (unnormalised p @ V sums), then
-// m[R] (base-2 units) and l[R]; padded to whole 16-byte units so blocks can be
-// bulk-copied and every acc row is 16-byte aligned.
-__host__ __device__ constexpr int part_block_floats(int R, int D) { return (R * (D + 2) + 3) / 4 * 4; }
-
-// Deferred merge: a chunk's partial is R rows of acc[D], m (base 2), l, padded to 16 bytes, so
-// a run of rows of one chunk is contiguous.
-__host__ __device__ constexpr int merge_row_floats(int D) { return D + 4; }
+// A chunk's partial result for its row block is R rows of part_row_floats(D) floats: acc[D]
+// (unnormalised p @ V sums), m (base-2 units) and l, padded to 16 bytes, so a block and any
+// run of its rows can be bulk-copied and every acc row is 16-byte aligned.
+__host__ __device__ constexpr int part_row_floats(int D) { return D + 4; }
+__host__ __device__ constexpr int part_block_floats(int R, int D) { return R * part_row_floats(D); }
 
 
 template <typename E, int D, int RP>
@@ -302,7 +293,7 @@ template <typename E, int D, int ROWS>
 __device__ void merge_group(const SplitParams &p, float *smem_f, int smem_floats, uint64_t *bar, uint32_t &phase,
                             int b, int kvh, int rb, int NC, int nv) {
   constexpr int kFB = 64;  // most chunks staged at a time
-  constexpr int D4 = D / 4;
+  constexpr int D4 = D / 4, RF = part_row_floats(D);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int R = p.R;
   const int BF = part_block_floats(R, D);
@@ -340,8 +331,8 @@ __device__ void merge_group(const SplitParams &p, float *smem_f, int smem_floats
 #pragma unroll
       for (int k = 0; k < 2; ++k) {
         const int c = lane + 32 * k;
-        lv[k] = c < nb ? stage[c * BF + R * D + R + r] : 0.f;
-        mv[k] = lv[k] > 0.f ? stage[c * BF + R * D + r] : -INFINITY;
+        lv[k] = c < nb ? stage[c * BF + r * RF + D + 1] : 0.f;
+        mv[k] = lv[k] > 0.f ? stage[c * BF + r * RF + D] : -INFINITY;
       }
       float bm = fmaxf(mv[0], mv[1]);
 #pragma unroll
@@ -374,7 +365,7 @@ __device__ void merge_group(const SplitParams &p, float *smem_f, int smem_floats
 #pragma unroll 1
     for (int idx = tid; idx < nv * D4; idx += kThreads) {
       const int r = idx / D4, d = (idx % D4) * 4;
-      const float *a = stage + r * D + d;
+      const float *a = stage + r * RF + d;
       const float *f = fac + r * kFB;
       float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
       if (c0 > 0) {
@@ -403,164 +394,121 @@ __device__ void merge_group(const SplitParams &p, float *smem_f, int smem_floats
   }
 }
 
-// Rows of a slice of the deferred merge (one CTA of merge_slices_kernel each).
-constexpr int kSliceRows = 2;
-
-// Deferred merge of rows [s0, s1) of group (b, kv head, row block rb) over its NC chunk
-// partials in the row-major layout (merge_row_floats), staged from L2 by bulk asynchronous
-// copies (one contiguous run of rows per chunk), as many chunks at a time as `smem_floats`
-// holds, and merged online as merge_group does. Writes out and lse.
-template <typename E, int D>
-__device__ void merge_row_slice(const SplitParams &p, float *smem_f, int smem_floats, uint64_t *bar, uint32_t &phase,
-                                int b, int kvh, int rb, int NC, int s0, int s1) {
-  constexpr int RF = merge_row_floats(D), D4 = D / 4, kFB = 64;
-  static_assert(D4 % 8 == 0, "whole warps per pass of the weighted sums");
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int ns = s1 - s0;
-  const long long g = ((long long)b * p.Hkv + kvh) * p.RB + rb;
-  const float *src = p.ws_part + (g * p.ns_ws * p.R + s0) * (long long)RF;  // chunk c at + c * R * RF
-  float *acc = smem_f;            // [ns][D] running weighted sums (between rounds)
-  float *st = acc + ns * D;       // M[ns], Lsum[ns], rescale[ns], 1 / Lsum[ns]
-  float *fac = st + 4 * ns;       // [ns][kFB] factors 2^(m_c - M) of the staged chunks
-  float *stage = fac + ns * kFB;  // [FB][ns][RF], 16-byte aligned: ns * (D + 68) floats before it
-  int FB = (smem_floats - ns * (D + 4 + kFB)) / (ns * RF);
-  if (FB > kFB) FB = kFB;
-  if (tid < ns) {
-    st[tid] = -INFINITY;
-    st[ns + tid] = 0.f;
+// Waits, bounded, until the completion counter at `cnt` reads at least `target` (acquire:
+// the partials released before those tickets are visible after it). Thread 0 polls; the CTA
+// takes one decision. False if the count never arrived (TD_DEV_WAIT_TIMEOUT is set).
+__device__ __forceinline__ bool wait_count(const SplitParams &p, const int *cnt, int target) {
+  __shared__ int s_ok;
+  if (threadIdx.x == 0) {
+    int ok = 1;
+    if (ld_acquire(cnt) < target) {
+      const long long t0 = clock64();
+      while (ld_acquire(cnt) < target) {
+        if (clock64() - t0 > kWaitLimitCycles) {
+          ok = 0;
+          report(p.status, TD_DEV_WAIT_TIMEOUT);
+          break;
+        }
+        __nanosleep(64);
+      }
+    }
+    s_ok = ok;
   }
-#pragma unroll 1
-  for (int c0 = 0; c0 < NC; c0 += FB) {
-    const int nb = min(FB, NC - c0);
-    const bool last = c0 + nb >= NC;
-    if (tid == 0) {
-      fence_proxy_async_global();
-      mbar_arrive_expect_tx(smem_u32(bar), (uint32_t)(nb * ns * RF * 4));
-      for (int c = 0; c < nb; ++c)
-        bulk_g2s_plain(smem_u32(stage + c * ns * RF), src + (long long)(c0 + c) * p.R * RF, (uint32_t)(ns * RF * 4),
-                       smem_u32(bar));
-    }
-    if (!mbar_wait_bounded(smem_u32(bar), phase)) {
-      report(p.status, TD_DEV_WAIT_TIMEOUT);
-      mbar_wait_bounded(smem_u32(bar), phase);  // one more bounded wait for the copies in flight
-    }
-    phase ^= 1u;
-    __syncthreads();  // staged runs and the previous round's statistics are visible
-    // per-row statistics of this round (base 2): a warp per row, lanes over chunks
-#pragma unroll 1
-    for (int r = warp; r < ns; r += kWarps) {
-      float mv[2], lv[2];
-#pragma unroll
-      for (int k = 0; k < 2; ++k) {
-        const int c = lane + 32 * k;
-        lv[k] = c < nb ? stage[(c * ns + r) * RF + D + 1] : 0.f;
-        mv[k] = lv[k] > 0.f ? stage[(c * ns + r) * RF + D] : -INFINITY;
-      }
-      float bm = fmaxf(mv[0], mv[1]);
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, o));
-      const float Mo = st[r];
-      const float Mn = fmaxf(Mo, bm);
-      const float base = Mn == -INFINITY ? 0.f : Mn;
-      float ls = 0.f;
-#pragma unroll
-      for (int k = 0; k < 2; ++k) {
-        const float f = lv[k] > 0.f ? exp2f(mv[k] - base) : 0.f;
-        if (lane + 32 * k < nb) fac[r * kFB + lane + 32 * k] = f;
-        ls = fmaf(lv[k], f, ls);
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) ls += __shfl_xor_sync(0xffffffffu, ls, o);
-      if (lane == 0) {
-        const float alpha = exp2f(Mo - base);
-        const float Ls = st[ns + r] * alpha + ls;
-        st[r] = Mn;
-        st[ns + r] = Ls;
-        st[2 * ns + r] = alpha;
-        st[3 * ns + r] = Ls > 0.f ? 1.f / Ls : 0.f;
-        if (last && p.lse != nullptr)
-          p.lse[out_row_of(p, b, kvh, rb, s0 + r)] = Ls > 0.f ? (Mn + log2f(Ls)) * kLn2 : -INFINITY;
-      }
-    }
-    __syncthreads();
-    // weighted sums: four lanes per (row, four dims), each over every fourth staged chunk,
-    // summed by shuffles; in the last round they are the output
-#pragma unroll 1
-    for (int idx = tid; idx < ns * D4 * 4; idx += kThreads) {
-      const int q = idx & 3, pr = idx >> 2;
-      const int r = pr / D4, d = (pr % D4) * 4;
-      const float *a = stage + r * RF + d;
-      const float *f = fac + r * kFB;
-      float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-      for (int c = q; c < nb; c += 4) {
-        const float4 v = *reinterpret_cast<const float4 *>(a + c * ns * RF);
-        const float w = f[c];
-        x.x = fmaf(v.x, w, x.x), x.y = fmaf(v.y, w, x.y), x.z = fmaf(v.z, w, x.z), x.w = fmaf(v.w, w, x.w);
-      }
-#pragma unroll
-      for (int o = 1; o < 4; o <<= 1) {
-        x.x += __shfl_xor_sync(0xffffffffu, x.x, o);
-        x.y += __shfl_xor_sync(0xffffffffu, x.y, o);
-        x.z += __shfl_xor_sync(0xffffffffu, x.z, o);
-        x.w += __shfl_xor_sync(0xffffffffu, x.w, o);
-      }
-      if (q != 0) continue;
-      if (c0 > 0) {
-        const float sc = st[2 * ns + r];
-        const float4 y = *reinterpret_cast<const float4 *>(acc + r * D + d);
-        x.x = fmaf(y.x, sc, x.x), x.y = fmaf(y.y, sc, x.y), x.z = fmaf(y.z, sc, x.z), x.w = fmaf(y.w, sc, x.w);
-      }
-      if (last) {
-        const float inv = st[3 * ns + r];
-        E *o = static_cast<E *>(p.out) + out_row_of(p, b, kvh, rb, s0 + r) * D + d;
-        store_elem<E>(o + 0, x.x * inv);
-        store_elem<E>(o + 1, x.y * inv);
-        store_elem<E>(o + 2, x.z * inv);
-        store_elem<E>(o + 3, x.w * inv);
-      } else {
-        *reinterpret_cast<float4 *>(acc + r * D + d) = x;
-      }
-    }
-    __syncthreads();  // the next round overwrites the staging area
-  }
+  __syncthreads();
+  return s_ok != 0;
 }
 
-// Deferred merge ("tinydecode" and "llm-decode-cuda": the chunks' partials merged by
-// log-sum-exp in a second step): one CTA per (b, kv head, row block, slice of kSliceRows
-// rows), launched right after a split kernel with p.deferred set and scheduled while it drains
-// (programmatic dependent launch). The split kernel's CTA 0 recorded the chunk size and every
-// sequence's attended length in p.plan_out; sequences of one chunk were written out by the
-// split kernel itself. For row blocks of more than 16 rows (a 24-row verify block of four
-// grouped heads) the merge of every chunk's rows then runs in parallel across the row slices,
-// where one CTA per group would stage every chunk's 24 rows by itself.
+// Merges rows [s0, s1) (at most kThreads / (D / 4) of them) of group (b, kv head, row block rb)
+// over its NC published partials with direct loads from L2. The threads are (row, column of
+// four dims) pairs times CG = kThreads / (rows * D/4) groups of chunks; group j folds chunks
+// j, j + CG, ... into a running (M, L, sums) in base 2, kBatch chunks' loads in flight at once,
+// and the groups are combined in shared memory `sm` (6 * kThreads floats). Writes out and lse.
 template <typename E, int D>
-__global__ void __launch_bounds__(kThreads) merge_slices_kernel(const SplitParams p, int smem_floats) {
-  extern __shared__ __align__(16) float msm[];
-  __shared__ __align__(8) uint64_t bar;
+__device__ void merge_rows_direct(const SplitParams &p, float *sm, int b, int kvh, int rb, int NC, int s0, int s1) {
+  constexpr int D4 = D / 4, RF = part_row_floats(D), kBatch = 8;
+  const int nr = s1 - s0;
+  const int cols = nr * D4;
+  const int CG = kThreads / cols;
   const int tid = threadIdx.x;
-  const int nsl = (p.R + kSliceRows - 1) / kSliceRows;
-  const int sl = blockIdx.x % nsl;
-  const int g = blockIdx.x / nsl;
-  const int rb = g % p.RB;
-  const int kvh = (g / p.RB) % p.Hkv;
-  const int b = g / (p.RB * p.Hkv);
-  if (tid == 0) {
-    mbar_init(smem_u32(&bar), 1);
-    fence_mbar_init();
+  const int cg = tid / cols, rr = (tid % cols) / D4, col = tid % D4;
+  const bool active = cg < CG;
+  const long long g = ((long long)b * p.Hkv + kvh) * p.RB + rb;
+  const float *row0 = p.ws_part + (g * p.ns_ws * p.R + s0 + rr) * (long long)RF;  // chunk c at + c * R * RF
+  const long long cstride = (long long)p.R * RF;
+  float M = -INFINITY, Ls = 0.f;
+  float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (active) {
+#pragma unroll 1
+    for (int c0 = cg; c0 < NC; c0 += CG * kBatch) {
+      float mv[kBatch], lv[kBatch];
+      float4 v[kBatch];
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k) {
+        const int c = c0 + k * CG;
+        lv[k] = 0.f;
+        mv[k] = -INFINITY;
+        v[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (c < NC) {
+          const float *rp = row0 + c * cstride;
+          lv[k] = __ldcg(rp + D + 1);
+          mv[k] = __ldcg(rp + D);
+          v[k] = __ldcg(reinterpret_cast<const float4 *>(rp) + col);
+        }
+      }
+      float bm = M;
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k)
+        if (lv[k] > 0.f) bm = fmaxf(bm, mv[k]);
+      const float base = bm == -INFINITY ? 0.f : bm;
+      const float alpha = exp2f(M - base);  // 0 while nothing is folded in (M = -inf)
+      Ls *= alpha;
+      A.x *= alpha, A.y *= alpha, A.z *= alpha, A.w *= alpha;
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k) {
+        if (lv[k] > 0.f) {
+          const float f = exp2f(mv[k] - base);
+          Ls = fmaf(lv[k], f, Ls);
+          A.x = fmaf(v[k].x, f, A.x), A.y = fmaf(v[k].y, f, A.y), A.z = fmaf(v[k].z, f, A.z),
+          A.w = fmaf(v[k].w, f, A.w);
+        }
+      }
+      M = bm;
+    }
   }
-  griddep_wait();  // the split kernel's partials and plan
-  griddep_launch_dependents();
+  float *sM = sm, *sL = sm + kThreads, *sA = sm + 2 * kThreads;  // [CG][nr], [CG][nr], [CG][nr][D]
+  if (active) {
+    if (col == 0) {
+      sM[cg * nr + rr] = M;
+      sL[cg * nr + rr] = Ls;
+    }
+    *reinterpret_cast<float4 *>(sA + (cg * nr + rr) * D + 4 * col) = A;
+  }
   __syncthreads();
-  const int S = p.plan_out[0];
-  const int L = p.plan_out[1 + b];
-  if (S <= 0 || L <= S) return;  // nothing to merge: no key, or one chunk written out directly
-  const int NC = (L + S - 1) / S;
-  const int nv = min(p.R, p.G * p.T - rb * p.R);
-  const int s0 = sl * kSliceRows, s1 = min(s0 + kSliceRows, nv);
-  if (s0 >= s1) return;
-  uint32_t phase = 0;
-  merge_row_slice<E, D>(p, msm, smem_floats, &bar, phase, b, kvh, rb, NC, s0, s1);
+  if (cg == 0) {
+    float Mt = -INFINITY;
+    for (int j = 0; j < CG; ++j)
+      if (sL[j * nr + rr] > 0.f) Mt = fmaxf(Mt, sM[j * nr + rr]);
+    float Lt = 0.f;
+    float4 At = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j = 0; j < CG; ++j) {
+      const float lj = sL[j * nr + rr];
+      if (lj > 0.f) {
+        const float f = exp2f(sM[j * nr + rr] - Mt);
+        const float4 x = *reinterpret_cast<const float4 *>(sA + (j * nr + rr) * D + 4 * col);
+        Lt = fmaf(lj, f, Lt);
+        At.x = fmaf(x.x, f, At.x), At.y = fmaf(x.y, f, At.y), At.z = fmaf(x.z, f, At.z), At.w = fmaf(x.w, f, At.w);
+      }
+    }
+    const long long orow = out_row_of(p, b, kvh, rb, s0 + rr);
+    const float inv = Lt > 0.f ? 1.f / Lt : 0.f;
+    E *o = static_cast<E *>(p.out) + orow * D + 4 * col;
+    store_elem<E>(o + 0, At.x * inv);
+    store_elem<E>(o + 1, At.y * inv);
+    store_elem<E>(o + 2, At.z * inv);
+    store_elem<E>(o + 3, At.w * inv);
+    if (col == 0 && p.lse != nullptr) p.lse[orow] = Lt > 0.f ? (Mt + log2f(Lt)) * kLn2 : -INFINITY;
+  }
+  __syncthreads();  // the scratch may be reused
 }
 
 // Completes one work item (sequence b, kv head, row block rb, chunk c of NC).
@@ -568,14 +516,24 @@ __global__ void __launch_bounds__(kThreads) merge_slices_kernel(const SplitParam
 //   cm[NSRC][ROWS] (row max), cl[NSRC][ROWS] (row sum), ca[NSRC][ROWS][CAS] (unnormalised p @ V)
 // at the start of the CTA's shared memory (`smem_f`, `smem_floats` floats free after this
 // call's combine), and a __syncthreads has made them visible. The sources are combined; a
-// chunk that is its sequence's only one writes out/lse, any other writes its partial block
-// to the workspace and, unless the merge is deferred, takes a completion ticket, and the CTA
-// holding the last ticket of (b, kv head, row block) merges all chunks and zeroes the counter
-// again. Ends with a __syncthreads (the shared areas may be reused afterwards).
+// chunk that is its sequence's only one writes out/lse; any other publishes its partial block
+// to the workspace and takes a completion ticket on its group's counter. The merge then:
+//  * blocks of more than 16 rows (a 24-row verify block of four grouped heads) in a one_wave
+//    launch (every CTA holds at most one item, and the launch fits the GPU at once): the CTAs
+//    holding the last NSL tickets of the group (NSL = min(rows, chunks)) each merge one slice
+//    of the rows, the last ticket slice 0 at once, the others after a bounded wait for the
+//    group's last ticket (a CTA they wait for is resident or becomes resident as other CTAs
+//    of the launch exit: none of them waits for it); the last of them to finish zeroes the
+//    group's counters again. One CTA staging every chunk's 24 rows took 28 us where the
+//    chunks streamed in 7;
+//  * otherwise the CTA holding the last ticket merges every row (merge_group): with a few rows
+//    the helpers' waits cost more than they save (their slots are the next call's).
+// Ends with a __syncthreads (the shared areas may be reused afterwards).
 template <typename E, int D, int ROWS, int NSRC, int CAS = D>
 __device__ void finish_item(const SplitParams &p, float *smem_f, int smem_floats, uint64_t *merge_bar,
-                            uint32_t &merge_phase, int b, int kvh, int rb, int c, int NC, int *s_last) {
-  constexpr int D4 = D / 4;
+                            uint32_t &merge_phase, int b, int kvh, int rb, int c, int NC, int *s_last,
+                            bool one_wave) {
+  constexpr int D4 = D / 4, RF = part_row_floats(D);
   const int tid = threadIdx.x;
   const int GT = p.G * p.T;
   const int R = p.R;
@@ -611,7 +569,6 @@ __device__ void finish_item(const SplitParams &p, float *smem_f, int smem_floats
     __syncthreads();
   }
   float *blk = p.ws_part + (g * p.ns_ws + c) * (long long)part_block_floats(R, D);
-  float *row_blk = p.ws_part + (g * p.ns_ws + c) * (long long)R * merge_row_floats(D);
 #pragma unroll 1
   for (int idx = tid; idx < nv * D4; idx += kThreads) {
     const int r = idx / D4, d = (idx % D4) * 4;
@@ -647,31 +604,47 @@ __device__ void finish_item(const SplitParams &p, float *smem_f, int smem_floats
       store_elem<E>(o + 2, A.z * inv);
       store_elem<E>(o + 3, A.w * inv);
       if (d == 0 && p.lse != nullptr) p.lse[row] = Ls > 0.f ? (M + log2f(Ls)) * kLn2 : -INFINITY;
-    } else if (p.deferred) {
-      float *dst = row_blk + r * merge_row_floats(D);
+    } else {
+      float *dst = blk + r * RF;
       *reinterpret_cast<float4 *>(dst + d) = A;
       if (d == 0) {
         dst[D] = Ls > 0.f ? M : -INFINITY;
         dst[D + 1] = Ls;
       }
-    } else {
-      *reinterpret_cast<float4 *>(blk + r * D + d) = A;
-      if (d == 0) {
-        blk[R * D + r] = Ls > 0.f ? M : -INFINITY;
-        blk[R * D + R + r] = Ls;
-      }
     }
   }
-  if (!single && !p.deferred) {
+  if (!single) {
     __syncthreads();  // every thread's block writes happen before thread 0's release
     int *cnt = p.counters + g;
+    int *fin = p.counters + (long long)p.B * p.Hkv * p.RB + g;
     if (tid == 0) {
       const int before = ticket_acq_rel(cnt);
       if (before < 0 || before >= NC) report(p.status, TD_DEV_WORKSPACE_DIRTY);
-      *s_last = before == NC - 1;
+      *s_last = before;
     }
     __syncthreads();
-    if (*s_last) {
+    const int t = *s_last;
+    if (one_wave && ROWS > 16) {
+      const int nsl = min(nv, NC);
+      const int s = NC - 1 - t;  // 0 for the last ticket
+      if (s >= 0 && s < nsl) {
+        const int rs = (nv + nsl - 1) / nsl;
+        const int r0 = min(s * rs, nv), r1 = min(r0 + rs, nv);
+        // slice 0's CTA holds the last ticket: every partial is visible to it already
+        const bool ready = s == 0 || wait_count(p, cnt, NC);
+        if (ready) {
+          constexpr int kMost = kThreads / D4;  // rows one pass of merge_rows_direct takes
+          for (int a = r0; a < r1; a += kMost) merge_rows_direct<E, D>(p, smem_f, b, kvh, rb, NC, a, min(a + kMost, r1));
+        }
+        if (tid == 0) {
+          const int done = atomicAdd(fin, 1);
+          if (done == nsl - 1) {  // every slice merged (or given up): the counters go back to zero
+            *cnt = 0;
+            *fin = 0;
+          }
+        }
+      }
+    } else if (t == NC - 1) {
       merge_group<E, D, ROWS>(p, smem_f, smem_floats, merge_bar, merge_phase, b, kvh, rb, NC, nv);
       if (tid == 0) *cnt = 0;  // leave the counter area zero for the next call
     }
@@ -940,7 +913,7 @@ __global__ void __launch_bounds__(kThreads, 2) split_attn_kernel(const SplitPara
       for (int d = 0; d < C::DV; ++d) ca[(warp * RP + r) * D + lane * C::DV + d] = acc[r][d];
     __syncthreads();
     finish_item<E, D, RP, kWarps>(p, combine, kWarps * C::RING_BYTES / 4, &s_merge_bar, merge_phase, b, kvh, rb, c,
-                                  NC, &s_last);
+                                  NC, &s_last, W <= (int)gridDim.x);
     if (s_abort) break;
   }
 }

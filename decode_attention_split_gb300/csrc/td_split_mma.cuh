@@ -768,11 +768,6 @@ __global__ void __launch_bounds__(kThreads, 2) split_attn_mma_kernel(const __gri
   const int S = s_chunk;
   const int W = s_prefix[p.B];
   const int rows = p.Hq * p.T;
-  if (p.deferred && blockIdx.x == 0) {
-    // the plan the deferred merge kernel follows
-    for (int b = tid; b < p.B; b += kThreads) p.plan_out[1 + b] = s_len[b];
-    if (tid == 0) p.plan_out[0] = S;
-  }
 
   // sequences with no key get no item: their rows are 0 with lse = -inf
   for (int b = blockIdx.x; b < p.B; b += gridDim.x) {
@@ -800,7 +795,7 @@ __global__ void __launch_bounds__(kThreads, 2) split_attn_mma_kernel(const __gri
     const int c0 = c * S;
     const bool ok = stream_chunk<D, NST, TILE>(a, smem, s_bars, seq, b, kvh, rb, L, c0, min(c0 + S, L));
     finish_item<E, D, TR, kWarps, combine_stride<D>()>(p, combine, C::RING_BYTES / 4, &s_merge_bar, merge_phase, b, kvh,
-                                                       rb, c, NC, &s_last);
+                                                       rb, c, NC, &s_last, W <= (int)gridDim.x);
     // the combine and merge wrote the ring through the generic proxy; the next item's first
     // stages refill it through the asynchronous proxy
     fence_proxy_async_smem();

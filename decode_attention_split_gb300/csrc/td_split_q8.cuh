@@ -583,7 +583,7 @@ __global__ void __launch_bounds__(kThreads, 2) split_attn_q8_kernel(const __grid
     const int c0 = c * S;
     const bool ok = stream_chunk_q8<D, NST, NARROW>(a, smem, s_bars, seq, b, kvh, rb, L, c0, min(c0 + S, L));
     finish_item<E, D, kMmaRows, kWarps>(p, combine, C::RING_BYTES / 4, &s_merge_bar, merge_phase, b,
-                                        kvh, rb, c, NC, &s_last);
+                                        kvh, rb, c, NC, &s_last, W <= (int)gridDim.x);
     fence_proxy_async_smem();
     __syncthreads();
     if (!ok) break;

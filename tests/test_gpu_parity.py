@@ -223,24 +223,25 @@ def test_cluster_kernel_against_oracle_and_persistent(td, D, Hq, Hkv, Smax, T, l
     assert_out_close(out_c, out_p.double().numpy(), "bf16", what="cluster vs persistent")
 
 
-# ------------------------------------------------------------- 24-row tile, deferred merge
+# ---------------------------------------------------- 24-row tile, merges by row slices
 
-DEFERRED = [
-    # D, Hq, Hkv, Smax, T, lengths, split: row blocks of 17 to 24 rows on the 24-row tile, whose
-    # chunks are merged by the second kernel, one CTA per slice of 4 rows
+ROW_SLICES = [
+    # D, Hq, Hkv, Smax, T, lengths, split: row blocks of 17 to 24 rows on the 24-row tile; in a
+    # one-wave plan the CTAs holding a group's last tickets merge one row slice each, in a
+    # plan of several waves (a small explicit split) the last CTA merges every row
     (128, 32, 8, 2000, 6, [1990], 0),          # verify: 24 rows, 6 slices
     (128, 16, 4, 700, 6, [690, 100], 0),       # verify, two sequences
     (128, 16, 4, 300, 6, [300, 6, 0], 0),      # a chunk of exactly T keys and an empty sequence
     (128, 160, 8, 900, 1, [900], 0),           # 20 rows: decode on the 24-row tile
     (64, 36, 2, 1000, 1, [1000, 999], 0),      # 18 rows at D = 64: a ragged last slice
-    (128, 32, 8, 2000, 6, [1990], 16),         # 125 chunks: the merge stages them in rounds
+    (128, 32, 8, 2000, 6, [1990], 16),         # 125 chunks, several waves: one CTA merges in rounds
     (128, 32, 8, 600, 6, [600, 33], 37),       # a 37-key split: ragged stages in every chunk
     (128, 40, 4, 500, 2, [500], 0),            # 20 rows from 10 heads x 2 tokens
 ]
 
 
-@pytest.mark.parametrize("D,Hq,Hkv,Smax,T,lens,split", DEFERRED)
-def test_deferred_merge_against_oracle(td, D, Hq, Hkv, Smax, T, lens, split):
+@pytest.mark.parametrize("D,Hq,Hkv,Smax,T,lens,split", ROW_SLICES)
+def test_row_slice_merges_against_oracle(td, D, Hq, Hkv, Smax, T, lens, split):
     B = len(lens)
     plan = td.td_split_plan(torch.bfloat16, B, Hq, Hkv, Smax, D, T, split)
     assert plan["kernel"] == "tensor_core_persistent" and 16 < plan["rows"] <= 24, plan
@@ -249,7 +250,7 @@ def test_deferred_merge_against_oracle(td, D, Hq, Hkv, Smax, T, lens, split):
     check_case(td, case, split=split)
 
 
-def test_deferred_merge_repeat_calls_bit_identical(td):
+def test_row_slice_merges_repeat_calls_bit_identical_and_counters_rezeroed(td):
     case = small_case(dtype="bf16", B=1, Hq=32, Hkv=8, D=128, Smax=5000, T=6, seq_lens=[5000], seed=21)
     q, k, v, sl = case.q.cuda(), case.k_cache.cuda(), case.v_cache.cuda(), case.seq_lens.cuda()
     ws = td.make_workspace(1, 32, 8, 5000, 128, 6, 0)
@@ -258,7 +259,8 @@ def test_deferred_merge_repeat_calls_bit_identical(td):
     o2 = td.td_verify_attn(q, k, v, sl, case.scale, 0, workspace=ws, dev_status=st)
     torch.cuda.synchronize()
     assert torch.equal(o1, o2) and int(st.item()) == 0
-    assert int(ws[:4 * 8].view(torch.int32).abs().sum()) == 0
+    # completion tickets and finished-slice counts of the 8 groups are back to zero
+    assert int(ws[:4 * 16].view(torch.int32).abs().sum()) == 0
 
 
 def test_automatic_split_fills_one_wave(td):
@@ -404,7 +406,7 @@ def test_repeat_calls_bit_identical_and_counters_rezeroed(td):
     o2 = td.td_decode_attn(q, k, v, sl, case.scale, 0, workspace=ws)
     torch.cuda.synchronize()
     assert torch.equal(o1, o2)
-    counters = ws[:2 * 8 * 4].view(torch.int32)
+    counters = ws[:2 * 2 * 8 * 4].view(torch.int32)  # tickets and finished-slice counts
     assert int(counters.abs().sum()) == 0
 
 

@@ -128,7 +128,6 @@ def test_hot_kernels_have_no_spills(lib):
            "split_attn_mma_kernelILi128ELb0ELi2E", "split_attn_mma_kernelILi128ELb0ELi0E",
            "split_attn_mma_kernelILi64ELb1ELi1E", "split_attn_mma_kernelILi64ELb1ELi0E",
            "split_attn_mma_kernelILi64ELb0ELi0E", "split_attn_kernelIfLi64ELi2E",
-           "merge_slices_kernelI13__nv_bfloat16Li128E",
            "split_attn_cluster_kernelILi128ELi0E", "split_attn_cluster_kernelILi128ELi1E",
            "split_attn_cluster_kernelILi128ELi2E", "split_attn_q8_kernelILi128ELb0ELb0E",
            "split_attn_q8_kernelILi128ELb1ELb0E", "split_attn_q8_kernelILi128ELb1ELb1E",
