@@ -62,10 +62,12 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--profile-launches", type=int, default=0,
                     help="profiling mode: W warm-up calls then this many plain launches, no graphs, no JSON extras")
-    ap.add_argument("--profile-row", default=None, choices=["q8", "prefill"],
-                    help="profiling mode for a NEXT row's kernel instead of the timed step's call: q8 = "
+    ap.add_argument("--profile-row", default=None, choices=["q8", "prefill", "verify6", "ragged8"],
+                    help="profiling mode for another kernel instead of the timed step's call: q8 = "
                          "td_decode_attn_q8 on the 3B-style layer at --seq-len with --profile-batch sequences "
-                         "(cache quantised on the GPU); prefill = td_prefill_attn on a --seq-len-token prompt")
+                         "(cache quantised on the GPU); prefill = td_prefill_attn on a --seq-len-token prompt; "
+                         "verify6 / ragged8 = td_verify_attn / td_decode_attn on those workloads, the launches "
+                         "rotating over cache copies that together exceed 4 x L2")
     ap.add_argument("--profile-batch", type=int, default=4)
     return ap.parse_args()
 
@@ -448,6 +450,26 @@ def sweep_point(td, name, L, dev, l2_bytes, peak, budget_calls=200, split=0):
 
 def profile_row(td, args, dev):
     """Plain launches of one NEXT row's kernel (W warm-up, then --profile-launches), no timing."""
+    if args.profile_row in ("verify6", "ragged8"):
+        w = WORKLOADS[args.profile_row]
+        case = make_case(w, seq_len=16390 if w.T > 1 else None)
+        nbytes = kv_read_bytes(w, case.seq_lens.tolist())
+        C = max(2, math.ceil(4 * torch.cuda.get_device_properties(dev).L2_cache_size / nbytes))
+        kc = rotating_copies(case.k_cache.to(dev), C)
+        vc = rotating_copies(case.v_cache.to(dev), C)
+        q, sl = case.q.to(dev), case.seq_lens.to(dev)
+        out = torch.empty_like(q)
+        ws = td.make_workspace(w.B, w.Hq, w.Hkv, w.Smax, w.D, w.T, 0, device=dev)
+        for i in range(args.warmup + args.profile_launches):
+            c = i % C
+            if w.T > 1:
+                td.td_verify_attn(q, kc[c], vc[c], sl, case.scale, 0, out=out, workspace=ws)
+            else:
+                td.td_decode_attn(q[:, :, 0], kc[c], vc[c], sl, case.scale, 0, out=out[:, :, 0], workspace=ws)
+        torch.cuda.synchronize(dev)
+        print(json.dumps({"profile_row": args.profile_row, "kv_bytes_per_launch": nbytes, "cache_copies": C,
+                          "launches": args.warmup + args.profile_launches, "ok": True}))
+        return
     g = torch.Generator(device=dev).manual_seed(0)
     w = WORKLOADS["llama3b"]
     L, B = args.seq_len, args.profile_batch
