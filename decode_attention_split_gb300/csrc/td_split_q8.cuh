@@ -46,7 +46,7 @@ struct Q8Cfg {
   static constexpr int SMEM_BYTES = RING_BYTES + 1024;         // + alignment slack
   static_assert(CODE_BYTES % 1024 == 0, "code tiles keep the swizzle's 1024-byte alignment");
   static_assert(SCALE_BOX * 4 <= SCALE_SLOT && (SCALE_BOX * 4) % 16 == 0, "scale box");
-  static_assert(kWarps * kMmaRows * (D + 2) * 4 <= RING_BYTES, "combine area fits");
+  static_assert(kWarps * kMmaRows * (D + 6) * 4 <= RING_BYTES, "combine area fits (rows D + 4 floats apart)");
 };
 
 // Ring depth: two CTAs per SM, NST - 1 stages in flight while one is read.
@@ -482,7 +482,7 @@ __device__ bool stream_chunk_q8(const Q8Args &a, unsigned char *smem, uint64_t *
         cl[warp * kMmaRows + r] = l_run[e];
       }
       const float bias = ob[e];  // 1152 * sum(p) of row r
-      float *row = &ca[(warp * kMmaRows + r) * D];
+      float *row = &ca[(warp * kMmaRows + r) * combine_stride<D>()];
 #pragma unroll
       for (int i = 0; i < D / 32; ++i) {
         *reinterpret_cast<float2 *>(&row[32 * i + 2 * gid]) = make_float2(o[2 * i][e] - bias, o[2 * i + 1][e] - bias);
@@ -503,7 +503,7 @@ __device__ bool stream_chunk_q8(const Q8Args &a, unsigned char *smem, uint64_t *
     const float bias = ob[2 * h];  // 1152 * sum(p) of row r: the code bias in every output
 #pragma unroll
     for (int j = 0; j < D / 16; ++j)
-      *reinterpret_cast<float4 *>(&ca[(warp * kMmaRows + r) * D + 16 * j + 4 * tig]) =
+      *reinterpret_cast<float4 *>(&ca[(warp * kMmaRows + r) * combine_stride<D>() + 16 * j + 4 * tig]) =
           make_float4(o[2 * j][2 * h] - bias, o[2 * j + 1][2 * h] - bias, o[2 * j][2 * h + 1] - bias,
                       o[2 * j + 1][2 * h + 1] - bias);
   }
@@ -582,7 +582,7 @@ __global__ void __launch_bounds__(kThreads, 2) split_attn_q8_kernel(const __grid
     const int kvh = rest / p.RB;
     const int c0 = c * S;
     const bool ok = stream_chunk_q8<D, NST, NARROW>(a, smem, s_bars, seq, b, kvh, rb, L, c0, min(c0 + S, L));
-    finish_item<E, D, kMmaRows, kWarps>(p, combine, C::RING_BYTES / 4, &s_merge_bar, merge_phase, b,
+    finish_item<E, D, kMmaRows, kWarps, combine_stride<D>()>(p, combine, C::RING_BYTES / 4, &s_merge_bar, merge_phase, b,
                                         kvh, rb, c, NC, &s_last, W <= (int)gridDim.x);
     fence_proxy_async_smem();
     __syncthreads();
