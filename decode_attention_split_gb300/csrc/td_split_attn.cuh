@@ -361,24 +361,45 @@ __device__ void merge_group(const SplitParams &p, float *smem_f, int smem_floats
       }
     }
     __syncthreads();
-    // weighted sums, four dims per thread; in the last round they are the output
+    // weighted sums, four dims per thread, over the staged chunks in four independent
+    // accumulators (chunk c into c % 4: a quarter of the dependent chain); in the last round
+    // they are the output
 #pragma unroll 1
     for (int idx = tid; idx < nv * D4; idx += kThreads) {
       const int r = idx / D4, d = (idx % D4) * 4;
       const float *a = stage + r * RF + d;
       const float *f = fac + r * kFB;
-      float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+      float4 xs[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) xs[k] = make_float4(0.f, 0.f, 0.f, 0.f);
       if (c0 > 0) {
         const float sc = st[2 * ROWS + r];
-        x = *reinterpret_cast<const float4 *>(acc + r * D + d);
-        x.x *= sc, x.y *= sc, x.z *= sc, x.w *= sc;
+        xs[0] = *reinterpret_cast<const float4 *>(acc + r * D + d);
+        xs[0].x *= sc, xs[0].y *= sc, xs[0].z *= sc, xs[0].w *= sc;
       }
-#pragma unroll 4
-      for (int c = 0; c < nb; ++c) {
+      int c = 0;
+#pragma unroll 1
+      for (; c + 4 <= nb; c += 4) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float4 v = *reinterpret_cast<const float4 *>(a + (c + k) * BF);
+          const float w = f[c + k];
+          xs[k].x = fmaf(v.x, w, xs[k].x), xs[k].y = fmaf(v.y, w, xs[k].y), xs[k].z = fmaf(v.z, w, xs[k].z),
+          xs[k].w = fmaf(v.w, w, xs[k].w);
+        }
+      }
+#pragma unroll 1
+      for (; c < nb; ++c) {
         const float4 v = *reinterpret_cast<const float4 *>(a + c * BF);
         const float w = f[c];
-        x.x = fmaf(v.x, w, x.x), x.y = fmaf(v.y, w, x.y), x.z = fmaf(v.z, w, x.z), x.w = fmaf(v.w, w, x.w);
+        xs[0].x = fmaf(v.x, w, xs[0].x), xs[0].y = fmaf(v.y, w, xs[0].y), xs[0].z = fmaf(v.z, w, xs[0].z),
+        xs[0].w = fmaf(v.w, w, xs[0].w);
       }
+      float4 x;
+      x.x = (xs[0].x + xs[1].x) + (xs[2].x + xs[3].x);
+      x.y = (xs[0].y + xs[1].y) + (xs[2].y + xs[3].y);
+      x.z = (xs[0].z + xs[1].z) + (xs[2].z + xs[3].z);
+      x.w = (xs[0].w + xs[1].w) + (xs[2].w + xs[3].w);
       if (last) {
         const float inv = st[3 * ROWS + r];
         E *o = static_cast<E *>(p.out) + out_row_of(p, b, kvh, rb, r) * D + d;
