@@ -446,7 +446,7 @@ __device__ __forceinline__ bool wait_count(const SplitParams &p, const int *cnt,
 // and the groups are combined in shared memory `sm` (6 * kThreads floats). Writes out and lse.
 template <typename E, int D>
 __device__ void merge_rows_direct(const SplitParams &p, float *sm, int b, int kvh, int rb, int NC, int s0, int s1) {
-  constexpr int D4 = D / 4, RF = part_row_floats(D), kBatch = 8;
+  constexpr int D4 = D / 4, RF = part_row_floats(D), kBatch = 12;
   const int nr = s1 - s0;
   const int cols = nr * D4;
   const int CG = kThreads / cols;
