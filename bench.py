@@ -292,9 +292,6 @@ def kernel_label(td, w) -> str:
                                   f"mma.sync bf16 {tile}, TMA)",
         "tensor_core_cluster": f"split_attn_cluster_kernel<{w.D}> (clusters of {plan['cluster']}, on-chip merge, "
                                f"mma.sync bf16 {tile}, TMA)",
-        "tensor_core_cluster_combine": f"split_attn_cc_kernel<{w.D}> (persistent clusters of {plan['cluster']}: "
-                                       f"chunk partials combined on chip, row-slice merges through the workspace, "
-                                       f"mma.sync bf16 {tile}, TMA)",
         "cuda_core": f"split_attn_kernel<{w.D}> (CUDA cores)",
     }
     return f"{names[plan['kernel']]}, grid {plan['grid']}, timed alone"

@@ -71,7 +71,7 @@ def td_decode_workspace_bytes(B: int, Hq: int, Hkv: int, Smax: int, D: int, q_le
     return int(lib().td_decode_workspace_bytes(B, Hq, Hkv, Smax, D, q_len, split))
 
 
-KERNEL_NAMES = ("cuda_core", "tensor_core_persistent", "tensor_core_cluster", "tensor_core_cluster_combine")
+KERNEL_NAMES = ("cuda_core", "tensor_core_persistent", "tensor_core_cluster")
 
 
 def td_split_plan(dtype: torch.dtype, B: int, Hq: int, Hkv: int, Smax: int, D: int, q_len: int = 1,

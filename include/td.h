@@ -116,7 +116,8 @@ size_t td_decode_workspace_bytes(int B, int Hq, int Hkv, int Smax, int D, int q_
  *               cluster per (b, kv head, row block), one chunk per CTA, the merge done in
  *               distributed shared memory; the workspace is not touched);
  *   *grid    CTAs launched;  *cluster  CTAs per cluster (0 unless kernel 2);
- *   *rows    query rows per CTA.
+ *   *rows    query rows per CTA (bf16: a kv head's rows cut into row blocks of at most 24: up to
+ *            8 on the narrow n8 tile, 9 to 16 on the m16 tile, 17 to 24 on the 24-row tile).
  * Returns what the attention call would return for a bad shape, TD_ERR_CUDA without a device.
  */
 td_status td_split_plan(td_dtype dtype, int B, int Hq, int Hkv, int Smax, int D, int q_len, int split, int *kernel,
