@@ -111,7 +111,9 @@ size_t td_decode_workspace_bytes(int B, int Hq, int Hkv, int Smax, int D, int q_
  *   *kernel  0: CUDA-core split kernel (fp32 caches);
  *            1: tensor-core persistent kernel (bf16; CTAs walk (b, kv head, row block, chunk)
  *               items, partials meet in the workspace and the CTA finishing a group's last
- *               chunk merges them);
+ *               chunk merges them; for row blocks of more than 16 rows in a launch where each
+ *               CTA holds one item, the CTAs holding the group's last tickets merge one row
+ *               each);
  *            2: tensor-core cluster kernel (bf16, split = 0, few groups: one thread-block
  *               cluster per (b, kv head, row block), one chunk per CTA, the merge done in
  *               distributed shared memory; the workspace is not touched);
