@@ -58,7 +58,7 @@ struct PfCfg {
   static constexpr int K_OFF = Q_TILE;                  // two K buffers
   static constexpr int V_OFF = K_OFF + 2 * KV_TILE;     // two V buffers
   static constexpr int SMEM = V_OFF + 2 * KV_TILE + 1024;  // + alignment slack
-  static constexpr int TMEM_COLS = 256;                 // two S buffers (64 each) + O (D), a power of two
+  static constexpr int TMEM_COLS = 256;                 // S (64), two P buffers (32 each), O (D): a power of two
   static_assert(2 * (SMEM + 1024 + 128) <= 228 * 1024, "two CTAs per SM");
 };
 
@@ -213,7 +213,8 @@ template <int D>
 __global__ void __launch_bounds__(kPfThreads, 2) prefill_kernel(const __grid_constant__ PfArgs a) {
   using C = PfCfg<D>;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
-  __shared__ __align__(8) uint64_t bar_q, bar_k[2], bar_v[2], bar_s[2], bar_p[2], bar_vfree[2], bar_o, bar_fin;
+  __shared__ __align__(8) uint64_t bar_q, bar_k[2], bar_v[2], bar_s[2], bar_sfree, bar_p[2], bar_vfree[2], bar_o,
+      bar_fin;
   __shared__ uint32_t s_taddr;
   __shared__ int s_issued[2], s_seen[3];  // wind-down: K / V tiles issued; K / V tiles, Q seen landed
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -239,6 +240,7 @@ __global__ void __launch_bounds__(kPfThreads, 2) prefill_kernel(const __grid_con
     s_issued[0] = s_issued[1] = 0;
     s_seen[0] = s_seen[1] = 0;
     s_seen[2] = 1;
+    mbar_init(smem_u32(&bar_sfree), kPfSoftmaxWarps);
     mbar_init(smem_u32(&bar_o), 1);
     mbar_init(smem_u32(&bar_fin), 1);
     fence_mbar_init();
@@ -253,7 +255,9 @@ __global__ void __launch_bounds__(kPfThreads, 2) prefill_kernel(const __grid_con
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = s_taddr;
-  const uint32_t tS = tmem, tO = tmem + 128;  // S buffer i at tS + 64 i
+  // S of the current tile in columns [0, 64), P of tile kt in P buffer kt % 2 (columns 64 + 32 (kt % 2),
+  // bf16 pairs), O in [128, 128 + D)
+  const uint32_t tS = tmem, tP = tmem + kPfKeys, tO = tmem + 128;
 
   griddep_wait();
   griddep_launch_dependents();
@@ -286,15 +290,16 @@ __global__ void __launch_bounds__(kPfThreads, 2) prefill_kernel(const __grid_con
       const uint64_t dq = smem_desc(sb + C::Q_OFF, 16, 1024);
       const uint64_t dk = smem_desc(sb + C::K_OFF, 16, 1024);
       const uint64_t dv = smem_desc(sb + C::V_OFF, kKRegion, 1024);
-      // S of tile kt into S buffer kt % 2 (K tile kt has landed): over D in steps of 16 (32
-      // bytes along a swizzled row; the next 64 columns are the next region)
+      // S of tile kt into the S columns (K tile kt has landed; its completion is signalled on
+      // the barrier of K buffer kt % 2): over D in steps of 16 (32 bytes along a swizzled row;
+      // the next 64 columns are the next region)
       auto issue_s = [&](int kt) {
         const uint32_t kb = (uint32_t)(kt & 1) * C::KV_TILE;
         tc_fence_after();
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
           const uint32_t off = (uint32_t)(k & 3) * 32;
-          tc_mma(tS + (kt & 1) * kPfKeys, dq + (((uint32_t)(k >> 2) * kQRegion + off) >> 4),
+          tc_mma(tS, dq + (((uint32_t)(k >> 2) * kQRegion + off) >> 4),
                  dk + ((kb + (uint32_t)(k >> 2) * kKRegion + off) >> 4), kIdS, k > 0);
         }
         tc_commit(smem_u32(&bar_s[kt & 1]));
@@ -308,15 +313,15 @@ __global__ void __launch_bounds__(kPfThreads, 2) prefill_kernel(const __grid_con
       for (int kt = 0; ok && kt < nkt; ++kt) {
         const int b0 = kt & 1, b1 = b0 ^ 1;
         if (kt + 1 < nkt) {
-          // S buffer b1 (P of kt-1) is free once the P V product of kt-1 is done
-          if (kt >= 1) ok = mbar_wait_bounded(smem_u32(&bar_o), (uint32_t)(kt - 1) & 1u);
+          // the S columns are free once every softmax warp has read S of kt
+          ok = mbar_wait_bounded(smem_u32(&bar_sfree), (uint32_t)kt & 1u);
           ok = ok && mbar_wait_bounded(smem_u32(&bar_k[b1]), (uint32_t)((kt + 1) >> 1) & 1u);
           if (!ok) break;
           kw = kt + 2;
           issue_s(kt + 1);
         }
-        // P of kt is in TMEM (all four softmax warps) and V of kt has landed: O += P V over
-        // 64 keys in steps of 16 (A: 8 TMEM columns per step; B: MN-major, 16 rows of 128
+        // P of kt is in P buffer b0 (all four softmax warps) and V of kt has landed: O += P V
+        // over 64 keys in steps of 16 (A: 8 TMEM columns per step; B: MN-major, 16 rows of 128
         // bytes per step, the next 64 columns in the next region)
         ok = mbar_wait_bounded(smem_u32(&bar_p[b0]), (uint32_t)(kt >> 1) & 1u) &&
              mbar_wait_bounded(smem_u32(&bar_v[b0]), (uint32_t)(kt >> 1) & 1u);
@@ -326,9 +331,9 @@ __global__ void __launch_bounds__(kPfThreads, 2) prefill_kernel(const __grid_con
         const uint32_t vb = (uint32_t)b0 * C::KV_TILE;
 #pragma unroll
         for (int k = 0; k < kPfKeys / 16; ++k)
-          tc_mma_ts(tO, tS + b0 * kPfKeys + 8 * k, dv + ((vb + (uint32_t)k * 16 * 128) >> 4), kIdO, kt > 0 || k > 0);
+          tc_mma_ts(tO, tP + b0 * (kPfKeys / 2) + 8 * k, dv + ((vb + (uint32_t)k * 16 * 128) >> 4), kIdO, kt > 0 || k > 0);
         tc_commit(smem_u32(&bar_o));
-        tc_commit(smem_u32(&bar_vfree[b0]));  // V buffer b0 may be refilled
+        tc_commit(smem_u32(&bar_vfree[b0]));  // V buffer b0 may be refilled, P buffer b0 rewritten
       }
       s_seen[0] = kw;
       s_seen[1] = vw;
@@ -382,7 +387,6 @@ __global__ void __launch_bounds__(kPfThreads, 2) prefill_kernel(const __grid_con
     for (int kt = 0; kt < nkt; ++kt) {
       const int b0 = kt & 1;
       const uint32_t ph = (uint32_t)(kt >> 1) & 1u;
-      const uint32_t tSk = tS + b0 * kPfKeys + lane_base;
       // S of kt is complete (the TMEM accesses below are warp-wide: one decision per warp)
       if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&bar_s[b0]), ph))) {
         ok = false;
@@ -405,9 +409,12 @@ __global__ void __launch_bounds__(kPfThreads, 2) prefill_kernel(const __grid_con
         }
         fence_proxy_async_smem();  // read next by the tensor core (asynchronous proxy)
       }
-      // this row's 64 scores, read once
+      // this row's 64 scores, read once; then the S columns are released for the next tile
       float sv[kPfKeys];
-      tmem_ld64(tSk, sv);
+      tmem_ld64(tS + lane_base, sv);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&bar_sfree));
       // tiles short of every row's diagonal and of the sequence's end need no mask; in the
       // others, keys from `vis` on are masked (this row's visible keys of the tile)
       const bool full = j0 + kPfKeys <= kall;
@@ -444,14 +451,21 @@ __global__ void __launch_bounds__(kPfThreads, 2) prefill_kernel(const __grid_con
           tmem_st32(tO + lane_base + c, o);
         }
       }
-      // P = 2^(s - m) as bf16 pairs over the S buffer's first 32 columns
+      // P = 2^(s - m) as bf16 pairs into P buffer b0, once the P V product of kt-2 has read it
       const float nbase = m_ref == -INFINITY ? 0.f : -m_ref;
       uint32_t pk[kPfKeys / 2];
       if (full)
         l += p_row<false>(sv, qscale, nbase, vis, pk);
       else
         l += p_row<true>(sv, qscale, nbase, vis, pk);
-      tmem_st32(tSk, pk);
+      if (kt >= 2) {
+        if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&bar_vfree[b0]), (uint32_t)((kt - 2) >> 1) & 1u))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+      }
+      tmem_st32(tP + b0 * (kPfKeys / 2) + lane_base, pk);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&bar_p[b0]));
