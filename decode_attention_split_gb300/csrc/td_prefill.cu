@@ -10,15 +10,16 @@
 // and V tiles cross by TMA with the 128-byte swizzle (K and V double-buffered with their own
 // barriers, 64 keys per tile). A fifth warp issues the tensor-core products and a sixth the
 // copies (a copy waits for its buffer's previous product, which must not hold up the next
-// product's issue); the accumulators live in TMEM:
-//   S[128 x 64] = Q K^T     (A = Q, B = K, both K-major in shared memory)  -> S buffer kt % 2
+// product's issue); the accumulators live in TMEM (256 columns: S in [0, 64), P buffers in
+// [64, 96) and [96, 128), O from column 128):
+//   S[128 x 64] = Q K^T     (A = Q, B = K, both K-major in shared memory)  -> S columns
 //   O[128 x D] += P V       (A = P in TMEM, B = V MN-major in shared memory) -> O
-// S is double-buffered (TMEM columns [0, 64) and [64, 128), O from column 128), so the
-// product S of tile kt+1 runs while the four softmax warps work on tile kt. Each softmax
-// thread owns one query row (its TMEM lane): it reads its 64 scores once, masks them
-// causally (only in tiles that reach the diagonal or the sequence's end), and writes
-// P = 2^(s - m) as bf16 pairs over the first 32 columns of the same S buffer, which the P V
-// product reads as its A operand (lane = row, one column per pair of keys). A softmax warp
+// Each softmax thread owns one query row (its TMEM lane): it reads its 64 scores once and at
+// once releases the S columns (an "S free" barrier, one arrival per warp), so the product S of
+// tile kt+1 runs while the four softmax warps work on tile kt. It masks the scores causally
+// (only in tiles that reach the diagonal or the sequence's end) and writes P = 2^(s - m) as
+// bf16 pairs into P buffer kt % 2 once the P V product of tile kt-2 has read it; the P V
+// product reads P as its A operand (lane = row, one column per pair of keys). A softmax warp
 // hands its rows over through an mbarrier (one arrival per warp), so the warps do not wait
 // for one another within a tile. The reference maximum m moves only when a row's maximum
 // rises more than 8 (base 2) above it, and only then are that row's O and l rescaled (after
