@@ -205,6 +205,11 @@ CLUSTER = [
     (128, 32, 8, 700, 6, [690, 100, 350, 7]),                  # verify: 24 rows on the 24-row tile
     (128, 32, 8, 64, 6, [64, 3, 60, 6]),                       # verify with short sequences
     (128, 24, 8, 1000, 1, [1000, 1000, 999, 1000]),            # Smax not a stage multiple
+    # ragged batches: long sequences beside short and empty ones
+    (128, 24, 8, 8192, 1, [8192, 64, 8192, 100]),               # long sequences beside short ones
+    (128, 32, 8, 4096, 6, [4096, 100, 50, 2000]),               # verify rows on the 24-row tile
+    (64, 16, 4, 5000, 1, [5000, 3, 2500, 4999, 1, 0, 4000, 700]),  # D = 64, short and empty ones
+    (128, 32, 8, 6000, 1, [5911, 443, 5723, 17, 600, 3000, 1, 4500]),  # pieces beside whole groups
 ]
 
 
@@ -261,6 +266,26 @@ def test_row_slice_merges_repeat_calls_bit_identical_and_counters_rezeroed(td):
     assert torch.equal(o1, o2) and int(st.item()) == 0
     # completion tickets and finished-slice counts of the 8 groups are back to zero
     assert int(ws[:4 * 16].view(torch.int32).abs().sum()) == 0
+
+
+def test_cluster_ragged_repeat_calls_bit_identical_and_workspace_clean(td):
+    """A ragged batch on the cluster kernel: a second call on the same workspace gives the same
+    bits, and the workspace's counters are left at zero for the next call."""
+    lens = [8000, 100, 7000, 5]
+    B, Hq, Hkv, D, Smax = len(lens), 32, 8, 128, 8000
+    assert td.td_split_plan(torch.bfloat16, B, Hq, Hkv, Smax, D, 1, 0)["kernel"] == "tensor_core_cluster"
+    case = small_case(dtype="bf16", B=B, Hq=Hq, Hkv=Hkv, D=D, Smax=Smax, T=1, seq_lens=lens, seed=5)
+    q, k, v, sl = case.q.cuda()[:, :, 0], case.k_cache.cuda(), case.v_cache.cuda(), case.seq_lens.cuda()
+    ws = td.make_workspace(B, Hq, Hkv, Smax, D, 1, 0)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    o1 = td.td_decode_attn(q, k, v, sl, case.scale, 0, workspace=ws, dev_status=st)
+    o2 = td.td_decode_attn(q, k, v, sl, case.scale, 0, workspace=ws, dev_status=st)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and int(st.item()) == 0
+    assert int(ws[:4 * 2 * B * Hkv].view(torch.int32).abs().sum()) == 0
+    ref, _, _ = oracle.load().attention(to_numpy(case.q), to_numpy(case.k_cache), to_numpy(case.v_cache),
+                                        to_numpy(case.seq_lens), case.scale)
+    assert_out_close(o1.cpu()[:, :, None], ref, "bf16")
 
 
 def test_automatic_split_fills_one_wave(td):
