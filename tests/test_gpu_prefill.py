@@ -42,6 +42,9 @@ PREFILL = [
     (1, 8, 8, 128, 1000, 129, [1000]),          # 129 tokens on an 871-token prefix
     (1, 4, 1, 128, 64, 64, [64]),
     (3, 12, 4, 128, 700, 200, [700, 200, 455]),
+    # more query tiles (heads x tiles) than CTA slots: a second wave of CTAs
+    (2, 40, 8, 128, 700, 512, [512, 700]),      # with a 188-token prefix in sequence 1
+    (4, 32, 4, 64, 400, 384, [384, 400, 390, 384]),
 ]
 
 
