@@ -323,7 +323,7 @@ def spec_point(td, dev, l2_bytes, peak, B=1, G=4, V=128256, budget_calls=200):
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=s):
         calls()
-    ms = min(time_graph(g, s, 3) for _ in range(3))
+    ms = statistics.median(time_graph(g, s, 3) for _ in range(5))
     us = ms * 1e3 / (3 * R)
     del target, draft
     torch.cuda.empty_cache()
@@ -365,7 +365,7 @@ def q8_point(td, name, L, dev, l2_bytes, peak, budget_calls=200):
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=s):
         calls()
-    ms = min(time_graph(g, s, 3) for _ in range(3))
+    ms = statistics.median(time_graph(g, s, 3) for _ in range(5))
     us = ms * 1e3 / (3 * R)
     del kcs, kss, vcs, vss
     torch.cuda.empty_cache()
@@ -393,7 +393,7 @@ def prefill_point(td, dev, T=4096, B=1, Hq=24, Hkv=8, D=128, reps=20):
     with torch.cuda.graph(gr, stream=s):
         for _ in range(reps):
             td.td_prefill_attn(q, k, v, sl, out=out, stream=s)
-    ms = min(time_graph(gr, s, 2) for _ in range(3)) / (2 * reps)
+    ms = statistics.median(time_graph(gr, s, 2) for _ in range(5)) / (2 * reps)
     flops = 4 * D * Hq * B * T * (T + 1) / 2
     tf = flops / (ms * 1e-3) / 1e12
     peaks, kind = measured_peaks()
@@ -435,7 +435,7 @@ def sweep_point(td, name, L, dev, l2_bytes, peak, budget_calls=200, split=0):
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=s):
         calls()
-    ms = min(time_graph(g, s, 3) for _ in range(3))
+    ms = statistics.median(time_graph(g, s, 3) for _ in range(5))
     us = ms * 1e3 / (3 * R)
     gbs = bytes_call / (us * 1e-6) / 1e9
     del kc, vc
