@@ -406,6 +406,19 @@ def test_empty_sequence(td):
     assert_value_close(out, ref, case_value_stats(case, ref_lse))
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_largest_batch(td, dtype):
+    """1024 sequences (the library's batch limit) of short mixed lengths, some empty: the
+    device plan's per-sequence arrays at their size limit, a plan of several waves, and every
+    row against the oracle."""
+    B = 1024
+    g = torch.Generator().manual_seed(11)
+    lens = torch.randint(0, 101, (B,), generator=g)
+    lens[::97] = 0
+    case = small_case(dtype=dtype, B=B, Hq=4, Hkv=2, D=64, Smax=100, seq_lens=lens.tolist(), seed=12)
+    check_case(td, case, split=0)
+
+
 def test_all_empty_batch(td):
     case = small_case(dtype="f32", B=2, Hq=4, Hkv=2, D=64, Smax=32, seq_lens=[0, 0], seed=8)
     out, lse, _ = run_attention(td, case)
