@@ -102,6 +102,8 @@ Q8 = [
     (128, 16, 2, 700, 1, [700, 129], 0),        # 8 rows per kv head: the narrow tile's limit
     (64, 18, 2, 700, 1, [650, 64], 0),          # 9 rows: one 16-row m tile
     (128, 4, 2, 300, 4, [300, 70], 0),          # verify, 8 rows, each with its own causal limit
+    # 40 sequences of mixed lengths (one empty): past 1/16 of the slots, the late plan and the full grid
+    (128, 24, 8, 600, 1, [(37 * i) % 601 for i in range(40)], 0),
 ]
 
 
