@@ -128,6 +128,8 @@ FUSED = [
     (1, 15, 5, 64, 1000, 1, [999], True, True),              # D = 64
     (3, 8, 2, 128, 256, 3, [250, 254, 40], True, True),      # second sequence overflows
     (1, 24, 8, 128, 4096, 1, [3000], False, True),           # no rotation: append + attention
+    # 200 sequences (400 groups): items in several waves; the lengths advance once every CTA read them
+    (200, 8, 2, 64, 300, 1, [(13 * i) % 290 for i in range(200)], True, True),
 ]
 
 
