@@ -7,7 +7,8 @@ array, with different shapes, element types and split sizes (a bf16 3B-style lay
 fp32 config with its named split 64, the bf16 360M layer, the 3B-style layer with an explicit
 split), so every call after the first runs on scratch an earlier call left behind. Each must
 match the oracle (the stated tolerance and, for bf16, the value-side bound) and the workspace
-entry point on the same inputs. A shape beyond the array's size is refused on the host. This
+entry point on the same inputs. A ragged batch of four then runs on the cluster kernel's plan
+on the same array. A shape beyond the array's size is refused on the host. This
 file is collected last so a run stopping at its first failure has already run every other
 test.
 """
@@ -65,6 +66,35 @@ def test_noalloc_matches_oracle_and_workspace_entry_point_in_a_row():
         torch.cuda.synchronize()
         assert_out_close(out.cpu(), ws_out.double().cpu().numpy(), dt, what=f"{what} vs workspace call")
         assert_lse_close(lse.cpu(), ws_lse.double().cpu().numpy(), what=f"{what} lse vs workspace call")
+
+
+def test_noalloc_batch_on_the_cluster_kernel():
+    """A ragged batch of four on the same array: the cluster kernel's plan (no partials in the
+    scratch, only its counter area), against the oracle and the workspace entry point."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from decode_attention_split_gb300 import _lib, build
+    build.build()
+    import decode_attention_split_gb300 as td
+    from decode_attention_split_gb300.workloads import small_case
+    lib = _lib.lib()
+    lens = [2048, 1000, 77, 1900]
+    assert td.td_split_plan(torch.bfloat16, 4, 24, 8, 2048, 128, 1, 0)["kernel"] == "tensor_core_cluster"
+    case = small_case(dtype="bf16", B=4, Hq=24, Hkv=8, D=128, Smax=2048, seq_lens=lens, seed=31, heavy=0.01)
+    q = case.q[:, :, 0].contiguous().cuda()
+    kc, vc, sl = case.k_cache.cuda(), case.v_cache.cuda(), case.seq_lens.cuda()
+    out = torch.full_like(q, float("nan"))
+    lse = torch.full(q.shape[:2], float("nan"), dtype=torch.float32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    assert _noalloc(lib, q, kc, vc, sl, case.scale, 0, out, lse, status) == 0
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    check_bf16_attention(out.cpu(), lse.cpu(), to_numpy(case.q[:, :, 0]), to_numpy(case.k_cache),
+                         to_numpy(case.v_cache), to_numpy(case.seq_lens), case.scale, what="cluster batch")
+    ws_out, ws_lse = td.td_decode_attn(q, kc, vc, sl, case.scale, 0, return_lse=True)
+    torch.cuda.synchronize()
+    assert_out_close(out.cpu(), ws_out.double().cpu().numpy(), "bf16", what="cluster batch vs workspace call")
+    assert_lse_close(lse.cpu(), ws_lse.double().cpu().numpy(), what="cluster batch lse vs workspace call")
 
 
 def test_noalloc_rejects_shapes_beyond_its_scratch():
