@@ -181,7 +181,7 @@ static __device__ void plan_items(const SplitParams &p, int *s_len, int *s_prefi
   // Per-thread segment sums of items, then a CTA-wide exclusive scan. With an automatic
   // chunk size, rounding each sequence's chunk count up can push the items past the grid,
   // leaving a second, mostly idle wave: then S grows, by the overshoot and by at least enough
-  // to take one chunk off the longest sequence, and the scan is redone (a few rounds at
+  // to take one chunk off the longest sequence, and the scan is redone (a few passes at
   // most; it cannot fit once every nonempty sequence is down to one chunk per unit).
   for (int round = 0;; ++round) {
     int seg = 0;
@@ -299,7 +299,7 @@ __device__ void merge_group(const SplitParams &p, float *smem_f, int smem_floats
   const int BF = part_block_floats(R, D);
   const long long g = ((long long)b * p.Hkv + kvh) * p.RB + rb;
   const float *src = p.ws_part + g * p.ns_ws * (long long)BF;
-  float *acc = smem_f;          // [ROWS][D] running weighted sums (between rounds)
+  float *acc = smem_f;          // [ROWS][D] running weighted sums (between passes)
   float *st = acc + ROWS * D;   // M[ROWS], Lsum[ROWS], rescale[ROWS], 1 / Lsum[ROWS]
   float *fac = st + 4 * ROWS;   // [ROWS][kFB] factors 2^(m_c - M) of the staged chunks
   float *stage = fac + ROWS * kFB;
@@ -323,7 +323,7 @@ __device__ void merge_group(const SplitParams &p, float *smem_f, int smem_floats
       mbar_wait_bounded(smem_u32(bar), phase);  // one more bounded wait for the copy in flight
     }
     phase ^= 1u;
-    __syncthreads();  // staged blocks and the previous round's statistics are visible
+    __syncthreads();  // staged blocks and the previous pass's statistics are visible
     // per-row statistics of this block (base 2): a warp per row, lanes over chunks
 #pragma unroll 1
     for (int r = warp; r < nv; r += kWarps) {
@@ -362,7 +362,7 @@ __device__ void merge_group(const SplitParams &p, float *smem_f, int smem_floats
     }
     __syncthreads();
     // weighted sums, four dims per thread, over the staged chunks in four independent
-    // accumulators (chunk c into c % 4: a quarter of the dependent chain); in the last round
+    // accumulators (chunk c into c % 4: a quarter of the dependent chain); in the last pass
     // they are the output
 #pragma unroll 1
     for (int idx = tid; idx < nv * D4; idx += kThreads) {
