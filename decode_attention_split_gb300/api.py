@@ -10,6 +10,7 @@ and warm the call up once outside the capture.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import math
 import threading
@@ -54,6 +55,12 @@ def _cuda(*ts: torch.Tensor | None) -> torch.device:
         elif t.device != dev:
             raise ValueError("all tensors must be on one CUDA device")
     return dev
+
+
+def _on(dev: torch.device):
+    """The device guard a launch needs: none when `dev` is already the current device (the
+    common case, and a measurable share of a call's host time), else torch's."""
+    return contextlib.nullcontext() if torch.cuda.current_device() == dev.index else torch.cuda.device(dev)
 
 
 def _ptr(t: torch.Tensor | None):
@@ -126,7 +133,7 @@ def td_kv_append(k_new, v_new, k_cache, v_cache, seq_lens, advance: bool = True,
         raise TypeError("new rows and caches must share a dtype")
     if seq_lens.dtype != torch.int32 or seq_lens.shape != (B,):
         raise TypeError("seq_lens must be int32 [B]")
-    with torch.cuda.device(dev):
+    with _on(dev):
         st = lib().td_kv_append(_code(k_cache), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
                                 _ptr(seq_lens), B, Hkv, T, Smax, D, int(bool(advance)), _ptr(dev_status),
                                 _stream(stream, dev))
@@ -145,7 +152,7 @@ def _attn(name, q4, k_cache, v_cache, seq_lens, scale, split, out, lse, workspac
         raise TypeError("seq_lens must be int32 [B]")
     if scale is None:
         scale = 1.0 / math.sqrt(D)
-    with torch.cuda.device(dev):
+    with _on(dev):
         sp = _stream(stream, dev)
         if workspace is None:
             need = td_decode_workspace_bytes(B, Hq, Hkv, Smax, D, T, split)
@@ -214,7 +221,7 @@ def td_lse_merge(m, l, acc, seq_lens, split: int, out_dtype=torch.float32, out=N
         out = torch.empty(B, rows, D, dtype=out_dtype, device=acc.device)
     if lse is None and return_lse:
         lse = torch.empty(B, rows, dtype=torch.float32, device=acc.device)
-    with torch.cuda.device(dev):
+    with _on(dev):
         st = lib().td_lse_merge(_ptr(m), _ptr(l), _ptr(acc), _ptr(seq_lens), B, rows, NS, D, int(split), _code(out),
                                 _ptr(out), _ptr(lse), _stream(stream, dev))
     check("td_lse_merge", st)
@@ -255,7 +262,7 @@ def td_rope_kv_append(k_new, v_new, k_cache, v_cache, seq_lens, cos_t, sin_t, q=
             q_out = torch.empty_like(q)
         if q_out.shape != q.shape or q_out.dtype != q.dtype:
             raise TypeError("q_out must match q")
-    with torch.cuda.device(dev):
+    with _on(dev):
         st = lib().td_rope_kv_append(_code(k_cache), _ptr(q), _ptr(q_out), Hq, _ptr(k_new), _ptr(v_new), _ptr(cos_t),
                                      _ptr(sin_t), _ptr(k_cache), _ptr(v_cache), _ptr(seq_lens), B, Hkv, T, Smax, D,
                                      int(bool(advance)), _ptr(dev_status), _stream(stream, dev))
@@ -291,7 +298,7 @@ def td_rope_append_attn(q, k_new, v_new, k_cache, v_cache, seq_lens, scale: floa
         raise TypeError("lse must be float32 [B, Hq, T]")
     if out.shape != q.shape or out.dtype != q.dtype:
         raise TypeError("out must match q")
-    with torch.cuda.device(dev):
+    with _on(dev):
         sp = _stream(stream, dev)
         if workspace is None:
             need = td_decode_workspace_bytes(B, Hq, Hkv, Smax, D, T, split)
@@ -329,7 +336,7 @@ def td_spec_accept(target_logits, draft_tokens, draft_logits=None, uniforms=None
         n_accepted = torch.empty(B, dtype=torch.int32, device=target_logits.device)
     if next_token is None:
         next_token = torch.empty(B, dtype=torch.int32, device=target_logits.device)
-    with torch.cuda.device(dev):
+    with _on(dev):
         sp = _stream(stream, dev)
         if workspace is None:
             need = int(lib().td_spec_workspace_bytes(B, G, V))
@@ -353,7 +360,7 @@ def td_quantize_q8(x, codes=None, scales=None, stream=None):
         codes = torch.empty(x.shape, dtype=torch.int8, device=x.device)
     if scales is None:
         scales = torch.empty(x.shape[:-1], dtype=torch.float32, device=x.device)
-    with torch.cuda.device(dev):
+    with _on(dev):
         st = lib().td_quantize_q8(_code(x), _ptr(x), rows, D, _ptr(codes), _ptr(scales), _stream(stream, dev))
     check("td_quantize_q8", st)
     return codes, scales
@@ -369,7 +376,7 @@ def td_kv_append_q8(k_new, v_new, k_codes, k_scales, v_codes, v_scales, seq_lens
         raise TypeError("codes must be int8 [B, Hkv, Smax, D]")
     if k_scales.shape != (B, Hkv, Smax) or k_scales.dtype != torch.float32 or v_scales.shape != k_scales.shape:
         raise TypeError("scales must be float32 [B, Hkv, Smax]")
-    with torch.cuda.device(dev):
+    with _on(dev):
         st = lib().td_kv_append_q8(_code(k_new), _ptr(k_new), _ptr(v_new), _ptr(k_codes), _ptr(k_scales),
                                    _ptr(v_codes), _ptr(v_scales), _ptr(seq_lens), B, Hkv, T, Smax, D,
                                    int(bool(advance)), _ptr(dev_status), _stream(stream, dev))
@@ -392,7 +399,7 @@ def td_verify_attn_q8(q, k_codes, k_scales, v_codes, v_scales, seq_lens, scale: 
         out = torch.empty_like(q)
     if lse is None and return_lse:
         lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device)
-    with torch.cuda.device(dev):
+    with _on(dev):
         sp = _stream(stream, dev)
         if workspace is None:
             need = td_decode_workspace_bytes(B, Hq, Hkv, Smax, D, T, split)
@@ -434,7 +441,7 @@ def td_prefill_attn(q, k_cache, v_cache, seq_lens, scale: float | None = None, o
         out = torch.empty_like(q)
     if lse is None and return_lse:
         lse = torch.empty(B, Hq, T, dtype=torch.float32, device=q.device)
-    with torch.cuda.device(dev):
+    with _on(dev):
         st = lib().td_prefill_attn(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(seq_lens), B, Hq, Hkv, T, Smax, D,
                                    float(scale), _ptr(out), _ptr(lse), _ptr(dev_status), _stream(stream, dev))
     check("td_prefill_attn", st)
